@@ -1,0 +1,363 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 selected-attention backward (one JSON line on rank 0).
+
+A step is one full backward call (preprocess, index inversion, main kernel,
+dQ finish) on one synthetic batch of the chosen workload, inputs resident in
+HBM.  The default workload is the long-context one (B=1, S=32768, N1=64,
+N2=4, Dqk=192, Dv=128, bf16, 16 blocks of 64).  Its inputs (Q alone is
+805 MB) are larger than the 129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config I]
+                    [--deterministic] [--impl ours|reference]
+
+Under torchrun each rank runs its own independent problem (weak scaling, no
+collective on the data path); the time is the max over ranks.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "selected-attn backward TFLOP/s and % of GB300 bf16 roofline; ms per call"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, help="workload index (0..4)")
+    ap.add_argument("--deterministic", action="store_true")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "sparse_attention_backward_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, det: bool):
+    """DRAM bytes per launch of the main kernel from a committed ncu summary,
+    used only while the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    key = f"{workload}:{'deterministic' if det else 'default'}"
+    e = d.get(key)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                c = [x.strip() for x in line.split(",")]
+                if len(c) < 9:
+                    continue
+                try:
+                    sm.append(float(c[1]))
+                    mx.append(float(c[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, c[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- CPU oracle
+def _np16(t):
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def oracle_sample(w, x, n_tokens, rng):
+    """A bounded sample of the workload: n_tokens query tokens of batch 0 with
+    the G heads of KV head 0 against their batch's keys (a full backward of
+    those rows: dQ, and their dK / dV scatter)."""
+    import oracle
+    b, j, G = 0, 0, w.group
+    q0, q1 = w.cu_q[b], w.cu_q[b + 1]
+    toks = np.sort(rng.choice(np.arange(q0, q1), size=min(n_tokens, q1 - q0), replace=False))
+    t = torch.as_tensor(toks, device=x["q"].device)
+    k0, k1 = w.cu_kv[b], w.cu_kv[b + 1]
+    hs = slice(j * G, (j + 1) * G)
+    p = oracle.Problem(
+        cu_q=np.array([0, len(toks)], np.int32), cu_kv=np.array([0, k1 - k0], np.int32), n1=G, n2=1,
+        d_qk=w.d_qk, d_v=w.d_v, block_size=w.block_size, block_count=w.block_count, scale=w.scale,
+        topk=x["topk"][t][:, j:j + 1].cpu().numpy(), q=_np16(x["q"][t][:, hs]),
+        k=_np16(x["k"][k0:k1, j:j + 1]), v=_np16(x["v"][k0:k1, j:j + 1]), o=_np16(x["o"][t][:, hs]),
+        dy=_np16(x["dy"][t][:, hs]), smax=x["softmax_max"][t][:, hs].cpu().numpy(),
+        ssum=x["softmax_sum"][t][:, hs].cpu().numpy(), stat_stride=8, kind=w.dtype)
+    flops = 2.0 * w.selected_keys * (3 * w.d_qk + 2 * w.d_v) * len(toks) * G
+    return p, flops, len(toks)
+
+
+def time_oracle(w, x, budget_s, seed=0):
+    """TFLOP/s of the oracle on a sample sized to about budget_s seconds."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    p, f, n = oracle_sample(w, x, 1, rng)
+    t0 = time.perf_counter()
+    oracle.backward(p)
+    per_token = max(1e-4, time.perf_counter() - t0)
+    n = max(1, int(budget_s / per_token))
+    p, f, n = oracle_sample(w, x, n, rng)
+    t0 = time.perf_counter()
+    oracle.backward(p)
+    dt = time.perf_counter() - t0
+    return f / dt / 1e12, dt, n
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    x = synth.make_inputs(w, device="cpu" if w.t1 * w.n1 * w.d_qk < (1 << 27) else "cuda")
+    if "o" not in x:
+        x.update(synth.synthetic_forward_stats(w, torch.Generator(device=x["q"].device).manual_seed(w.seed + 7),
+                                               x["q"].device))
+    per_step = min(5.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_oracle(w, x, per_step)
+    vals, times = [], []
+    for s in range(args.steps):
+        v, dt, n = time_oracle(w, x, per_step, seed=s + 1)
+        vals.append(v)
+        times.append(dt)
+    value = statistics.median(vals)
+    sample = (f"{n} query tokens x {w.group} heads of KV head 0, batch 0 (full backward of those rows) "
+              f"per step, ~{per_step:.1f} s each")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, args.deterministic),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, det):
+    return {"workload": w.name, "batch": w.batch, "seq_len_q": [int(v) for v in np.diff(w.cu_q)[:4]] if w.batch <= 4 else "varlen",
+            "n1": w.n1, "n2": w.n2, "d_qk": w.d_qk, "d_v": w.d_v, "block_size": w.block_size,
+            "block_count": w.block_count, "dtype": w.dtype, "mode": "deterministic" if det else "default",
+            "l2": "inputs larger than L2 (129 MB): no flush between steps" if w.algorithmic_bytes() > 4 * 129e6
+            else "L2 flushed between steps (256 MB write)"}
+
+
+# --------------------------------------------------------------------- ours
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = synth.WORKLOADS[args.config]
+    if args.impl == "reference":
+        if world > 1 and rank != 0:
+            return
+        run_reference(args, w, rank, world)
+        return
+
+    import sparse_attention_backward_gb300 as sab
+    sab.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    x = synth.make_inputs(w, device=dev, seed=w.seed + rank)
+    if "o" not in x:   # workloads whose stats normally come from a forward
+        g = torch.Generator(device=dev).manual_seed(w.seed + 7 + rank)
+        x.update(synth.synthetic_forward_stats(w, g, dev))
+    stream = torch.cuda.current_stream(dev)
+    desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count,
+                         w.scale, sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, args.deterministic)
+    info = sab.plan_info(desc)
+    ws = torch.empty(int(info.workspace_bytes), dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
+    ins = [x[k] for k in ("q", "k", "v", "o", "dy", "softmax_max", "softmax_sum", "topk")]
+    flush = None
+    if w.algorithmic_bytes() <= 4 * 129e6:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def call(ev0=None, ev1=None):
+        sab.sel_attn_grad(desc, *[t.data_ptr() for t in ins], dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                          ws.data_ptr(), ws.numel(), stream.cuda_stream,
+                          ev0.cuda_event if ev0 is not None else None,
+                          ev1.cuda_event if ev1 is not None else None)
+
+    for _ in range(args.warmup):
+        call()
+    st = sab.query_error(ws.data_ptr(), stream.cuda_stream)
+    if st != sab.SAG_OK:
+        raise sab.SagError(st, "device")
+
+    K = args.steps
+    mk0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    mk1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in mk0 + mk1:
+        e.record(stream)   # creates the event so its handle can be passed down
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    t0.record(stream)
+    for i in range(K):
+        if flush is not None:
+            flush.zero_()
+        call(mk0[i], mk1[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t0.elapsed_time(t1) / K
+    main_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(mk0, mk1))
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    flops = w.flops()
+    value = flops * world / (ms * 1e-3) / 1e12
+    pk, pk_src = peaks()
+    peak = float(pk["bf16_tflops"])
+    roofline_ms = max(flops / (peak * 1e12), w.algorithmic_bytes() / (float(pk["hbm_gbs"]) * 1e9)) * 1e3
+    achieved = flops / (main_ms * 1e-3) / 1e12
+
+    # end to end through the C ABI with host buffers (pinned), copies timed
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.cpu().pin_memory() for t in ins]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def e2e_step():
+            for d, h in zip(ins, host_in):
+                d.copy_(h, non_blocking=True)
+            call()
+            for h, d in zip(host_out, (dq, dk, dv)):
+                h.copy_(d, non_blocking=True)
+        for _ in range(max(1, min(args.warmup, 3))):
+            e2e_step()
+        torch.cuda.synchronize()
+        ke = max(3, min(K, 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ems = a.elapsed_time(b) / ke
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": flops * world / (ems * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, n = time_oracle(w, x, args.cpu_seconds)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} query tokens x {w.group} heads (KV head 0, batch 0), full backward of those "
+                         f"rows, {dt:.1f} s on one host core"}
+
+    if rank == 0:
+        traffic = profiled_traffic(w.name, args.deterministic)
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": workload_config(w, args.deterministic),
+            "pct_of_roofline": 100.0 * roofline_ms / ms,
+            "roofline_ms": roofline_ms,
+            "roofline": {"bound": "tensor", "kernel": "main backward", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": f"{pk_src} bf16 burst",
+                         "kernel_ms": main_ms, "traffic": traffic},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(info.launches) * K,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,188 @@
+/*
+ * selattn.h -- C ABI of the GB300 selected-attention backward library
+ * (libselattn.so).
+ *
+ * The operation is the training backward of NSA-style selected attention as
+ * the "NsaSelectedAttentionGrad" README (ops-transformer) defines it:
+ *
+ *   function description: for every query token and KV head, gather
+ *     selectedBlockCount blocks of selectedBlockSize key / value rows named by
+ *     topkIndices (selectedKey = Gather(key, topkIndices[i])), then run the
+ *     attention backward over the gathered rows:
+ *         dV = P^T dY,   dQ = dS K / sqrt(d),   dK = dS^T Q / sqrt(d)
+ *     with dK and dV scatter-added back to the gathered key rows;
+ *   parameters: query, key, value, attentionOut, attentionOutGrad (bf16 or
+ *     fp16), softmaxMax and softmaxSum (fp32 forward intermediates),
+ *     topkIndices (int32), scaleValue (double, the 1/sqrt(d) of the formula);
+ *     outputs dqOut, dkOut, dvOut in the input dtype;
+ *   constraints: TND layout, N1 a multiple of N2 with G = N1/N2 in [1, 32],
+ *     D in {128, 192}, block size a multiple of 16 and <= 128, block count in
+ *     [1, 128], count * size < 8192, per-batch S2 a multiple of the block size
+ *     and at least count * size, stats [T1, N1, 8], topkIndices
+ *     [T1, N2, selectedBlockCount].
+ *
+ * With P = exp(scale * Q K_sel^T - lse), lse = softmaxMax + ln(softmaxSum)
+ * (lane 0 of the 8), Delta = rowsum(dY * O) and dS = P * (dY V_sel^T - Delta)
+ * (the softmax adjoint behind the dense formulas of the
+ * "aclnnFlashAttentionUnpaddingScoreGradV3" page).
+ *
+ * The calling convention is the two-phase one those pages describe: phase 1
+ * validates the parameters and returns the workspace size; phase 2 takes the
+ * caller's workspace and a stream and enqueues the work.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers, 16-byte aligned, densely packed
+ *     in TND order (row-major, last dimension contiguous).  cu_seqlens_* in
+ *     the descriptor are HOST arrays.
+ *   - The caller owns every buffer, including the workspace.  The library
+ *     allocates no memory and keeps no state between calls.
+ *   - Inputs are never written.  dq, dk and dv are fully overwritten; key rows
+ *     that no query selected get dK = dV = 0.
+ *   - Host-side problems are reported synchronously, before anything is
+ *     enqueued.  Problems found by the device (a block id out of range, a
+ *     bounded wait that ran out) are recorded in the workspace and read back
+ *     with sel_attn_grad_query_error.
+ */
+#ifndef SELATTN_H
+#define SELATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sag_status {
+    SAG_OK = 0,
+    SAG_ERR_NULL = 1,        /* a required pointer (or the descriptor) is NULL */
+    SAG_ERR_SHAPE = 2,       /* a size or length outside the constraints */
+    SAG_ERR_DTYPE = 3,       /* dtype is neither SAG_BF16 nor SAG_FP16 */
+    SAG_ERR_UNSUPPORTED = 4, /* allowed by the constraints but not built here */
+    SAG_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than phase 1 said */
+    SAG_ERR_ALIGN = 6,       /* a device pointer is not 16-byte aligned */
+    SAG_ERR_CUDA = 7,        /* a CUDA runtime call or launch failed */
+    SAG_ERR_INDEX = 8,       /* device: a topkIndices entry outside [0, S2_b / block_size) */
+    SAG_ERR_TIMEOUT = 9      /* device: a bounded wait in a kernel ran out */
+} sag_status;
+
+typedef enum sag_dtype { SAG_BF16 = 0, SAG_FP16 = 1 } sag_dtype;
+
+/*
+ * Problem descriptor.
+ *   batch          B >= 1
+ *   cu_seqlens_q   host int32[B+1]: query prefix sums, [0] = 0, [B] = T1.  A
+ *                  batch may have no query tokens.
+ *   cu_seqlens_kv  host int32[B+1]: key prefix sums, [0] = 0, [B] = T2; every
+ *                  batch's S2 is a multiple of block_size and >= block_size *
+ *                  block_count.
+ *   n1, n2         query heads and key/value heads (N1 % N2 == 0, N1/N2 <= 32)
+ *   d_qk, d_v      head dims of query/key and of value/attentionOut/dY
+ *                  (each 128 or 192)
+ *   block_size     selectedBlockSize (multiple of 16, <= 128)
+ *   block_count    selectedBlockCount (1..128, block_size * block_count < 8192)
+ *   scale          scaleValue
+ *   dtype          sag_dtype of query, key, value, attentionOut, dY, dq, dk, dv
+ *   deterministic  0: default mode (dQ reduced with fp32 atomics, results may
+ *                  differ in the last bits between runs); 1: every output is
+ *                  bit-identical run to run
+ */
+typedef struct sag_desc {
+    int32_t batch;
+    int32_t n1, n2;
+    int32_t d_qk, d_v;
+    int32_t block_size, block_count;
+    int32_t dtype;
+    int32_t deterministic;
+    int32_t reserved_;   /* must be 0 */
+    double scale;
+    const int32_t *cu_seqlens_q;
+    const int32_t *cu_seqlens_kv;
+} sag_desc;
+
+/*
+ * Phase 1.  Validates the descriptor against the constraints (host only, no
+ * CUDA call) and writes the workspace size in bytes the problem needs.
+ * Returns SAG_OK, SAG_ERR_NULL, SAG_ERR_SHAPE, SAG_ERR_DTYPE or
+ * SAG_ERR_UNSUPPORTED.
+ */
+sag_status sel_attn_grad_workspace_size(const sag_desc *desc, size_t *workspace_bytes);
+
+/*
+ * Phase 2.  Enqueues the whole backward on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and returns without waiting.
+ *   query               [T1, n1, d_qk]   dtype
+ *   key                 [T2, n2, d_qk]   dtype
+ *   value               [T2, n2, d_v]    dtype
+ *   attention_out       [T1, n1, d_v]    dtype (required: Delta needs it)
+ *   attention_out_grad  [T1, n1, d_v]    dtype
+ *   softmax_max         [T1, n1, 8]      fp32 (lane 0 is read)
+ *   softmax_sum         [T1, n1, 8]      fp32 (lane 0 is read)
+ *   topk_indices        [T1, n2, block_count] int32, block ids local to the
+ *                       token's batch
+ *   dq                  [T1, n1, d_qk]   dtype, written
+ *   dk                  [T2, n2, d_qk]   dtype, written
+ *   dv                  [T2, n2, d_v]    dtype, written
+ *   workspace           device scratch of at least the phase-1 size; its
+ *                       contents are undefined between calls and two calls in
+ *                       flight at once must not share it
+ * Returns SAG_OK once enqueued, or a host-side status (nothing enqueued), or
+ * SAG_ERR_CUDA when a launch failed.
+ */
+sag_status sel_attn_grad(const sag_desc *desc, const void *query, const void *key,
+                         const void *value, const void *attention_out,
+                         const void *attention_out_grad, const float *softmax_max,
+                         const float *softmax_sum, const int32_t *topk_indices, void *dq,
+                         void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/*
+ * Waits for `stream` and returns the status the device recorded in
+ * `workspace` during the last sel_attn_grad on it: SAG_OK, SAG_ERR_INDEX
+ * (the offending selections were skipped; outputs are not meaningful) or
+ * SAG_ERR_TIMEOUT.  SAG_ERR_CUDA if the wait or the read fails.
+ */
+sag_status sel_attn_grad_query_error(const void *workspace, void *stream);
+
+/*
+ * Launch plan of a problem (host only, no CUDA call): what sel_attn_grad will
+ * enqueue for `desc`.
+ *   workspace_bytes   same value as sel_attn_grad_workspace_size
+ *   launches          kernels one call launches (memsets and copies excluded)
+ *   items             key blocks (batch, KV head, block id) the work is split into
+ *   token_chunks      query-token chunks the deterministic mode runs in (1 otherwise)
+ *   main_kernel       0: CUDA-core kernel, 1: tensor-core (tcgen05) kernel
+ */
+typedef struct sag_plan_info {
+    uint64_t workspace_bytes;
+    int32_t launches;
+    int32_t token_chunks;
+    int64_t items;
+    int32_t main_kernel;
+    int32_t reserved_;
+} sag_plan_info;
+
+sag_status sel_attn_grad_plan_info(const sag_desc *desc, sag_plan_info *info);
+
+/*
+ * sel_attn_grad with two optional cudaEvent_t handles (NULL = not recorded):
+ * main_start is recorded on `stream` just before the first launch of the main
+ * backward kernel and main_stop just after its last one, so a caller can time
+ * the dominant kernel alone with cudaEventElapsedTime.  Arguments, ownership
+ * and errors are those of sel_attn_grad.
+ */
+sag_status sel_attn_grad_timed(const sag_desc *desc, const void *query, const void *key,
+                               const void *value, const void *attention_out,
+                               const void *attention_out_grad, const float *softmax_max,
+                               const float *softmax_sum, const int32_t *topk_indices, void *dq,
+                               void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                               void *stream, void *main_start, void *main_stop);
+
+/* Static, human-readable name of a status code. */
+const char *sel_attn_grad_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SELATTN_H */

@@ -72,10 +72,14 @@ def _load():
         P = ctypes.POINTER(_Problem)
         dp = ctypes.c_void_p
         lib.sao_forward.argtypes = [P, dp, dp, dp]
+        lib.sao_forward_rows.argtypes = [P, ctypes.c_int64, dp, dp, dp, dp]
         lib.sao_backward.argtypes = [P, dp, dp, dp]
         lib.sao_dq_rows.argtypes = [P, ctypes.c_int64, dp, dp]
         lib.sao_dkdv_block.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, dp, dp]
-        for f in (lib.sao_forward, lib.sao_backward, lib.sao_dq_rows, lib.sao_dkdv_block):
+        lib.sao_dkdv_block_range.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int64, ctypes.c_int64, dp, dp]
+        for f in (lib.sao_forward, lib.sao_forward_rows, lib.sao_backward, lib.sao_dq_rows, lib.sao_dkdv_block,
+                  lib.sao_dkdv_block_range):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -194,6 +198,19 @@ def forward(p: Problem):
     return o, m, l
 
 
+def forward_rows(p: Problem, rows_th):
+    """Forward of the rows rows_th[i] = t * n1 + h: o [n, d_v], m [n], l [n]."""
+    lib = _load()
+    rows = np.ascontiguousarray(np.asarray(rows_th, dtype=np.int64))
+    o = np.zeros((len(rows), p.d_v))
+    m = np.zeros(len(rows))
+    l = np.zeros(len(rows))
+    c = p._c()
+    _check(lib.sao_forward_rows(ctypes.byref(c), len(rows), rows.ctypes.data, o.ctypes.data,
+                                m.ctypes.data, l.ctypes.data), "forward_rows")
+    return o, m, l
+
+
 def backward(p: Problem):
     """Full fp64 (dq, dk, dv)."""
     lib = _load()
@@ -222,4 +239,15 @@ def dkdv_block(p: Problem, b: int, n2: int, kb: int):
     dv = np.zeros((p.block_size, p.d_v))
     c = p._c()
     _check(lib.sao_dkdv_block(ctypes.byref(c), b, n2, kb, dk.ctypes.data, dv.ctypes.data), "dkdv_block")
+    return dk, dv
+
+
+def dkdv_block_range(p: Problem, b: int, n2: int, kb: int, t_lo: int, t_hi: int):
+    """Contribution of query tokens [t_lo, t_hi) of batch b to key block kb."""
+    lib = _load()
+    dk = np.zeros((p.block_size, p.d_qk))
+    dv = np.zeros((p.block_size, p.d_v))
+    c = p._c()
+    _check(lib.sao_dkdv_block_range(ctypes.byref(c), b, n2, kb, t_lo, t_hi, dk.ctypes.data,
+                                    dv.ctypes.data), "dkdv_block_range")
     return dk, dv

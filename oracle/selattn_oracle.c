@@ -186,37 +186,66 @@ static double score_of(const sao_problem *p, int64_t t, int h, int n2, int64_t r
  *   m = max_j s_j,  l = sum_j exp(s_j - m),  O = sum_j exp(s_j - m)/l * v_j
  * Outputs: o [T1, n1, d_v], m and l [T1, n1] (one value per row).
  */
+/* forward of one row (t, h) of batch b into o_row[d_v], *m, *l */
+static int row_forward(const sao_problem *p, int b, int64_t t, int h, int64_t *rows, double *s,
+                       double *o_row, double *m_out, double *l_out)
+{
+    int G = p->n1 / p->n2;
+    int n2 = h / G;
+    int64_t L = (int64_t)p->block_count * p->block_size;
+    int rc = gather_rows(p, b, t, n2, rows);
+    if (rc) return rc;
+    for (int64_t j = 0; j < L; ++j) s[j] = score_of(p, t, h, n2, rows[j]);
+    double m = -INFINITY;
+    for (int64_t j = 0; j < L; ++j) if (s[j] > m) m = s[j];
+    double l = 0.0;
+    for (int64_t j = 0; j < L; ++j) l += exp(s[j] - m);
+    for (int d = 0; d < p->d_v; ++d) o_row[d] = 0.0;
+    for (int64_t j = 0; j < L; ++j) {
+        double pj = exp(s[j] - m) / l;
+        int64_t voff = (rows[j] * p->n2 + n2) * p->d_v;
+        for (int d = 0; d < p->d_v; ++d) o_row[d] += pj * ld(&p->v, voff + d);
+    }
+    *m_out = m;
+    *l_out = l;
+    return SAO_OK;
+}
+
 int sao_forward(const sao_problem *p, double *o, double *m_out, double *l_out)
 {
     int rc = check_problem(p);
     if (rc) return rc;
     int64_t L = (int64_t)p->block_count * p->block_size;
-    int G = p->n1 / p->n2;
     int64_t *rows = malloc(sizeof(int64_t) * L);
     double *s = malloc(sizeof(double) * L);
     if (!rows || !s) { free(rows); free(s); return SAO_ENOMEM; }
-    for (int b = 0; b < p->batch && rc == SAO_OK; ++b) {
-        for (int64_t t = p->cu_q[b]; t < p->cu_q[b + 1] && rc == SAO_OK; ++t) {
-            for (int h = 0; h < p->n1; ++h) {
-                int n2 = h / G;
-                rc = gather_rows(p, b, t, n2, rows);
-                if (rc) break;
-                for (int64_t j = 0; j < L; ++j) s[j] = score_of(p, t, h, n2, rows[j]);
-                double m = -INFINITY;
-                for (int64_t j = 0; j < L; ++j) if (s[j] > m) m = s[j];
-                double l = 0.0;
-                for (int64_t j = 0; j < L; ++j) l += exp(s[j] - m);
-                double *orow = o + ((int64_t)t * p->n1 + h) * p->d_v;
-                for (int d = 0; d < p->d_v; ++d) orow[d] = 0.0;
-                for (int64_t j = 0; j < L; ++j) {
-                    double pj = exp(s[j] - m) / l;
-                    int64_t voff = (rows[j] * p->n2 + n2) * p->d_v;
-                    for (int d = 0; d < p->d_v; ++d) orow[d] += pj * ld(&p->v, voff + d);
-                }
-                m_out[(int64_t)t * p->n1 + h] = m;
-                l_out[(int64_t)t * p->n1 + h] = l;
+    for (int b = 0; b < p->batch && rc == SAO_OK; ++b)
+        for (int64_t t = p->cu_q[b]; t < p->cu_q[b + 1] && rc == SAO_OK; ++t)
+            for (int h = 0; h < p->n1 && rc == SAO_OK; ++h) {
+                int64_t r = (int64_t)t * p->n1 + h;
+                rc = row_forward(p, b, t, h, rows, s, o + r * p->d_v, m_out + r, l_out + r);
             }
-        }
+    free(rows);
+    free(s);
+    return rc;
+}
+
+/* Forward of selected rows only: rows_th[i] = t * n1 + h; o is [nrows, d_v]. */
+int sao_forward_rows(const sao_problem *p, int64_t nrows, const int64_t *rows_th, double *o,
+                     double *m_out, double *l_out)
+{
+    int rc = check_problem(p);
+    if (rc) return rc;
+    int64_t L = (int64_t)p->block_count * p->block_size;
+    int64_t *rows = malloc(sizeof(int64_t) * L);
+    double *s = malloc(sizeof(double) * L);
+    if (!rows || !s) { free(rows); free(s); return SAO_ENOMEM; }
+    for (int64_t i = 0; i < nrows && rc == SAO_OK; ++i) {
+        int64_t t = rows_th[i] / p->n1;
+        int h = (int)(rows_th[i] % p->n1);
+        int b = batch_of_token(p, t);
+        if (b < 0) { rc = SAO_EARG; break; }
+        rc = row_forward(p, b, t, h, rows, s, o + i * p->d_v, m_out + i, l_out + i);
     }
     free(rows);
     free(s);
@@ -314,22 +343,26 @@ int sao_dq_rows(const sao_problem *p, int64_t nrows, const int64_t *rows_th, dou
 }
 
 /*
- * dK and dV of one key block (batch b, KV head n2, block id kb): every query
- * row of batch b whose list for n2 names kb contributes (once per naming).
- * dk_blk is [block_size, d_qk], dv_blk is [block_size, d_v].
+ * dK and dV of one key block (batch b, KV head n2, block id kb) from the query
+ * tokens t in [t_lo, t_hi) of batch b: every such row whose list for n2 names
+ * kb contributes (once per naming).  dk_blk is [block_size, d_qk], dv_blk is
+ * [block_size, d_v]; both are overwritten.
  */
-int sao_dkdv_block(const sao_problem *p, int b, int n2, int kb, double *dk_blk, double *dv_blk)
+int sao_dkdv_block_range(const sao_problem *p, int b, int n2, int kb, int64_t t_lo, int64_t t_hi,
+                         double *dk_blk, double *dv_blk)
 {
     int rc = check_problem(p);
     if (rc) return rc;
     if (b < 0 || b >= p->batch || n2 < 0 || n2 >= p->n2 || kb < 0) return SAO_EARG;
+    if (t_lo < p->cu_q[b]) t_lo = p->cu_q[b];
+    if (t_hi > p->cu_q[b + 1]) t_hi = p->cu_q[b + 1];
     int G = p->n1 / p->n2;
     int64_t L = (int64_t)p->block_count * p->block_size;
     memset(dk_blk, 0, sizeof(double) * p->block_size * p->d_qk);
     memset(dv_blk, 0, sizeof(double) * p->block_size * p->d_v);
     int64_t *rows = malloc(sizeof(int64_t) * L);
     if (!rows) return SAO_ENOMEM;
-    for (int64_t t = p->cu_q[b]; t < p->cu_q[b + 1] && rc == SAO_OK; ++t) {
+    for (int64_t t = t_lo; t < t_hi && rc == SAO_OK; ++t) {
         const int32_t *ids = p->topk + ((int64_t)t * p->n2 + n2) * p->block_count;
         int hit = 0;
         for (int i = 0; i < p->block_count; ++i) hit |= ids[i] == kb;
@@ -339,4 +372,11 @@ int sao_dkdv_block(const sao_problem *p, int b, int n2, int kb, double *dk_blk, 
     }
     free(rows);
     return rc;
+}
+
+/* dK and dV of one key block from all query tokens of its batch. */
+int sao_dkdv_block(const sao_problem *p, int b, int n2, int kb, double *dk_blk, double *dv_blk)
+{
+    if (!p || b < 0 || b >= p->batch) return SAO_EARG;
+    return sao_dkdv_block_range(p, b, n2, kb, p->cu_q[b], p->cu_q[b + 1], dk_blk, dv_blk);
 }

@@ -1,0 +1,182 @@
+"""GB300 (sm_103a) selected-attention backward: thin Python binding.
+
+Every step of the backward runs in the CUDA kernels of ``libselattn.so``; this
+module only marshals arguments into its C ABI (``include/selattn.h``) with
+ctypes.  PyTorch is used for device memory and streams.  There is no CPU path:
+if the library is missing, importing the binding's entry points raises.
+
+    import sparse_attention_backward_gb300 as sab
+    dq, dk, dv = sab.backward(q, k, v, o, dy, softmax_max, softmax_sum, topk,
+                              cu_seqlens_q, cu_seqlens_kv, scale,
+                              block_size, block_count, deterministic=False)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libselattn.so")
+
+SAG_OK, SAG_ERR_NULL, SAG_ERR_SHAPE, SAG_ERR_DTYPE, SAG_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
+SAG_ERR_WORKSPACE, SAG_ERR_ALIGN, SAG_ERR_CUDA, SAG_ERR_INDEX, SAG_ERR_TIMEOUT = 5, 6, 7, 8, 9
+SAG_BF16, SAG_FP16 = 0, 1
+
+EXPORTED = ("sel_attn_grad_workspace_size", "sel_attn_grad", "sel_attn_grad_timed",
+            "sel_attn_grad_plan_info", "sel_attn_grad_query_error", "sel_attn_grad_status_string")
+
+
+class SagDesc(ctypes.Structure):
+    """Mirror of ``sag_desc`` in include/selattn.h."""
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("n1", ctypes.c_int32), ("n2", ctypes.c_int32),
+        ("d_qk", ctypes.c_int32), ("d_v", ctypes.c_int32),
+        ("block_size", ctypes.c_int32), ("block_count", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("deterministic", ctypes.c_int32), ("reserved_", ctypes.c_int32),
+        ("scale", ctypes.c_double),
+        ("cu_seqlens_q", ctypes.POINTER(ctypes.c_int32)),
+        ("cu_seqlens_kv", ctypes.POINTER(ctypes.c_int32)),
+    ]
+
+
+class SagPlanInfo(ctypes.Structure):
+    """Mirror of ``sag_plan_info`` in include/selattn.h."""
+    _fields_ = [("workspace_bytes", ctypes.c_uint64), ("launches", ctypes.c_int32),
+                ("token_chunks", ctypes.c_int32), ("items", ctypes.c_int64),
+                ("main_kernel", ctypes.c_int32), ("reserved_", ctypes.c_int32)]
+
+
+class SagError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libselattn.so (built by ``build.py``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} not found: build it with "
+                           "`python -m sparse_attention_backward_gb300.build`")
+    lib = ctypes.CDLL(path)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    D = ctypes.POINTER(SagDesc)
+    lib.sel_attn_grad_workspace_size.argtypes = [D, ctypes.POINTER(sz)]
+    lib.sel_attn_grad_workspace_size.restype = ctypes.c_int
+    lib.sel_attn_grad.argtypes = [D] + [vp] * 11 + [vp, sz, vp]
+    lib.sel_attn_grad.restype = ctypes.c_int
+    lib.sel_attn_grad_timed.argtypes = [D] + [vp] * 11 + [vp, sz, vp, vp, vp]
+    lib.sel_attn_grad_timed.restype = ctypes.c_int
+    lib.sel_attn_grad_plan_info.argtypes = [D, ctypes.POINTER(SagPlanInfo)]
+    lib.sel_attn_grad_plan_info.restype = ctypes.c_int
+    lib.sel_attn_grad_query_error.argtypes = [vp, vp]
+    lib.sel_attn_grad_query_error.restype = ctypes.c_int
+    lib.sel_attn_grad_status_string.argtypes = [ctypes.c_int]
+    lib.sel_attn_grad_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().sel_attn_grad_status_string(int(status)).decode()
+
+
+def make_desc(cu_seqlens_q, cu_seqlens_kv, n1, n2, d_qk, d_v, block_size, block_count, scale,
+              dtype=SAG_BF16, deterministic=False):
+    """Build a descriptor; keeps the host cu_seqlens arrays alive on the object."""
+    cq = (ctypes.c_int32 * len(cu_seqlens_q))(*[int(x) for x in cu_seqlens_q])
+    ck = (ctypes.c_int32 * len(cu_seqlens_kv))(*[int(x) for x in cu_seqlens_kv])
+    d = SagDesc(batch=len(cu_seqlens_q) - 1, n1=n1, n2=n2, d_qk=d_qk, d_v=d_v,
+                block_size=block_size, block_count=block_count, dtype=dtype,
+                deterministic=1 if deterministic else 0, reserved_=0, scale=float(scale),
+                cu_seqlens_q=ctypes.cast(cq, ctypes.POINTER(ctypes.c_int32)),
+                cu_seqlens_kv=ctypes.cast(ck, ctypes.POINTER(ctypes.c_int32)))
+    d._keep = (cq, ck)
+    return d
+
+
+def workspace_size(desc: SagDesc) -> int:
+    """Phase 1: validate and return the workspace size in bytes."""
+    n = ctypes.c_size_t(0)
+    st = load().sel_attn_grad_workspace_size(ctypes.byref(desc), ctypes.byref(n))
+    if st != SAG_OK:
+        raise SagError(st, "sel_attn_grad_workspace_size")
+    return n.value
+
+
+def plan_info(desc: SagDesc) -> SagPlanInfo:
+    """Launch plan of a problem (host only)."""
+    info = SagPlanInfo()
+    st = load().sel_attn_grad_plan_info(ctypes.byref(desc), ctypes.byref(info))
+    if st != SAG_OK:
+        raise SagError(st, "sel_attn_grad_plan_info")
+    return info
+
+
+def sel_attn_grad(desc: SagDesc, query, key, value, attention_out, attention_out_grad,
+                  softmax_max, softmax_sum, topk_indices, dq, dk, dv, workspace,
+                  workspace_bytes: int, stream, main_start=None, main_stop=None) -> None:
+    """Phase 2 on raw device pointers (ints); raises on a non-OK status.
+
+    ``main_start`` / ``main_stop`` are optional raw cudaEvent_t handles recorded
+    around the main backward kernel (``sel_attn_grad_timed``).
+    """
+    lib = load()
+    if main_start is None and main_stop is None:
+        st = lib.sel_attn_grad(ctypes.byref(desc), query, key, value, attention_out,
+                               attention_out_grad, softmax_max, softmax_sum, topk_indices,
+                               dq, dk, dv, workspace, workspace_bytes, stream)
+    else:
+        st = lib.sel_attn_grad_timed(ctypes.byref(desc), query, key, value, attention_out,
+                                     attention_out_grad, softmax_max, softmax_sum, topk_indices,
+                                     dq, dk, dv, workspace, workspace_bytes, stream, main_start,
+                                     main_stop)
+    if st != SAG_OK:
+        raise SagError(st, "sel_attn_grad")
+
+
+def query_error(workspace, stream) -> int:
+    """Wait for the stream; return the status the device recorded."""
+    return load().sel_attn_grad_query_error(workspace, stream)
+
+
+def backward(q, k, v, o, dy, softmax_max, softmax_sum, topk, cu_seqlens_q, cu_seqlens_kv, scale,
+             block_size, block_count, deterministic=False, out=None, workspace=None, stream=None,
+             check=False):
+    """torch-tensor convenience over the C ABI (allocation and marshalling only).
+
+    All tensors must be CUDA tensors in TND layout; returns (dq, dk, dv).  With
+    ``check`` the device status is read back (this synchronizes the stream).
+    """
+    import torch
+    if not q.is_cuda:
+        raise ValueError("inputs must be CUDA tensors (there is no CPU path)")
+    dtype = SAG_FP16 if q.dtype == torch.float16 else SAG_BF16
+    t1, n1, d_qk = q.shape
+    _, n2, d_v = v.shape
+    desc = make_desc(cu_seqlens_q, cu_seqlens_kv, n1, n2, d_qk, d_v, block_size, block_count, scale,
+                     dtype, deterministic)
+    need = workspace_size(desc)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    dq, dk, dv = out
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    tensors = (q, k, v, o, dy, softmax_max, softmax_sum, topk, dq, dk, dv)
+    for t in tensors:
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    sel_attn_grad(desc, *[t.data_ptr() for t in tensors], workspace.data_ptr(), need,
+                  stream.cuda_stream)
+    if check:
+        st = query_error(workspace.data_ptr(), stream.cuda_stream)
+        if st != SAG_OK:
+            raise SagError(st, "device")
+    return dq, dk, dv

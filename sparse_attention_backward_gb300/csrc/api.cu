@@ -1,0 +1,295 @@
+// C ABI: parameter validation (phase 1), workspace carving and the launch
+// sequence (phase 2).  The parameter and shape rules follow the constraints
+// section of the "NsaSelectedAttentionGrad" README; the two-phase shape
+// follows the aclnn calling convention described on the same pages
+// (GetWorkspaceSize validates, the second call runs on a stream).
+#include <string.h>
+
+#include <vector>
+
+#include "kernels.cuh"
+
+namespace sag {
+
+namespace {
+
+constexpr int64_t kMaxTokens = 2LL * 1024 * 1024;     // T1, T2, B <= 2M
+constexpr int64_t kMaxSeq = 128LL * 1024;             // per-batch S <= 128K
+constexpr size_t kAlign = 256;
+// deterministic mode stores dS for at most this many bytes of query tokens at
+// once; larger problems run in token chunks
+constexpr int64_t kDsChunkBytes = 16LL << 30;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Plan {
+    Geometry g;
+    bool fp16, det;
+    // byte offsets inside the workspace
+    size_t o_hdr, o_cu_q, o_cu_kv, o_item_base, o_count, o_offset, o_cursor, o_scan, o_entries,
+        o_delta, o_lse2, o_dq_acc, o_ds, o_dkv, total;
+    int32_t chunk_tokens, n_chunks;
+    std::vector<int64_t> item_base;   // host copy, B+1
+};
+
+sag_status validate(const sag_desc *d) {
+    if (!d || !d->cu_seqlens_q || !d->cu_seqlens_kv) return SAG_ERR_NULL;
+    if (d->dtype != SAG_BF16 && d->dtype != SAG_FP16) return SAG_ERR_DTYPE;
+    if (d->reserved_ != 0 || (d->deterministic != 0 && d->deterministic != 1)) return SAG_ERR_SHAPE;
+    if (d->batch < 1 || d->batch > kMaxTokens) return SAG_ERR_SHAPE;
+    if (d->n1 < 1 || d->n1 > 128 || d->n2 < 1 || d->n2 > 128 || d->n1 % d->n2 != 0) return SAG_ERR_SHAPE;
+    if (d->n1 / d->n2 > 32) return SAG_ERR_SHAPE;
+    if ((d->d_qk != 128 && d->d_qk != 192) || (d->d_v != 128 && d->d_v != 192)) return SAG_ERR_SHAPE;
+    if (d->block_size < 16 || d->block_size > 128 || d->block_size % 16 != 0) return SAG_ERR_SHAPE;
+    if (d->block_count < 1 || d->block_count > 128) return SAG_ERR_SHAPE;
+    if ((int64_t)d->block_size * d->block_count >= 8192) return SAG_ERR_SHAPE;
+    if (!(d->scale == d->scale) || d->scale > 1e30 || d->scale < -1e30) return SAG_ERR_SHAPE;
+    const int32_t *cq = d->cu_seqlens_q, *ck = d->cu_seqlens_kv;
+    if (cq[0] != 0 || ck[0] != 0) return SAG_ERR_SHAPE;
+    const int64_t sel = (int64_t)d->block_size * d->block_count;
+    for (int b = 0; b < d->batch; ++b) {
+        const int64_t s1 = (int64_t)cq[b + 1] - cq[b];
+        const int64_t s2 = (int64_t)ck[b + 1] - ck[b];
+        if (s1 < 0 || s1 > kMaxSeq) return SAG_ERR_SHAPE;
+        if (s2 < sel || s2 > kMaxSeq || s2 % d->block_size != 0) return SAG_ERR_SHAPE;
+    }
+    const int64_t t1 = cq[d->batch], t2 = ck[d->batch];
+    if (t1 < 1 || t1 > kMaxTokens || t2 < 1 || t2 > kMaxTokens) return SAG_ERR_SHAPE;
+    return SAG_OK;
+}
+
+sag_status make_plan(const sag_desc *d, Plan *p) {
+    sag_status st = validate(d);
+    if (st != SAG_OK) return st;
+    Geometry &g = p->g;
+    g.batch = d->batch;
+    g.t1 = d->cu_seqlens_q[d->batch];
+    g.t2 = d->cu_seqlens_kv[d->batch];
+    g.n1 = d->n1;
+    g.n2 = d->n2;
+    g.group = d->n1 / d->n2;
+    g.d_qk = d->d_qk;
+    g.d_v = d->d_v;
+    g.block_size = d->block_size;
+    g.block_count = d->block_count;
+    g.scale = (float)d->scale;
+    g.scale_log2 = (float)(d->scale * 1.4426950408889634);
+    p->fp16 = d->dtype == SAG_FP16;
+    p->det = d->deterministic != 0;
+    p->item_base.assign(d->batch + 1, 0);
+    for (int b = 0; b < d->batch; ++b) {
+        const int64_t nblk = (d->cu_seqlens_kv[b + 1] - d->cu_seqlens_kv[b]) / d->block_size;
+        p->item_base[b + 1] = p->item_base[b] + nblk * d->n2;
+    }
+    g.n_items = p->item_base[d->batch];
+    if (g.n_items > max_scannable_items()) return SAG_ERR_UNSUPPORTED;
+
+    const int64_t rows = (int64_t)g.t1 * g.n1;
+    const int64_t sel = (int64_t)g.t1 * g.n2 * g.block_count;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
+    p->o_hdr = take(sizeof(WsHeader));
+    p->o_cu_q = take(sizeof(int32_t) * (g.batch + 1));
+    p->o_cu_kv = take(sizeof(int32_t) * (g.batch + 1));
+    p->o_item_base = take(sizeof(int64_t) * (g.batch + 1));
+    p->o_count = take(sizeof(int32_t) * (g.n_items + 1));
+    p->o_cursor = take(sizeof(int32_t) * g.n_items);
+    p->o_offset = take(sizeof(int32_t) * (g.n_items + 1));
+    p->o_scan = take(sizeof(int32_t) * scan_parts(g.n_items));
+    p->o_entries = take(sizeof(int32_t) * sel);
+    p->o_delta = take(sizeof(float) * rows);
+    p->o_lse2 = take(sizeof(float) * rows);
+    p->o_dq_acc = p->det ? o : take(sizeof(float) * rows * g.d_qk);
+    const int64_t ds_per_token = (int64_t)g.n2 * g.block_count * g.group * g.block_size * 2;
+    int64_t chunk = kDsChunkBytes / ds_per_token;
+    if (chunk < 1) chunk = 1;
+    if (chunk > g.t1) chunk = g.t1;
+    p->chunk_tokens = p->det ? (int32_t)chunk : g.t1;
+    p->n_chunks = p->det ? (int32_t)((g.t1 + chunk - 1) / chunk) : 1;
+    p->o_ds = p->det ? take((size_t)ds_per_token * chunk) : o;
+    p->o_dkv = p->n_chunks > 1 ? take(sizeof(float) * (int64_t)g.t2 * g.n2 * (g.d_qk + g.d_v)) : o;
+    g.tok_lo = 0;
+    g.tok_hi = g.t1;
+    g.chunked = p->n_chunks > 1;
+    p->total = o;
+    return SAG_OK;
+}
+
+Workspace carve(const Plan &p, void *base) {
+    char *c = static_cast<char *>(base);
+    Workspace w;
+    w.hdr = reinterpret_cast<WsHeader *>(c + p.o_hdr);
+    w.cu_q = reinterpret_cast<int32_t *>(c + p.o_cu_q);
+    w.cu_kv = reinterpret_cast<int32_t *>(c + p.o_cu_kv);
+    w.item_base = reinterpret_cast<int64_t *>(c + p.o_item_base);
+    w.count = reinterpret_cast<int32_t *>(c + p.o_count);
+    w.offset = reinterpret_cast<int32_t *>(c + p.o_offset);
+    w.cursor = reinterpret_cast<int32_t *>(c + p.o_cursor);
+    w.scan_part = reinterpret_cast<int32_t *>(c + p.o_scan);
+    w.entries = reinterpret_cast<int32_t *>(c + p.o_entries);
+    w.delta = reinterpret_cast<float *>(c + p.o_delta);
+    w.lse2 = reinterpret_cast<float *>(c + p.o_lse2);
+    w.dq_acc = p.det ? nullptr : reinterpret_cast<float *>(c + p.o_dq_acc);
+    w.ds = p.det ? reinterpret_cast<uint16_t *>(c + p.o_ds) : nullptr;
+    w.dkv_acc = p.n_chunks > 1 ? reinterpret_cast<float *>(c + p.o_dkv) : nullptr;
+    return w;
+}
+
+bool aligned16(const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; }
+
+int device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+    return sms;
+}
+
+}  // namespace
+}  // namespace sag
+
+using namespace sag;
+
+extern "C" sag_status sel_attn_grad_workspace_size(const sag_desc *desc, size_t *workspace_bytes) {
+    if (!workspace_bytes) return SAG_ERR_NULL;
+    Plan p;
+    sag_status st = make_plan(desc, &p);
+    if (st != SAG_OK) return st;
+    *workspace_bytes = p.total;
+    return SAG_OK;
+}
+
+namespace {
+int launches_of(const Plan &p) {
+    // preprocess, histogram, 3 scan passes, fill, sort
+    int n = 7;
+    if (!p.det) return n + 2;                        // main, cast dQ
+    return n + 2 * p.n_chunks + (p.n_chunks > 1);    // (main, dQ) per chunk, cast dK/dV
+}
+}  // namespace
+
+extern "C" sag_status sel_attn_grad_plan_info(const sag_desc *desc, sag_plan_info *info) {
+    if (!info) return SAG_ERR_NULL;
+    Plan p;
+    sag_status st = make_plan(desc, &p);
+    if (st != SAG_OK) return st;
+    info->workspace_bytes = p.total;
+    info->launches = launches_of(p);
+    info->token_chunks = p.n_chunks;
+    info->items = p.g.n_items;
+    info->main_kernel = 0;
+    info->reserved_ = 0;
+    return SAG_OK;
+}
+
+extern "C" sag_status sel_attn_grad(const sag_desc *desc, const void *query, const void *key,
+                                    const void *value, const void *attention_out,
+                                    const void *attention_out_grad, const float *softmax_max,
+                                    const float *softmax_sum, const int32_t *topk_indices, void *dq,
+                                    void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
+    return sel_attn_grad_timed(desc, query, key, value, attention_out, attention_out_grad, softmax_max,
+                               softmax_sum, topk_indices, dq, dk, dv, workspace, workspace_bytes, stream,
+                               nullptr, nullptr);
+}
+
+extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *query, const void *key,
+                                          const void *value, const void *attention_out,
+                                          const void *attention_out_grad, const float *softmax_max,
+                                          const float *softmax_sum, const int32_t *topk_indices, void *dq,
+                                          void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                                          void *stream, void *main_start, void *main_stop) {
+    cudaEvent_t ev0 = static_cast<cudaEvent_t>(main_start), ev1 = static_cast<cudaEvent_t>(main_stop);
+    Plan p;
+    sag_status st = make_plan(desc, &p);
+    if (st != SAG_OK) return st;
+    const void *ptrs[] = {query, key, value, attention_out, attention_out_grad, softmax_max,
+                          softmax_sum, topk_indices, dq, dk, dv};
+    for (const void *x : ptrs)
+        if (!x) return SAG_ERR_NULL;
+    if (!workspace) return SAG_ERR_WORKSPACE;
+    for (const void *x : ptrs)
+        if (!aligned16(x)) return SAG_ERR_ALIGN;
+    if (!aligned16(workspace)) return SAG_ERR_ALIGN;
+    if (workspace_bytes < p.total) return SAG_ERR_WORKSPACE;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Geometry &g = p.g;
+    Workspace ws = carve(p, workspace);
+    const int sms = device_sms();
+
+    // staged host metadata: cu_q, cu_kv, item_base (pageable source: the copy
+    // has consumed it by the time cudaMemcpyAsync returns)
+    std::vector<char> meta(p.o_count - p.o_cu_q, 0);
+    memcpy(meta.data() + (p.o_cu_q - p.o_cu_q), desc->cu_seqlens_q, sizeof(int32_t) * (g.batch + 1));
+    memcpy(meta.data() + (p.o_cu_kv - p.o_cu_q), desc->cu_seqlens_kv, sizeof(int32_t) * (g.batch + 1));
+    memcpy(meta.data() + (p.o_item_base - p.o_cu_q), p.item_base.data(), sizeof(int64_t) * (g.batch + 1));
+
+    cudaError_t e;
+    (void)e;
+    char *base = static_cast<char *>(workspace);
+    if ((e = cudaMemsetAsync(base + p.o_hdr, 0, sizeof(WsHeader), s)) != cudaSuccess) return SAG_ERR_CUDA;
+    if ((e = cudaMemcpyAsync(base + p.o_cu_q, meta.data(), meta.size(), cudaMemcpyHostToDevice, s)) !=
+        cudaSuccess)
+        return SAG_ERR_CUDA;
+    // count and cursor are adjacent: one memset
+    if ((e = cudaMemsetAsync(base + p.o_count, 0, p.o_offset - p.o_count, s)) != cudaSuccess) return SAG_ERR_CUDA;
+
+    if ((e = launch_preprocess(g, ws, attention_out, attention_out_grad, softmax_max, softmax_sum, p.fp16,
+                               !p.det, s, sms)) != cudaSuccess)
+        return SAG_ERR_CUDA;
+    if ((e = launch_inversion(g, ws, topk_indices, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
+    if (!p.det) {
+        if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return SAG_ERR_CUDA;
+        if ((e = launch_bwd_simt(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s, sms)) !=
+            cudaSuccess)
+            return SAG_ERR_CUDA;
+        if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SAG_ERR_CUDA;
+        if ((e = launch_cast(ws.dq_acc, dq, (int64_t)g.t1 * g.n1 * g.d_qk, g.scale, p.fp16, s, sms)) !=
+            cudaSuccess)
+            return SAG_ERR_CUDA;
+        return SAG_OK;
+    }
+    // deterministic: token chunks in order; dS of a chunk -> its dQ
+    if (g.chunked && cudaMemsetAsync(ws.dkv_acc, 0, sizeof(float) * (size_t)g.t2 * g.n2 * (g.d_qk + g.d_v), s) !=
+                         cudaSuccess)
+        return SAG_ERR_CUDA;
+    if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return SAG_ERR_CUDA;
+    for (int c = 0; c < p.n_chunks; ++c) {
+        Geometry gc = g;
+        gc.tok_lo = c * p.chunk_tokens;
+        gc.tok_hi = gc.tok_lo + p.chunk_tokens < g.t1 ? gc.tok_lo + p.chunk_tokens : g.t1;
+        if ((e = launch_bwd_simt(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s, sms)) !=
+            cudaSuccess)
+            return SAG_ERR_CUDA;
+        if ((e = launch_dq_from_ds(gc, ws, key, topk_indices, dq, p.fp16, s, sms)) != cudaSuccess)
+            return SAG_ERR_CUDA;
+    }
+    if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SAG_ERR_CUDA;
+    if (g.chunked && (e = launch_cast_dkv(g, ws, dk, dv, p.fp16, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
+    return SAG_OK;
+}
+
+extern "C" sag_status sel_attn_grad_query_error(const void *workspace, void *stream) {
+    if (!workspace) return SAG_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SAG_ERR_CUDA;
+    int32_t code = 0;
+    if (cudaMemcpy(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) return SAG_ERR_CUDA;
+    return static_cast<sag_status>(code);
+}
+
+extern "C" const char *sel_attn_grad_status_string(int status) {
+    switch (status) {
+    case SAG_OK: return "ok";
+    case SAG_ERR_NULL: return "a required pointer is NULL";
+    case SAG_ERR_SHAPE: return "a size or length is outside the operator's constraints";
+    case SAG_ERR_DTYPE: return "dtype must be bf16 or fp16";
+    case SAG_ERR_UNSUPPORTED: return "allowed by the constraints but not supported by this build";
+    case SAG_ERR_WORKSPACE: return "workspace missing or smaller than the phase-1 size";
+    case SAG_ERR_ALIGN: return "a device pointer is not 16-byte aligned";
+    case SAG_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case SAG_ERR_INDEX: return "a topkIndices entry is outside its batch's block range";
+    case SAG_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    default: return "unknown status";
+    }
+}

@@ -1,0 +1,29 @@
+// Launchers of the library's kernels (host side).
+#pragma once
+
+#include "common.cuh"
+
+namespace sag {
+
+cudaError_t launch_preprocess(const Geometry &g, const Workspace &ws, const void *o, const void *dy,
+                              const float *smax, const float *ssum, bool fp16, bool zero_dq,
+                              cudaStream_t s, int num_sms);
+cudaError_t launch_inversion(const Geometry &g, const Workspace &ws, const int32_t *topk, cudaStream_t s,
+                             int num_sms);
+cudaError_t launch_cast(const float *in, void *out, int64_t n, float mul, bool fp16, cudaStream_t s,
+                        int num_sms);
+int scan_parts(int64_t n_items);
+int64_t max_scannable_items();
+
+// CUDA-core key-block-major backward (any supported shape).
+cudaError_t launch_bwd_simt(const Geometry &g, const Workspace &ws, const void *q, const void *k,
+                            const void *v, const void *dy, void *dk, void *dv, bool fp16,
+                            bool deterministic, cudaStream_t s, int num_sms);
+// dK/dV from the fp32 accumulator after the last token chunk.
+cudaError_t launch_cast_dkv(const Geometry &g, const Workspace &ws, void *dk, void *dv, bool fp16,
+                            cudaStream_t s, int num_sms);
+// dQ from the stored dS, fixed order (deterministic mode).
+cudaError_t launch_dq_from_ds(const Geometry &g, const Workspace &ws, const void *k,
+                              const int32_t *topk, void *dq, bool fp16, cudaStream_t s, int num_sms);
+
+}  // namespace sag

@@ -1,0 +1,331 @@
+// Preprocess, index inversion and cast kernels.
+//
+// Preprocess: Delta[t,h] = sum_d dY[t,h,d] * O[t,h,d] (the rowsum(dY * O) term
+// of dS = P * (dP - Delta)) and the log2-domain softmax constant
+// lse2 = (softmaxMax + ln softmaxSum) * log2(e), read from lane 0 of the
+// [T1, N1, 8] stats ("NsaSelectedAttentionGrad" README, parameters:
+// attentionOut, softmaxMax, softmaxSum).
+//
+// Inversion: topkIndices [T1, N2, count] names, per (token, KV head), the key
+// blocks its query rows attend to (README, Gather formula).  The backward
+// accumulates dK / dV per key block, so the lists are inverted into
+// key-block-major buckets: item = (batch, KV head, block id) -> the
+// (token, slot) pairs that selected it, in increasing token order
+// (histogram -> exclusive scan -> fill -> per-bucket sort, so the order does
+// not depend on atomic timing).
+#include "kernels.cuh"
+
+namespace sag {
+
+// ---------------------------------------------------------------------------
+// One warp per (t, h) row.  Also zeroes the fp32 dQ accumulator row when
+// zero_dq is set (default mode).
+template <bool kFp16>
+__global__ void __launch_bounds__(256) k_preprocess(Geometry g, const uint16_t *__restrict__ o,
+                                                    const uint16_t *__restrict__ dy,
+                                                    const float *__restrict__ smax,
+                                                    const float *__restrict__ ssum,
+                                                    float *__restrict__ delta,
+                                                    float *__restrict__ lse2,
+                                                    float *__restrict__ dq_acc, int zero_dq) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = (int64_t)g.t1 * g.n1;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r = warp0; r < rows; r += nwarps) {
+        const uint16_t *orow = o + r * g.d_v;
+        const uint16_t *yrow = dy + r * g.d_v;
+        float acc = 0.f;
+        // d_v is 128 or 192: lanes take 4 consecutive elements (8 bytes)
+        for (int d = lane * 4; d < g.d_v; d += 128) {
+            uint2 ov = *reinterpret_cast<const uint2 *>(orow + d);
+            uint2 yv = *reinterpret_cast<const uint2 *>(yrow + d);
+            const uint16_t *op = reinterpret_cast<const uint16_t *>(&ov);
+            const uint16_t *yp = reinterpret_cast<const uint16_t *>(&yv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc = fmaf(u16_to_f<kFp16>(yp[e]), u16_to_f<kFp16>(op[e]), acc);
+        }
+#pragma unroll
+        for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+        if (lane == 0) {
+            delta[r] = acc;
+            const float m = smax[r * 8];
+            const float l = ssum[r * 8];
+            lse2[r] = (m + logf(l)) * 1.4426950408889634f;
+        }
+        if (zero_dq) {
+            float4 *dst = reinterpret_cast<float4 *>(dq_acc + r * g.d_qk);
+            for (int d = lane; d < g.d_qk / 4; d += 32) dst[d] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Item of a selection, or -1 (and the error flag) when the block id is out of
+// its batch's range.
+__device__ __forceinline__ int64_t item_of(const Geometry &g, const Workspace &ws, int t, int n2,
+                                           int id, int *b_out) {
+    const int b = batch_of(ws.cu_q, g.batch, t);
+    const int nblk = (ws.cu_kv[b + 1] - ws.cu_kv[b]) / g.block_size;
+    *b_out = b;
+    if (id < 0 || id >= nblk) return -1;
+    return ws.item_base[b] + (int64_t)n2 * nblk + id;
+}
+
+__global__ void __launch_bounds__(256) k_histogram(Geometry g, Workspace ws,
+                                                   const int32_t *__restrict__ topk) {
+    const int64_t n = (int64_t)g.t1 * g.n2 * g.block_count;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / ((int64_t)g.n2 * g.block_count));
+        const int n2 = (int)((i / g.block_count) % g.n2);
+        int b;
+        const int64_t item = item_of(g, ws, t, n2, __ldg(topk + i), &b);
+        if (item < 0) { raise_error(&ws.hdr->error, SAG_ERR_INDEX); continue; }
+        atomicAdd(ws.count + item, 1);
+    }
+}
+
+// Exclusive scan of count[0..n) into offset[0..n] in three passes:
+// per-block sums, a single-block scan of those sums, per-block scans.
+constexpr int kScanBlock = 1024;
+constexpr int kScanPerThread = 4;
+constexpr int kScanTile = kScanBlock * kScanPerThread;
+
+__device__ __forceinline__ int block_exclusive_scan(int v, int *smem_warp, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, s);
+        if (lane >= s) x += y;
+    }
+    if (lane == 31) smem_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < (blockDim.x >> 5) ? smem_warp[lane] : 0;
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, w, s);
+            if (lane >= s) w += y;
+        }
+        smem_warp[lane] = w;
+    }
+    __syncthreads();
+    const int before = (warp ? smem_warp[warp - 1] : 0) + x - v;
+    *total = smem_warp[(blockDim.x >> 5) - 1];
+    __syncthreads();
+    return before;
+}
+
+__global__ void __launch_bounds__(kScanBlock) k_scan_partials(const int32_t *__restrict__ in,
+                                                              int64_t n, int32_t *__restrict__ part) {
+    __shared__ int warp_sums[32];
+    const int64_t base = (int64_t)blockIdx.x * kScanTile;
+    int v = 0;
+#pragma unroll
+    for (int e = 0; e < kScanPerThread; ++e) {
+        const int64_t i = base + (int64_t)threadIdx.x * kScanPerThread + e;
+        if (i < n) v += in[i];
+    }
+    int total;
+    block_exclusive_scan(v, warp_sums, &total);
+    if (threadIdx.x == 0) part[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(kScanBlock) k_scan_tops(int32_t *__restrict__ part, int nparts) {
+    __shared__ int warp_sums[32];
+    // nparts <= kScanTile (checked on the host): one tile
+    int v[kScanPerThread];
+    int sum = 0;
+#pragma unroll
+    for (int e = 0; e < kScanPerThread; ++e) {
+        const int i = threadIdx.x * kScanPerThread + e;
+        v[e] = i < nparts ? part[i] : 0;
+        sum += v[e];
+    }
+    int total;
+    int run = block_exclusive_scan(sum, warp_sums, &total);
+#pragma unroll
+    for (int e = 0; e < kScanPerThread; ++e) {
+        const int i = threadIdx.x * kScanPerThread + e;
+        if (i < nparts) part[i] = run;
+        run += v[e];
+    }
+}
+
+__global__ void __launch_bounds__(kScanBlock) k_scan_apply(const int32_t *__restrict__ in, int64_t n,
+                                                           const int32_t *__restrict__ part,
+                                                           int32_t *__restrict__ out) {
+    __shared__ int warp_sums[32];
+    const int64_t base = (int64_t)blockIdx.x * kScanTile;
+    int v[kScanPerThread];
+    int sum = 0;
+#pragma unroll
+    for (int e = 0; e < kScanPerThread; ++e) {
+        const int64_t i = base + (int64_t)threadIdx.x * kScanPerThread + e;
+        v[e] = i < n ? in[i] : 0;
+        sum += v[e];
+    }
+    int total;
+    int run = block_exclusive_scan(sum, warp_sums, &total) + part[blockIdx.x];
+#pragma unroll
+    for (int e = 0; e < kScanPerThread; ++e) {
+        const int64_t i = base + (int64_t)threadIdx.x * kScanPerThread + e;
+        if (i < n) out[i] = run;
+        run += v[e];
+    }
+    // offset[n] = grand total, written by the block holding element n-1
+    if (base <= n - 1 && n - 1 < base + kScanTile && threadIdx.x == 0) {
+        int grand = part[blockIdx.x] + total;
+        out[n] = grand;
+    }
+}
+
+__global__ void __launch_bounds__(256) k_fill(Geometry g, Workspace ws,
+                                              const int32_t *__restrict__ topk) {
+    const int64_t n = (int64_t)g.t1 * g.n2 * g.block_count;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / ((int64_t)g.n2 * g.block_count));
+        const int n2 = (int)((i / g.block_count) % g.n2);
+        const int slot = (int)(i % g.block_count);
+        int b;
+        const int64_t item = item_of(g, ws, t, n2, __ldg(topk + i), &b);
+        if (item < 0) continue;
+        const int pos = ws.offset[item] + atomicAdd(ws.cursor + item, 1);
+        ws.entries[pos] = t * g.block_count + slot;
+    }
+}
+
+// Sort each bucket ascending (token-major order).  Buckets of up to
+// kSortCap entries are sorted in shared memory (bitonic); larger ones by one
+// thread with heapsort in place (rare: needs more than kSortCap selections of
+// one key block).
+constexpr int kSortCap = 8192;
+
+__device__ void heap_sort_global(int32_t *a, int n) {
+    auto sift = [&](int root, int end) {
+        while (2 * root + 1 < end) {
+            int child = 2 * root + 1;
+            if (child + 1 < end && a[child] < a[child + 1]) ++child;
+            if (a[root] < a[child]) {
+                int tmp = a[root]; a[root] = a[child]; a[child] = tmp;
+                root = child;
+            } else {
+                return;
+            }
+        }
+    };
+    for (int s = n / 2 - 1; s >= 0; --s) sift(s, n);
+    for (int end = n - 1; end > 0; --end) {
+        int tmp = a[0]; a[0] = a[end]; a[end] = tmp;
+        sift(0, end);
+    }
+}
+
+__global__ void __launch_bounds__(512) k_sort_buckets(Geometry g, Workspace ws) {
+    __shared__ int32_t keys[kSortCap];
+    for (int64_t item = blockIdx.x; item < g.n_items; item += gridDim.x) {
+        const int off = ws.offset[item];
+        const int n = ws.offset[item + 1] - off;
+        if (n <= 1) continue;
+        int32_t *a = ws.entries + off;
+        if (n > kSortCap) {
+            if (threadIdx.x == 0) heap_sort_global(a, n);
+            __syncthreads();
+            continue;
+        }
+        int p2 = 1;
+        while (p2 < n) p2 <<= 1;
+        for (int i = threadIdx.x; i < p2; i += blockDim.x) keys[i] = i < n ? a[i] : INT32_MAX;
+        __syncthreads();
+        for (int k = 2; k <= p2; k <<= 1) {
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                for (int i = threadIdx.x; i < p2; i += blockDim.x) {
+                    const int l = i ^ j;
+                    if (l > i) {
+                        const int32_t x = keys[i], y = keys[l];
+                        const bool up = (i & k) == 0;
+                        if ((x > y) == up) { keys[i] = y; keys[l] = x; }
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        for (int i = threadIdx.x; i < n; i += blockDim.x) a[i] = keys[i];
+        __syncthreads();
+    }
+}
+
+// fp32 -> 16-bit, scaled (used for dQ in default mode).
+template <bool kFp16>
+__global__ void __launch_bounds__(256) k_cast(const float *__restrict__ in, uint16_t *__restrict__ out,
+                                              int64_t n4, float mul) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 v = reinterpret_cast<const float4 *>(in)[i];
+        ushort4 o;
+        o.x = f_to_u16<kFp16>(v.x * mul);
+        o.y = f_to_u16<kFp16>(v.y * mul);
+        o.z = f_to_u16<kFp16>(v.z * mul);
+        o.w = f_to_u16<kFp16>(v.w * mul);
+        reinterpret_cast<ushort4 *>(out)[i] = o;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers.
+static int grid_for(int64_t work, int per_block, int max_blocks) {
+    int64_t b = (work + per_block - 1) / per_block;
+    if (b < 1) b = 1;
+    if (b > max_blocks) b = max_blocks;
+    return (int)b;
+}
+
+cudaError_t launch_preprocess(const Geometry &g, const Workspace &ws, const void *o, const void *dy,
+                              const float *smax, const float *ssum, bool fp16, bool zero_dq,
+                              cudaStream_t s, int num_sms) {
+    const int64_t rows = (int64_t)g.t1 * g.n1;
+    const int grid = grid_for(rows, 8, num_sms * 16);
+    if (rows == 0) return cudaSuccess;
+    if (fp16)
+        k_preprocess<true><<<grid, 256, 0, s>>>(g, (const uint16_t *)o, (const uint16_t *)dy, smax, ssum,
+                                                ws.delta, ws.lse2, ws.dq_acc, zero_dq);
+    else
+        k_preprocess<false><<<grid, 256, 0, s>>>(g, (const uint16_t *)o, (const uint16_t *)dy, smax, ssum,
+                                                 ws.delta, ws.lse2, ws.dq_acc, zero_dq);
+    return cudaGetLastError();
+}
+
+int scan_parts(int64_t n_items) { return (int)((n_items + kScanTile - 1) / kScanTile); }
+int64_t max_scannable_items() { return (int64_t)kScanTile * kScanTile; }
+
+cudaError_t launch_inversion(const Geometry &g, const Workspace &ws, const int32_t *topk, cudaStream_t s,
+                             int num_sms) {
+    const int64_t sel = (int64_t)g.t1 * g.n2 * g.block_count;
+    if (sel > 0) {
+        k_histogram<<<grid_for(sel, 256, num_sms * 8), 256, 0, s>>>(g, ws, topk);
+    }
+    const int parts = scan_parts(g.n_items);
+    k_scan_partials<<<parts, kScanBlock, 0, s>>>(ws.count, g.n_items, ws.scan_part);
+    k_scan_tops<<<1, kScanBlock, 0, s>>>(ws.scan_part, parts);
+    k_scan_apply<<<parts, kScanBlock, 0, s>>>(ws.count, g.n_items, ws.scan_part, ws.offset);
+    if (sel > 0) {
+        k_fill<<<grid_for(sel, 256, num_sms * 8), 256, 0, s>>>(g, ws, topk);
+        k_sort_buckets<<<grid_for(g.n_items, 1, num_sms * 4), 512, 0, s>>>(g, ws);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cast(const float *in, void *out, int64_t n, float mul, bool fp16, cudaStream_t s,
+                        int num_sms) {
+    const int64_t n4 = n / 4;
+    if (n4 == 0) return cudaSuccess;
+    const int grid = grid_for(n4, 256, num_sms * 8);
+    if (fp16) k_cast<true><<<grid, 256, 0, s>>>(in, (uint16_t *)out, n4, mul);
+    else k_cast<false><<<grid, 256, 0, s>>>(in, (uint16_t *)out, n4, mul);
+    return cudaGetLastError();
+}
+
+}  // namespace sag

@@ -1,0 +1,118 @@
+"""C ABI checks that need no GPU: the library loads, exports every entry point
+declared in include/selattn.h, and phase 1 (parameter validation + workspace
+size, host only) follows the operator's documented constraints."""
+import json
+import os
+import re
+
+import pytest
+
+import sparse_attention_backward_gb300 as sab
+from sparse_attention_backward_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLD = json.load(open(os.path.join(ROOT, "tests", "golden", "constraints.json")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return sab.load()
+
+
+def _declared():
+    hdrs = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+            if f.endswith(".h")]
+    names = set()
+    for h in hdrs:
+        txt = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(sel_attn_grad\w*)\s*\(", txt))
+    return names
+
+
+def test_exports_every_declared_entry_point(lib):
+    names = _declared()
+    assert set(sab.EXPORTED) <= names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _desc(**kw):
+    a = dict(cu_seqlens_q=[0, 256], cu_seqlens_kv=[0, 256], n1=4, n2=1, d_qk=192, d_v=128,
+             block_size=16, block_count=4, scale=192 ** -0.5, dtype=sab.SAG_BF16, deterministic=False)
+    a.update(kw)
+    return sab.make_desc(**a)
+
+
+def _status(d):
+    import ctypes
+    n = ctypes.c_size_t(0)
+    return sab.load().sel_attn_grad_workspace_size(ctypes.byref(d), ctypes.byref(n)), n.value
+
+
+def test_valid_descriptor_gives_workspace(lib):
+    st, n = _status(_desc())
+    assert st == sab.SAG_OK and n > 0
+    st2, n2 = _status(_desc(deterministic=True))
+    assert st2 == sab.SAG_OK and n2 > 0
+
+
+G = sab.SAG_ERR_SHAPE
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(block_size=8), G),                                   # below 16 / not a multiple of 16
+    (dict(block_size=24), G),                                  # not a multiple of 16
+    (dict(block_size=GOLD["block_size_max"] + 16, cu_seqlens_kv=[0, 1024]), G),
+    (dict(block_count=0), G),
+    (dict(block_count=GOLD["block_count"][1] + 1), G),
+    (dict(block_size=64, block_count=128, cu_seqlens_kv=[0, 8192]), G),   # 64*128 = 8192 not < 8192
+    (dict(block_size=64, block_count=127, cu_seqlens_kv=[0, 8128]), sab.SAG_OK),
+    (dict(n1=33, n2=1), G),                                    # G = 33 > 32
+    (dict(n1=32, n2=1), sab.SAG_OK),                           # G = 32
+    (dict(n1=129, n2=1), G),
+    (dict(n1=6, n2=4), G),                                     # N1 not a multiple of N2
+    (dict(n1=256, n2=128), G),                                 # N1 > 128
+    (dict(n1=128, n2=128), sab.SAG_OK),
+    (dict(d_qk=64), G),
+    (dict(d_v=96), G),
+    (dict(d_qk=128, d_v=192), sab.SAG_OK),                     # K and V head dims may differ
+    (dict(cu_seqlens_kv=[0, 250]), G),                         # S2 not a multiple of the block size
+    (dict(cu_seqlens_kv=[0, 48]), G),                          # S2 < size * count
+    (dict(cu_seqlens_kv=[0, 64]), sab.SAG_OK),                 # S2 == size * count (reading: >=)
+    (dict(cu_seqlens_q=[0, 0, 10], cu_seqlens_kv=[0, 64, 128]), sab.SAG_OK),   # empty query batch
+    (dict(cu_seqlens_q=[0, GOLD["S"][1] + 1], cu_seqlens_kv=[0, 256]), G),     # S1 > 128K
+    (dict(cu_seqlens_kv=[0, GOLD["S"][1] + 16]), G),           # S2 > 128K
+    (dict(cu_seqlens_q=[1, 256]), G),                          # prefix sums start at 0
+    (dict(cu_seqlens_q=[0, 0]), G),                            # T1 >= 1
+    (dict(dtype=2), sab.SAG_ERR_DTYPE),
+    (dict(deterministic=2), G),
+    (dict(scale=float("nan")), G),
+])
+def test_phase1_follows_documented_constraints(lib, kw, want):
+    d = _desc(**{k: v for k, v in kw.items() if k != "deterministic"})
+    if "deterministic" in kw:
+        d.deterministic = kw["deterministic"]
+    st, _ = _status(d)
+    assert st == want, (kw, st, sab.status_string(st))
+
+
+def test_null_arguments(lib):
+    import ctypes
+    n = ctypes.c_size_t(0)
+    assert lib.sel_attn_grad_workspace_size(None, ctypes.byref(n)) == sab.SAG_ERR_NULL
+    assert lib.sel_attn_grad_workspace_size(ctypes.byref(_desc()), None) == sab.SAG_ERR_NULL
+    d = _desc()
+    d.cu_seqlens_q = None
+    assert _status(d)[0] == sab.SAG_ERR_NULL
+
+
+def test_status_strings(lib):
+    for st in range(10):
+        assert sab.status_string(st) and sab.status_string(st) != "unknown status"
+    assert sab.status_string(99) == "unknown status"
+
+
+def test_golden_totals_match_limits():
+    # the selection limit and stat lane count the validation encodes
+    assert GOLD["selected_keys_below"] == 128 * 64 and GOLD["stat_lanes"] == 8

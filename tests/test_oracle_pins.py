@@ -181,6 +181,20 @@ def test_sampled_entry_points_match_full_backward():
         np.testing.assert_allclose(bk, dk[r0:r0 + p.block_size, j], rtol=0, atol=1e-14)
         np.testing.assert_allclose(bv, dv[r0:r0 + p.block_size, j], rtol=0, atol=1e-14)
     assert G == 2
+    # a token range split of one block adds up to the whole block
+    b, j, kb = 1, 0, 1
+    mid = (p.cu_q[b] + p.cu_q[b + 1]) // 2
+    k1, v1 = oracle.dkdv_block_range(p, b, j, kb, 0, mid)
+    k2, v2 = oracle.dkdv_block_range(p, b, j, kb, mid, p.t1)
+    wk, wv = oracle.dkdv_block(p, b, j, kb)
+    np.testing.assert_allclose(k1 + k2, wk, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(v1 + v2, wv, rtol=0, atol=1e-14)
+    # the row-subset forward equals the full forward on those rows
+    o, m, l = oracle.forward(p)
+    o2, m2, l2 = oracle.forward_rows(p, rows)
+    np.testing.assert_array_equal(o2, o.reshape(-1, p.d_v)[rows])
+    np.testing.assert_array_equal(m2, m.reshape(-1)[rows])
+    np.testing.assert_array_equal(l2, l.reshape(-1)[rows])
 
 
 def test_list_order_does_not_matter():
