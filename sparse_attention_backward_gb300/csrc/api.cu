@@ -144,6 +144,18 @@ int device_sms() {
     return sms;
 }
 
+// Make the device that owns `s` current for this library's runtime (the
+// caller's framework may keep its own notion of the current device).  The
+// legacy default stream (NULL) keeps the current device.
+bool bind_stream_device(cudaStream_t s) {
+    if (s == nullptr) return true;
+    int dev = 0;
+    if (cudaStreamGetDevice(s, &dev) != cudaSuccess) return false;
+    int cur = -1;
+    if (cudaGetDevice(&cur) == cudaSuccess && cur == dev) return true;
+    return cudaSetDevice(dev) == cudaSuccess;
+}
+
 }  // namespace
 }  // namespace sag
 
@@ -213,6 +225,7 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
     if (workspace_bytes < p.total) return SAG_ERR_WORKSPACE;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!bind_stream_device(s)) return SAG_ERR_CUDA;
     const Geometry &g = p.g;
     Workspace ws = carve(p, workspace);
     const int sms = device_sms();
@@ -272,6 +285,7 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
 extern "C" sag_status sel_attn_grad_query_error(const void *workspace, void *stream) {
     if (!workspace) return SAG_ERR_NULL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!bind_stream_device(s)) return SAG_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return SAG_ERR_CUDA;
     int32_t code = 0;
     if (cudaMemcpy(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) return SAG_ERR_CUDA;
