@@ -178,6 +178,40 @@ sag_status sel_attn_grad_timed(const sag_desc *desc, const void *query, const vo
                                void *dk, void *dv, void *workspace, size_t workspace_bytes,
                                void *stream, void *main_start, void *main_stop);
 
+/*
+ * Allocation-free variant of sel_attn_grad.  The operator pages have no
+ * counterpart: it exists for callers that cannot allocate device memory at
+ * the point of the call -- code that runs inside a framework whose memory
+ * pool forbids raw cudaMalloc, plug-ins that are handed only tensors by their
+ * host, or steps where an allocation (and the synchronisation it implies) is
+ * not allowed.
+ *
+ * The caller passes inputs, outputs and a stream as for sel_attn_grad, but no
+ * workspace: the scratch lives in one fixed array of
+ * SEL_ATTN_GRAD_NOALLOC_MAX_SCRATCH bytes inside the library, which every GPU
+ * that loads the library holds until the process exits.  Nothing is
+ * allocated, on the host or the device, by this call.
+ *   - A problem whose phase-1 workspace size exceeds the maximum is rejected
+ *     with SAG_ERR_WORKSPACE before anything is enqueued (use sel_attn_grad
+ *     with a caller-owned workspace for those).
+ *   - The first call on a device looks up that device's copy of the array
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls on a device share the one array.  Each call re-initialises
+ *     what has to start at zero, so earlier contents do not matter, but calls
+ *     whose work overlaps on the GPU (different streams, or another thread)
+ *     race on it: serialise them.
+ *   - The device status (SAG_ERR_INDEX, ...) is not readable through
+ *     sel_attn_grad_query_error, which needs the workspace pointer.
+ * Returns the statuses of sel_attn_grad, or SAG_ERR_WORKSPACE as above.
+ */
+#define SEL_ATTN_GRAD_NOALLOC_MAX_SCRATCH ((size_t)64 << 20)
+
+sag_status sel_attn_grad_noalloc(const sag_desc *desc, const void *query, const void *key,
+                                 const void *value, const void *attention_out,
+                                 const void *attention_out_grad, const float *softmax_max,
+                                 const float *softmax_sum, const int32_t *topk_indices, void *dq,
+                                 void *dk, void *dv, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *sel_attn_grad_status_string(int status);
 

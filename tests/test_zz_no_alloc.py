@@ -1,0 +1,74 @@
+"""The allocation-free entry point against the workspace entry point.
+
+sel_attn_grad_noalloc serves callers that cannot allocate device memory when
+they call the backward (a framework memory pool that forbids raw cudaMalloc,
+a plug-in handed only tensors): its scratch is a fixed array inside the
+library.  Here it is called through the C ABI twice in a row (the second call
+finds the first call's leftovers in the shared array) and must agree with
+sel_attn_grad on a caller-owned workspace within the parity tolerance.  The
+file is collected last so that a stop-at-first-failure run has already run
+every other test.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import sparse_attention_backward_gb300 as sab
+import synth
+from tests import _support as S
+
+pytestmark = pytest.mark.gpu
+
+
+def _entry(lib):
+    f = lib.sel_attn_grad_noalloc
+    f.argtypes = [ctypes.POINTER(sab.SagDesc)] + [ctypes.c_void_p] * 12
+    f.restype = ctypes.c_int
+    return f
+
+
+def _inputs(w, dev, seed):
+    x = synth.make_inputs(w, device=dev, seed=seed)
+    x.update(synth.synthetic_forward_stats(w, torch.Generator(device=dev).manual_seed(seed + 1), dev))
+    return [x[k] for k in ("q", "k", "v", "o", "dy", "softmax_max", "softmax_sum", "topk")]
+
+
+def _desc(w, det):
+    return sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
+                         sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, det)
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_noalloc_matches_workspace_entry_point(deterministic):
+    lib = sab.load()
+    f = _entry(lib)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    w = synth.WORKLOADS[0]
+    # two calls in a row on different inputs: the second must not see the first
+    for call, seed in enumerate((101, 202)):
+        ins = _inputs(w, dev, seed)
+        want = sab.backward(*ins, w.cu_q, w.cu_kv, w.scale, w.block_size, w.block_count,
+                            deterministic=deterministic, check=True)
+        got = [torch.full_like(t, float("nan")) for t in (ins[0], ins[1], ins[2])]
+        desc = _desc(w, deterministic)
+        st = f(ctypes.byref(desc), *[t.data_ptr() for t in ins], *[t.data_ptr() for t in got],
+               stream.cuda_stream)
+        assert st == sab.SAG_OK, sab.status_string(st)
+        torch.cuda.synchronize()
+        for name, g, r in zip(("dq", "dk", "dv"), got, want):
+            S.assert_close(f"call {call} {name}", S.f64(g), S.f64(r))
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    lib = sab.load()
+    f = _entry(lib)
+    w = synth.WORKLOADS[2]   # long context: its workspace is far above the fixed scratch
+    need = sab.workspace_size(_desc(w, False))
+    assert need > (64 << 20)
+    dev = torch.device("cuda", 0)
+    dummy = torch.empty(16, dtype=torch.uint8, device=dev)
+    st = f(ctypes.byref(_desc(w, False)), *([dummy.data_ptr()] * 11),
+           torch.cuda.current_stream(dev).cuda_stream)
+    assert st == sab.SAG_ERR_WORKSPACE
