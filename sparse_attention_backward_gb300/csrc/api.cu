@@ -3,6 +3,7 @@
 // section of the "NsaSelectedAttentionGrad" README; the two-phase shape
 // follows the aclnn calling convention described on the same pages
 // (GetWorkspaceSize validates, the second call runs on a stream).
+#include <stdlib.h>
 #include <string.h>
 
 #include <vector>
@@ -29,6 +30,7 @@ struct Plan {
     size_t o_hdr, o_cu_q, o_cu_kv, o_item_base, o_count, o_offset, o_cursor, o_scan, o_entries,
         o_delta, o_lse2, o_dq_acc, o_ds, o_dkv, total;
     int32_t chunk_tokens, n_chunks;
+    bool use_tc;                      // tensor-core main kernel (else the CUDA-core one)
     std::vector<int64_t> item_base;   // host copy, B+1
 };
 
@@ -111,6 +113,10 @@ sag_status make_plan(const sag_desc *d, Plan *p) {
     g.tok_lo = 0;
     g.tok_hi = g.t1;
     g.chunked = p->n_chunks > 1;
+    // SELATTN_FORCE_CUDA_CORE=1 selects the CUDA-core kernel for shapes the
+    // tensor-core one also covers (used to cross-check the two)
+    const char *force = getenv("SELATTN_FORCE_CUDA_CORE");
+    p->use_tc = bwd_tc_supported(g) && !(force && force[0] == '1');
     p->total = o;
     return SAG_OK;
 }
@@ -188,7 +194,7 @@ extern "C" sag_status sel_attn_grad_plan_info(const sag_desc *desc, sag_plan_inf
     info->launches = launches_of(p);
     info->token_chunks = p.n_chunks;
     info->items = p.g.n_items;
-    info->main_kernel = 0;
+    info->main_kernel = p.use_tc ? 1 : 0;
     info->reserved_ = 0;
     return SAG_OK;
 }
@@ -253,8 +259,9 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
     if ((e = launch_inversion(g, ws, topk_indices, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
     if (!p.det) {
         if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return SAG_ERR_CUDA;
-        if ((e = launch_bwd_simt(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s, sms)) !=
-            cudaSuccess)
+        if ((e = p.use_tc ? launch_bwd_tc(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s, sms)
+                          : launch_bwd_simt(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s,
+                                            sms)) != cudaSuccess)
             return SAG_ERR_CUDA;
         if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SAG_ERR_CUDA;
         if ((e = launch_cast(ws.dq_acc, dq, (int64_t)g.t1 * g.n1 * g.d_qk, g.scale, p.fp16, s, sms)) !=
@@ -271,8 +278,9 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
         Geometry gc = g;
         gc.tok_lo = c * p.chunk_tokens;
         gc.tok_hi = gc.tok_lo + p.chunk_tokens < g.t1 ? gc.tok_lo + p.chunk_tokens : g.t1;
-        if ((e = launch_bwd_simt(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s, sms)) !=
-            cudaSuccess)
+        if ((e = p.use_tc ? launch_bwd_tc(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s, sms)
+                          : launch_bwd_simt(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s,
+                                            sms)) != cudaSuccess)
             return SAG_ERR_CUDA;
         if ((e = launch_dq_from_ds(gc, ws, key, topk_indices, dq, p.fp16, s, sms)) != cudaSuccess)
             return SAG_ERR_CUDA;

@@ -1,0 +1,534 @@
+// Tensor-core (tcgen05 / TMEM / TMA) key-block-major backward.
+//
+// Work unit: a key tile = NK (<= 64) consecutive key rows of one selected
+// block of (batch b, KV head n2), with the bucket of (token, slot) pairs that
+// selected the block ("NsaSelectedAttentionGrad" README, Gather formula,
+// inverted by key block).  A persistent CTA walks its key tiles; for each it
+// keeps the K / V tile in shared memory and the dK / dV accumulators in TMEM
+// and streams the bucket's query rows in tiles of 128 (128 / G tokens x G
+// heads).  Per query tile:
+//     S    = Q K^T          (M = 128 rows, N = NK, K = Dqk)   -> TMEM
+//     dP   = dY V^T         (M = 128 rows, N = NK, K = Dv)    -> TMEM
+//     P    = exp2(S * scale*log2e - lse2),  dS = P (dP - Delta)  (CUDA cores)
+//     dV^T += dY^T P        (M = Dv dims, N = NK, K = 128 rows)
+//     dK^T += Q^T dS        (M = Dqk dims, 128 at a time, N = NK)
+//     dQ   = dS K           (M = 128 rows, N = Dqk, K = NK)   -> fp32 red into
+//                                                               the dQ accumulator
+// (dV = P^T dY, dK = dS^T Q / sqrt(d), dQ = dS K / sqrt(d): README function
+// description; dS = P * (dP - Delta): softmax adjoint of the dense formulas of
+// "aclnnFlashAttentionUnpaddingScoreGradV3").  In deterministic mode dQ is not
+// formed here: dS is stored and reduced in a fixed order by a second pass.
+//
+// Warp roles (320 threads): 0 TMA producer, 1 MMA issuer and TMEM owner,
+// 2-5 softmax / dS (thread = query row = TMEM lane), 6-9 epilogue (dQ reds per
+// tile, dK / dV per key tile).  Every wait is bounded; a timeout records
+// SAG_ERR_TIMEOUT and the CTA winds down.
+#include "kernels.cuh"
+#include "tc.cuh"
+#include "tmap.cuh"
+
+namespace sag {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kRows = 128;          // query rows per tile (MMA M)
+constexpr int kMeta = 4;            // depth of the tile-metadata ring
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+// TMEM columns (512 allocated)
+constexpr uint32_t kColS = 0, kColDP = 64, kColDV = 128, kColDKlo = 192, kColDKhi = 256, kColDQ = 320;
+
+template <int DQK>
+struct Smem {
+    static constexpr int KC = DQK / 64;                  // 64-wide chunks of a q / k row
+    static constexpr int DOS = (DQK == 128) ? 2 : 1;     // dY stages
+    static constexpr int K_TILE = KC * 8192;             // 64 rows x 128 B per chunk
+    static constexpr int V_TILE = 2 * 8192;
+    static constexpr int Q_STAGE = KC * 16384;           // 128 rows x 128 B per chunk
+    static constexpr int DO_STAGE = 2 * 16384;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + K_TILE;
+    static constexpr int OFF_Q = OFF_V + V_TILE;
+    static constexpr int OFF_DO = OFF_Q + 2 * Q_STAGE;
+    static constexpr int OFF_P = OFF_DO + DOS * DO_STAGE;
+    static constexpr int OFF_DS = OFF_P + 16384;
+    static constexpr int OFF_STG = OFF_DS + 16384;       // 4 epilogue warps x 4 KB
+    static constexpr int OFF_META = OFF_STG + 16384;     // kMeta x 128 ints
+    static constexpr int OFF_BAR = OFF_META + kMeta * kRows * 4;
+    static constexpr int TOTAL = OFF_BAR + 256 + 1024;   // + slack for 1024-B alignment
+};
+
+enum Bar {
+    B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL0, B_Q_FULL1, B_Q_EMPTY0, B_Q_EMPTY1, B_DO_FULL0, B_DO_FULL1,
+    B_DO_EMPTY0, B_DO_EMPTY1, B_S_FULL, B_P_FULL, B_MMA_DONE, B_DQ_FREE, B_ACC_FULL, B_ACC_FREE, B_COUNT
+};
+
+struct KeyTile {
+    int b, n2;
+    int64_t key0;       // first key row
+    int koff;           // offset of the tile inside its block
+    int64_t item;
+    int e0, ntok;       // bucket entries [e0, e0 + ntok) of this launch's token range
+    int ntiles;
+};
+
+__device__ __forceinline__ KeyTile decode(const Geometry &g, const Workspace &ws, int64_t titem, int halves,
+                                          int nk, int tpt) {
+    KeyTile kt;
+    kt.item = titem / halves;
+    const int half = (int)(titem % halves);
+    kt.b = batch_of_item(ws.item_base, g.batch, kt.item);
+    const int nblk = (ws.cu_kv[kt.b + 1] - ws.cu_kv[kt.b]) / g.block_size;
+    const int64_t local = kt.item - ws.item_base[kt.b];
+    kt.n2 = (int)(local / nblk);
+    const int kb = (int)(local % nblk);
+    kt.koff = half * nk;
+    kt.key0 = ws.cu_kv[kt.b] + (int64_t)kb * g.block_size + kt.koff;
+    const int e_end = ws.offset[kt.item + 1];
+    kt.e0 = lower_bound_token(ws.entries, ws.offset[kt.item], e_end, g.tok_lo, g.block_count);
+    const int e1 = lower_bound_token(ws.entries, kt.e0, e_end, g.tok_hi, g.block_count);
+    kt.ntok = e1 - kt.e0;
+    kt.ntiles = (kt.ntok + tpt - 1) / tpt;
+    return kt;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <bool kFp16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    return (uint32_t)f_to_u16<kFp16>(a) | ((uint32_t)f_to_u16<kFp16>(b) << 16);
+}
+
+// address of 16-byte chunk c of row r in a 128-byte-swizzled [rows x 128 B] tile
+__device__ __forceinline__ uint32_t sw_off(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+struct TcArgs {
+    Geometry g;
+    Workspace ws;
+    uint16_t *dk, *dv;
+    int nk, halves, tpt, deterministic;
+    int64_t n_titems;
+};
+
+template <bool kFp16, int DQK>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_bwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+             const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v, TcArgs A) {
+    using L = Smem<DQK>;
+    constexpr int DV = 128;
+    constexpr int KC = L::KC;
+    constexpr int DOS = L::DOS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_BAR + 8 * B_COUNT);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_BAR + 8 * B_COUNT + 4);
+    int *meta = reinterpret_cast<int *>(smem + L::OFF_META);
+    const Geometry &g = A.g;
+    const Workspace &ws = A.ws;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nk = A.nk, tpt = A.tpt, G = g.group;
+    const bool det = A.deterministic != 0;
+    const uint32_t sbase = tc::smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        tc::mbar_init(&bars[B_KV_FULL], 1);
+        tc::mbar_init(&bars[B_KV_EMPTY], 1);
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&bars[B_Q_FULL0 + s], 1);
+            tc::mbar_init(&bars[B_Q_EMPTY0 + s], 1);
+            tc::mbar_init(&bars[B_DO_FULL0 + s], 1);
+            tc::mbar_init(&bars[B_DO_EMPTY0 + s], 1);
+        }
+        tc::mbar_init(&bars[B_S_FULL], 1);
+        tc::mbar_init(&bars[B_P_FULL], 128);
+        tc::mbar_init(&bars[B_MMA_DONE], 1);
+        tc::mbar_init(&bars[B_DQ_FREE], 128);
+        tc::mbar_init(&bars[B_ACC_FULL], 1);
+        tc::mbar_init(&bars[B_ACC_FREE], 128);
+        tc::fence_mbar_init();
+    }
+    // rows of a Q / dY tile no token fills (when G does not divide 128) must
+    // hold finite values: zero the staging buffers once
+    if (tpt * G < kRows) {
+        for (int i = threadIdx.x; i < (2 * L::Q_STAGE + DOS * L::DO_STAGE) / 16; i += kThreads)
+            reinterpret_cast<uint4 *>(smem + L::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
+        tc::fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        raise_error(&ws.hdr->error, SAG_ERR_TIMEOUT);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tc::prefetch_tmap(&map_q);
+            tc::prefetch_tmap(&map_do);
+            tc::prefetch_tmap(&map_k);
+            tc::prefetch_tmap(&map_v);
+        }
+        const int oob_row = g.t1 * g.n1;   // out of range: the TMA fills zeros
+        int ne = 0, tc_i = 0;
+        bool ok = true;
+        for (int64_t ti = blockIdx.x; ti < A.n_titems && ok; ti += gridDim.x) {
+            const KeyTile kt = decode(g, ws, ti, A.halves, nk, tpt);
+            if (kt.ntok == 0) continue;
+            if (ne > 0 && !tc::mbar_wait(&bars[B_KV_EMPTY], (ne - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            if (lane == 0) {
+                tc::mbar_arrive_expect_tx(&bars[B_KV_FULL], (uint32_t)nk * (DQK + DV) * 2);
+                for (int c = 0; c < KC; ++c)
+                    tc::tma_load_3d(smem + L::OFF_K + c * 8192, &map_k, c * 64, kt.n2, (int)kt.key0, &bars[B_KV_FULL]);
+                for (int c = 0; c < 2; ++c)
+                    tc::tma_load_3d(smem + L::OFF_V + c * 8192, &map_v, c * 64, kt.n2, (int)kt.key0, &bars[B_KV_FULL]);
+            }
+            for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
+                const int s = tc_i & 1;
+                if (tc_i >= 2 && !tc::mbar_wait(&bars[B_Q_EMPTY0 + s], ((tc_i >> 1) - 1) & 1, abort_flag, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                const int nt = min(tpt, kt.ntok - i * tpt);
+                int *m = meta + (tc_i % kMeta) * kRows;
+                for (int tt = lane; tt < tpt; tt += 32) m[tt] = tt < nt ? ws.entries[kt.e0 + i * tpt + tt] : -1;
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive_expect_tx(&bars[B_Q_FULL0 + s], (uint32_t)tpt * G * DQK * 2);
+                __syncwarp();
+                uint8_t *qdst = smem + L::OFF_Q + s * L::Q_STAGE;
+                for (int tt = lane; tt < tpt; tt += 32) {
+                    const int y = tt < nt ? (m[tt] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
+                    for (int c = 0; c < KC; ++c)
+                        tc::tma_load_2d(qdst + c * 16384 + tt * G * 128, &map_q, c * 64, y, &bars[B_Q_FULL0 + s]);
+                }
+                const int d = tc_i % DOS;
+                if (tc_i >= DOS &&
+                    !tc::mbar_wait(&bars[B_DO_EMPTY0 + d], ((tc_i / DOS) - 1) & 1, abort_flag, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) tc::mbar_arrive_expect_tx(&bars[B_DO_FULL0 + d], (uint32_t)tpt * G * DV * 2);
+                __syncwarp();
+                uint8_t *ddst = smem + L::OFF_DO + d * L::DO_STAGE;
+                for (int tt = lane; tt < tpt; tt += 32) {
+                    const int y = tt < nt ? (m[tt] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
+                    for (int c = 0; c < 2; ++c)
+                        tc::tma_load_2d(ddst + c * 16384 + tt * G * 128, &map_do, c * 64, y, &bars[B_DO_FULL0 + d]);
+                }
+            }
+            ++ne;
+        }
+        if (!ok) fail();
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const bool bf16 = !kFp16;
+            const uint32_t id_s = tc::idesc_f16(kRows, nk, bf16, false, false);
+            const uint32_t id_t = tc::idesc_f16(128, nk, bf16, true, true);
+            const uint32_t id_q = tc::idesc_f16(kRows, DQK, bf16, false, true);
+            int ne = 0, tc_i = 0;
+            bool ok = true;
+            for (int64_t ti = blockIdx.x; ti < A.n_titems && ok; ti += gridDim.x) {
+                const KeyTile kt = decode(g, ws, ti, A.halves, nk, tpt);
+                if (kt.ntok == 0) continue;
+                if (!tc::mbar_wait(&bars[B_KV_FULL], ne & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                if (ne > 0 && !tc::mbar_wait(&bars[B_ACC_FREE], (ne - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
+                    const int s = tc_i & 1, d = tc_i % DOS;
+                    if (!tc::mbar_wait(&bars[B_Q_FULL0 + s], (tc_i >> 1) & 1, abort_flag, kWaitNs) ||
+                        !tc::mbar_wait(&bars[B_DO_FULL0 + d], (tc_i / DOS) & 1, abort_flag, kWaitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint32_t qs = sbase + L::OFF_Q + s * L::Q_STAGE;
+                    const uint32_t ds_ = sbase + L::OFF_DO + d * L::DO_STAGE;
+                    const uint32_t ks = sbase + L::OFF_K, vs = sbase + L::OFF_V;
+                    // S = Q K^T, dP = dY V^T (both operands K-major)
+                    for (int kk = 0; kk < DQK / 16; ++kk)
+                        tc::mma_f16_ss(tmem + kColS, tc::sw128_desc(qs + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                                       tc::sw128_desc(ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+                    for (int kk = 0; kk < DV / 16; ++kk)
+                        tc::mma_f16_ss(tmem + kColDP, tc::sw128_desc(ds_ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                                       tc::sw128_desc(vs + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+                    tc::mma_commit(&bars[B_S_FULL]);
+                    if (!tc::mbar_wait(&bars[B_P_FULL], tc_i & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t ps = sbase + L::OFF_P, dss = sbase + L::OFF_DS;
+                    // dV^T += dY^T P (A: dY tile MN-major, B: P MN-major)
+                    for (int kk = 0; kk < kRows / 16; ++kk)
+                        tc::mma_f16_ss(tmem + kColDV, tc::sw128_desc(ds_ + kk * 2048, 16384, 1024),
+                                       tc::sw128_desc(ps + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
+                    tc::mma_commit(&bars[B_DO_EMPTY0 + d]);
+                    // dK^T += Q^T dS, dims [0,128) and (192 wide) dims [64,192)
+                    for (int kk = 0; kk < kRows / 16; ++kk)
+                        tc::mma_f16_ss(tmem + kColDKlo, tc::sw128_desc(qs + kk * 2048, 16384, 1024),
+                                       tc::sw128_desc(dss + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
+                    if (DQK == 192)
+                        for (int kk = 0; kk < kRows / 16; ++kk)
+                            tc::mma_f16_ss(tmem + kColDKhi, tc::sw128_desc(qs + 16384 + kk * 2048, 16384, 1024),
+                                           tc::sw128_desc(dss + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
+                    tc::mma_commit(&bars[B_Q_EMPTY0 + s]);
+                    if (!det) {
+                        // dQ = dS K (A: dS K-major, B: K tile MN-major, N = Dqk)
+                        if (tc_i > 0 && !tc::mbar_wait(&bars[B_DQ_FREE], (tc_i - 1) & 1, abort_flag, kWaitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::tc_fence_after();
+                        for (int kk = 0; kk < nk / 16; ++kk)
+                            tc::mma_f16_ss(tmem + kColDQ, tc::sw128_desc(dss + kk * 32, 16, 1024),
+                                           tc::sw128_desc(ks + kk * 2048, 8192, 1024), id_q, kk > 0);
+                    }
+                    tc::mma_commit(&bars[B_MMA_DONE]);
+                }
+                if (!ok) break;
+                tc::mma_commit(&bars[B_ACC_FULL]);
+                tc::mma_commit(&bars[B_KV_EMPTY]);
+                ++ne;
+            }
+            if (!ok) fail();
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------ softmax / dS
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;                      // query row = TMEM lane
+        const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+        const int tt = r / G, gg = r % G;
+        int tc_i = 0;
+        bool ok = true;
+        for (int64_t ti = blockIdx.x; ti < A.n_titems && ok; ti += gridDim.x) {
+            const KeyTile kt = decode(g, ws, ti, A.halves, nk, tpt);
+            if (kt.ntok == 0) continue;
+            for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
+                const int s = tc_i & 1;
+                ok = tc::mbar_wait(&bars[B_Q_FULL0 + s], (tc_i >> 1) & 1, abort_flag, kWaitNs);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                const int ent = tt < tpt ? meta[(tc_i % kMeta) * kRows + tt] : -1;
+                const bool valid = ent >= 0;
+                int64_t grow = 0;
+                float lse2 = 0.f, delta = 0.f;
+                if (valid) {
+                    grow = (int64_t)(ent / g.block_count) * g.n1 + kt.n2 * G + gg;
+                    lse2 = ws.lse2[grow];
+                    delta = ws.delta[grow];
+                }
+                ok = tc::mbar_wait(&bars[B_S_FULL], tc_i & 1, abort_flag, kWaitNs);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc::tc_fence_after();
+                uint32_t pk[32], dk2[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (c >= nk / 16) break;
+                    uint32_t sv[16], dv[16];
+                    tc::tmem_ld16(trow + kColS + c * 16, sv);
+                    tc::tmem_ld16(trow + kColDP + c * 16, dv);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        float p0 = 0.f, p1 = 0.f, d0 = 0.f, d1 = 0.f;
+                        if (valid) {
+                            p0 = ex2(fmaf(__uint_as_float(sv[j]), g.scale_log2, -lse2));
+                            p1 = ex2(fmaf(__uint_as_float(sv[j + 1]), g.scale_log2, -lse2));
+                            d0 = p0 * (__uint_as_float(dv[j]) - delta);
+                            d1 = p1 * (__uint_as_float(dv[j + 1]) - delta);
+                        }
+                        pk[c * 8 + j / 2] = pack2<kFp16>(p0, p1);
+                        dk2[c * 8 + j / 2] = pack2<kFp16>(d0, d1);
+                    }
+                }
+                // the previous tile's MMAs must be done with the P / dS buffers
+                if (tc_i > 0) {
+                    ok = tc::mbar_wait(&bars[B_MMA_DONE], (tc_i - 1) & 1, abort_flag, kWaitNs);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                }
+                uint8_t *prow = smem + L::OFF_P;
+                uint8_t *drow = smem + L::OFF_DS;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    if (c >= nk / 8) break;
+                    *reinterpret_cast<uint4 *>(prow + sw_off(r, c)) =
+                        make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
+                    *reinterpret_cast<uint4 *>(drow + sw_off(r, c)) =
+                        make_uint4(dk2[c * 4], dk2[c * 4 + 1], dk2[c * 4 + 2], dk2[c * 4 + 3]);
+                }
+                if (det && valid) {
+                    // dS[t - tok_lo][n2][slot][g][key] in the input dtype
+                    const int t = ent / g.block_count, slot = ent % g.block_count;
+                    const int64_t base =
+                        ((((int64_t)(t - g.tok_lo) * g.n2 + kt.n2) * g.block_count + slot) * G + gg) * g.block_size +
+                        kt.koff;
+                    uint4 *dst = reinterpret_cast<uint4 *>(ws.ds + base);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        if (c < nk / 8) dst[c] = make_uint4(dk2[c * 4], dk2[c * 4 + 1], dk2[c * 4 + 2], dk2[c * 4 + 3]);
+                }
+                tc::fence_proxy_async_smem();
+                tc::tc_fence_before();
+                tc::mbar_arrive(&bars[B_P_FULL]);
+            }
+        }
+        if (!ok) fail();
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+        const int tt = r / G, gg = r % G;
+        uint8_t *stg = smem + L::OFF_STG + (warp - 6) * 4096;
+        const int et = threadIdx.x - 192;                 // 0..127
+        int ne = 0, tc_i = 0;
+        bool ok = true;
+        for (int64_t ti = blockIdx.x; ti < A.n_titems && ok; ti += gridDim.x) {
+            const KeyTile kt = decode(g, ws, ti, A.halves, nk, tpt);
+            if (kt.ntok == 0) {
+                if (!g.chunked) {
+                    for (int i = et; i < nk * (DQK + DV); i += 128) {
+                        const int j = i / (DQK + DV), c = i % (DQK + DV);
+                        const int64_t row = (kt.key0 + j) * g.n2 + kt.n2;
+                        if (c < DQK) A.dk[row * DQK + c] = 0;
+                        else A.dv[row * DV + c - DQK] = 0;
+                    }
+                }
+                continue;
+            }
+            for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
+                if (det) continue;
+                ok = tc::mbar_wait(&bars[B_MMA_DONE], tc_i & 1, abort_flag, kWaitNs);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc::tc_fence_after();
+                const int ent = tt < tpt ? meta[(tc_i % kMeta) * kRows + tt] : -1;
+                const int64_t grow = ent >= 0 ? (int64_t)(ent / g.block_count) * g.n1 + kt.n2 * G + gg : -1;
+                for (int c = 0; c < DQK / 32; ++c) {
+                    uint32_t v0[16], v1[16];
+                    tc::tmem_ld16(trow + kColDQ + c * 32, v0);
+                    tc::tmem_ld16(trow + kColDQ + c * 32 + 16, v1);
+                    tc::tmem_wait_ld();
+                    // stage the warp's 32 rows x 32 floats, then red whole row segments
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4)
+                        *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j4 ^ (lane & 7)) << 4)) =
+                            make_uint4(v0[4 * j4], v0[4 * j4 + 1], v0[4 * j4 + 2], v0[4 * j4 + 3]);
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4)
+                        *reinterpret_cast<uint4 *>(stg + lane * 128 + (((j4 + 4) ^ (lane & 7)) << 4)) =
+                            make_uint4(v1[4 * j4], v1[4 * j4 + 1], v1[4 * j4 + 2], v1[4 * j4 + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int rr = k * 4 + (lane >> 3), j4 = lane & 7;
+                        const int64_t gr = __shfl_sync(0xffffffffu, grow, rr);
+                        const float4 x = *reinterpret_cast<const float4 *>(stg + rr * 128 + ((j4 ^ (rr & 7)) << 4));
+                        if (gr >= 0) tc::red_add_v4(ws.dq_acc + gr * DQK + c * 32 + j4 * 4, x.x, x.y, x.z, x.w);
+                    }
+                    __syncwarp();
+                }
+                tc::tc_fence_before();
+                tc::mbar_arrive(&bars[B_DQ_FREE]);
+            }
+            if (!ok) break;
+            // dK / dV of this key tile
+            ok = tc::mbar_wait(&bars[B_ACC_FULL], ne & 1, abort_flag, kWaitNs);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc::tc_fence_after();
+            for (int j0 = 0; j0 < nk; j0 += 16) {
+                uint32_t av[16], ak[16], ah[16];
+                tc::tmem_ld16(trow + kColDV + j0, av);
+                tc::tmem_ld16(trow + kColDKlo + j0, ak);
+                if (DQK == 192) tc::tmem_ld16(trow + kColDKhi + j0, ah);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int64_t row = (kt.key0 + j0 + j) * g.n2 + kt.n2;
+                    const float vv = __uint_as_float(av[j]), kv = __uint_as_float(ak[j]);
+                    if (g.chunked) {
+                        float *acc = ws.dkv_acc + row * (DQK + DV);
+                        acc[r] += kv;
+                        acc[DQK + r] += vv;
+                        if (DQK == 192 && r >= 64) acc[64 + r] += __uint_as_float(ah[j]);
+                    } else {
+                        A.dk[row * DQK + r] = f_to_u16<kFp16>(kv * g.scale);
+                        A.dv[row * DV + r] = f_to_u16<kFp16>(vv);
+                        if (DQK == 192 && r >= 64) A.dk[row * DQK + 64 + r] = f_to_u16<kFp16>(__uint_as_float(ah[j]) * g.scale);
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&bars[B_ACC_FREE]);
+            ++ne;
+        }
+        if (!ok) fail();
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+bool bwd_tc_supported(const Geometry &g) {
+    const int bs = g.block_size;
+    return g.d_v == 128 && (g.d_qk == 128 || g.d_qk == 192) &&
+           (bs == 16 || bs == 32 || bs == 48 || bs == 64 || bs == 128);
+}
+
+template <bool kFp16, int DQK>
+static cudaError_t launch_tc_t(const Geometry &g, const Workspace &ws, const void *q, const void *k, const void *v,
+                               const void *dy, void *dk, void *dv, bool det, cudaStream_t s, int num_sms) {
+    const int nk = g.block_size > 64 ? 64 : g.block_size;
+    TcArgs a;
+    a.g = g;
+    a.ws = ws;
+    a.dk = (uint16_t *)dk;
+    a.dv = (uint16_t *)dv;
+    a.nk = nk;
+    a.halves = g.block_size / nk;
+    a.tpt = kRows / g.group;
+    a.deterministic = det ? 1 : 0;
+    a.n_titems = g.n_items * a.halves;
+    CUtensorMap mq, mdo, mk, mv;
+    if (!tmap_2d(&mq, q, kFp16, DQK, (uint64_t)g.t1 * g.n1, g.group) ||
+        !tmap_2d(&mdo, dy, kFp16, 128, (uint64_t)g.t1 * g.n1, g.group) ||
+        !tmap_3d(&mk, k, kFp16, DQK, g.n2, g.t2, nk) || !tmap_3d(&mv, v, kFp16, 128, g.n2, g.t2, nk))
+        return cudaErrorInvalidValue;
+    auto fn = k_bwd_tc<kFp16, DQK>;
+    const int smem = Smem<DQK>::TOTAL;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int64_t grid = a.n_titems < num_sms ? a.n_titems : num_sms;
+    if (grid < 1) grid = 1;
+    fn<<<(int)grid, kThreads, smem, s>>>(mq, mdo, mk, mv, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_tc(const Geometry &g, const Workspace &ws, const void *q, const void *k, const void *v,
+                          const void *dy, void *dk, void *dv, bool fp16, bool deterministic, cudaStream_t s,
+                          int num_sms) {
+    if (!bwd_tc_supported(g)) return cudaErrorInvalidValue;
+    if (fp16)
+        return g.d_qk == 192 ? launch_tc_t<true, 192>(g, ws, q, k, v, dy, dk, dv, deterministic, s, num_sms)
+                             : launch_tc_t<true, 128>(g, ws, q, k, v, dy, dk, dv, deterministic, s, num_sms);
+    return g.d_qk == 192 ? launch_tc_t<false, 192>(g, ws, q, k, v, dy, dk, dv, deterministic, s, num_sms)
+                         : launch_tc_t<false, 128>(g, ws, q, k, v, dy, dk, dv, deterministic, s, num_sms);
+}
+
+}  // namespace sag

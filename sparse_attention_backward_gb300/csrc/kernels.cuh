@@ -19,6 +19,12 @@ int64_t max_scannable_items();
 cudaError_t launch_bwd_simt(const Geometry &g, const Workspace &ws, const void *q, const void *k,
                             const void *v, const void *dy, void *dk, void *dv, bool fp16,
                             bool deterministic, cudaStream_t s, int num_sms);
+// Tensor-core (tcgen05) key-block-major backward: d_v == 128, d_qk in
+// {128, 192}, block size in {16, 32, 48, 64, 128}.
+bool bwd_tc_supported(const Geometry &g);
+cudaError_t launch_bwd_tc(const Geometry &g, const Workspace &ws, const void *q, const void *k, const void *v,
+                          const void *dy, void *dk, void *dv, bool fp16, bool deterministic, cudaStream_t s,
+                          int num_sms);
 // dK/dV from the fp32 accumulator after the last token chunk.
 cudaError_t launch_cast_dkv(const Geometry &g, const Workspace &ws, void *dk, void *dv, bool fp16,
                             cudaStream_t s, int num_sms);
