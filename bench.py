@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
+    ap.add_argument("--seq", type=int, default=0,
+                    help="override every batch's query and key length (smaller profiling captures)")
     return ap.parse_args()
 
 
@@ -223,6 +225,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     w = synth.WORKLOADS[args.config]
+    if args.seq:
+        cu = tuple(args.seq * i for i in range(w.batch + 1))
+        w = w.with_(name=f"{w.name}_seq{args.seq}", cu_q=cu, cu_kv=cu)
     if args.impl == "reference":
         if world > 1 and rank != 0:
             return

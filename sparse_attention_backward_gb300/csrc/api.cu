@@ -20,6 +20,15 @@ constexpr size_t kAlign = 256;
 // deterministic mode stores dS for at most this many bytes of query tokens at
 // once; larger problems run in token chunks
 constexpr int64_t kDsChunkBytes = 16LL << 30;
+// default mode: token windows are sized so one (batch, KV head) window's fp32
+// dQ rows take about this many bytes (they must stay resident in L2 while its
+// key tiles are processed); problems whose whole dQ accumulator is smaller
+// than kWindowMinAcc run without windows
+constexpr int64_t kWindowDqBytes = 48LL << 20;
+// Windows are built but off by default: on GB300 they measured slower than a
+// single pass (the per-window key-tile reloads cost more than the L2 hits of
+// the dQ reductions gained); SELATTN_WINDOW_TOKENS turns them on.
+constexpr int64_t kWindowMinAcc = INT64_MAX;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -27,11 +36,13 @@ struct Plan {
     Geometry g;
     bool fp16, det;
     // byte offsets inside the workspace
-    size_t o_hdr, o_cu_q, o_cu_kv, o_item_base, o_count, o_offset, o_cursor, o_scan, o_entries,
-        o_delta, o_lse2, o_dq_acc, o_ds, o_dkv, total;
+    size_t o_hdr, o_cu_q, o_cu_kv, o_item_base, o_unit_base, o_wtab_base, o_count, o_offset, o_cursor, o_scan,
+        o_entries, o_wtab, o_delta, o_lse2, o_dq_acc, o_ds, o_dkv, total;
     int32_t chunk_tokens, n_chunks;
     bool use_tc;                      // tensor-core main kernel (else the CUDA-core one)
     std::vector<int64_t> item_base;   // host copy, B+1
+    std::vector<int64_t> unit_base;   // host copy, B+1 (windowed)
+    std::vector<int64_t> wtab_base;   // host copy, B+1 (windowed)
 };
 
 sag_status validate(const sag_desc *d) {
@@ -88,17 +99,50 @@ sag_status make_plan(const sag_desc *d, Plan *p) {
 
     const int64_t rows = (int64_t)g.t1 * g.n1;
     const int64_t sel = (int64_t)g.t1 * g.n2 * g.block_count;
+    // SELATTN_FORCE_CUDA_CORE=1 selects the CUDA-core kernel for shapes the
+    // tensor-core one also covers (used to cross-check the two)
+    const char *force = getenv("SELATTN_FORCE_CUDA_CORE");
+    p->use_tc = bwd_tc_supported(g) && !(force && force[0] == '1');
+    g.halves = g.block_size > 64 ? g.block_size / 64 : 1;
+    // token windows: tensor-core default mode on problems whose dQ accumulator
+    // is well beyond L2.  SELATTN_WINDOW_TOKENS sets the window length (and
+    // forces windows on smaller problems too).
+    const char *wenv = getenv("SELATTN_WINDOW_TOKENS");
+    g.windowed = p->use_tc && !p->det && (rows * g.d_qk * 4 > kWindowMinAcc || (wenv && atoll(wenv) > 0));
+    {
+        int64_t wtok = kWindowDqBytes / ((int64_t)g.group * g.d_qk * 4);
+        if (wenv && atoll(wenv) > 0) wtok = atoll(wenv);
+        if (wtok < 1) wtok = 1;
+        if (wtok > kMaxSeq) wtok = kMaxSeq;
+        g.window = (int32_t)wtok;
+    }
+    g.n_units = g.n_items * g.halves;
+    p->unit_base.assign(d->batch + 1, 0);
+    p->wtab_base.assign(d->batch + 1, 0);
+    if (g.windowed) {
+        for (int b = 0; b < d->batch; ++b) {
+            const int64_t s1 = d->cu_seqlens_q[b + 1] - d->cu_seqlens_q[b];
+            const int64_t nwin = (s1 + g.window - 1) / g.window;
+            const int64_t items_b = p->item_base[b + 1] - p->item_base[b];
+            p->unit_base[b + 1] = p->unit_base[b] + nwin * items_b * g.halves;
+            p->wtab_base[b + 1] = p->wtab_base[b] + items_b * (nwin + 1);
+        }
+        g.n_units = p->unit_base[d->batch];
+    }
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
     p->o_hdr = take(sizeof(WsHeader));
     p->o_cu_q = take(sizeof(int32_t) * (g.batch + 1));
     p->o_cu_kv = take(sizeof(int32_t) * (g.batch + 1));
     p->o_item_base = take(sizeof(int64_t) * (g.batch + 1));
+    p->o_unit_base = take(sizeof(int64_t) * (g.batch + 1));
+    p->o_wtab_base = take(sizeof(int64_t) * (g.batch + 1));
     p->o_count = take(sizeof(int32_t) * (g.n_items + 1));
     p->o_cursor = take(sizeof(int32_t) * g.n_items);
     p->o_offset = take(sizeof(int32_t) * (g.n_items + 1));
     p->o_scan = take(sizeof(int32_t) * scan_parts(g.n_items));
     p->o_entries = take(sizeof(int32_t) * sel);
+    p->o_wtab = take(sizeof(int32_t) * (p->wtab_base.empty() ? 0 : p->wtab_base[g.batch]));
     p->o_delta = take(sizeof(float) * rows);
     p->o_lse2 = take(sizeof(float) * rows);
     p->o_dq_acc = p->det ? o : take(sizeof(float) * rows * g.d_qk);
@@ -109,14 +153,10 @@ sag_status make_plan(const sag_desc *d, Plan *p) {
     p->chunk_tokens = p->det ? (int32_t)chunk : g.t1;
     p->n_chunks = p->det ? (int32_t)((g.t1 + chunk - 1) / chunk) : 1;
     p->o_ds = p->det ? take((size_t)ds_per_token * chunk) : o;
-    p->o_dkv = p->n_chunks > 1 ? take(sizeof(float) * (int64_t)g.t2 * g.n2 * (g.d_qk + g.d_v)) : o;
+    p->o_dkv = (p->n_chunks > 1 || g.windowed) ? take(sizeof(float) * (int64_t)g.t2 * g.n2 * (g.d_qk + g.d_v)) : o;
     g.tok_lo = 0;
     g.tok_hi = g.t1;
     g.chunked = p->n_chunks > 1;
-    // SELATTN_FORCE_CUDA_CORE=1 selects the CUDA-core kernel for shapes the
-    // tensor-core one also covers (used to cross-check the two)
-    const char *force = getenv("SELATTN_FORCE_CUDA_CORE");
-    p->use_tc = bwd_tc_supported(g) && !(force && force[0] == '1');
     p->total = o;
     return SAG_OK;
 }
@@ -137,7 +177,10 @@ Workspace carve(const Plan &p, void *base) {
     w.lse2 = reinterpret_cast<float *>(c + p.o_lse2);
     w.dq_acc = p.det ? nullptr : reinterpret_cast<float *>(c + p.o_dq_acc);
     w.ds = p.det ? reinterpret_cast<uint16_t *>(c + p.o_ds) : nullptr;
-    w.dkv_acc = p.n_chunks > 1 ? reinterpret_cast<float *>(c + p.o_dkv) : nullptr;
+    w.dkv_acc = (p.n_chunks > 1 || p.g.windowed) ? reinterpret_cast<float *>(c + p.o_dkv) : nullptr;
+    w.unit_base = reinterpret_cast<int64_t *>(c + p.o_unit_base);
+    w.wtab_base = reinterpret_cast<int64_t *>(c + p.o_wtab_base);
+    w.wtab = reinterpret_cast<int32_t *>(c + p.o_wtab);
     return w;
 }
 
@@ -180,7 +223,7 @@ namespace {
 int launches_of(const Plan &p) {
     // preprocess, histogram, 3 scan passes, fill, sort
     int n = 7;
-    if (!p.det) return n + 2;                        // main, cast dQ
+    if (!p.det) return n + 2 + (p.g.windowed ? 1 : 0);   // main, cast dQ (, cast dK/dV)
     return n + 2 * p.n_chunks + (p.n_chunks > 1);    // (main, dQ) per chunk, cast dK/dV
 }
 }  // namespace
@@ -242,6 +285,8 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
     memcpy(meta.data() + (p.o_cu_q - p.o_cu_q), desc->cu_seqlens_q, sizeof(int32_t) * (g.batch + 1));
     memcpy(meta.data() + (p.o_cu_kv - p.o_cu_q), desc->cu_seqlens_kv, sizeof(int32_t) * (g.batch + 1));
     memcpy(meta.data() + (p.o_item_base - p.o_cu_q), p.item_base.data(), sizeof(int64_t) * (g.batch + 1));
+    memcpy(meta.data() + (p.o_unit_base - p.o_cu_q), p.unit_base.data(), sizeof(int64_t) * (g.batch + 1));
+    memcpy(meta.data() + (p.o_wtab_base - p.o_cu_q), p.wtab_base.data(), sizeof(int64_t) * (g.batch + 1));
 
     cudaError_t e;
     (void)e;
@@ -258,6 +303,9 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
         return SAG_ERR_CUDA;
     if ((e = launch_inversion(g, ws, topk_indices, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
     if (!p.det) {
+        if (g.windowed &&
+            cudaMemsetAsync(ws.dkv_acc, 0, sizeof(float) * (size_t)g.t2 * g.n2 * (g.d_qk + g.d_v), s) != cudaSuccess)
+            return SAG_ERR_CUDA;
         if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return SAG_ERR_CUDA;
         if ((e = p.use_tc ? launch_bwd_tc(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s, sms)
                           : launch_bwd_simt(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s,
@@ -267,6 +315,7 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
         if ((e = launch_cast(ws.dq_acc, dq, (int64_t)g.t1 * g.n1 * g.d_qk, g.scale, p.fp16, s, sms)) !=
             cudaSuccess)
             return SAG_ERR_CUDA;
+        if (g.windowed && (e = launch_cast_dkv(g, ws, dk, dv, p.fp16, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
         return SAG_OK;
     }
     // deterministic: token chunks in order; dS of a chunk -> its dQ

@@ -72,22 +72,49 @@ struct KeyTile {
     int ntiles;
 };
 
-__device__ __forceinline__ KeyTile decode(const Geometry &g, const Workspace &ws, int64_t titem, int halves,
-                                          int nk, int tpt) {
+// Work unit u -> key tile and its bucket entries.  Windowed: units of batch b
+// are ordered (KV head, window, block, half); the bucket range of a window
+// comes from the window table.  Otherwise u = item * halves + half and the
+// range is this launch's token chunk of the bucket.
+__device__ __forceinline__ KeyTile decode(const Geometry &g, const Workspace &ws, int64_t u, int nk, int tpt) {
     KeyTile kt;
-    kt.item = titem / halves;
-    const int half = (int)(titem % halves);
-    kt.b = batch_of_item(ws.item_base, g.batch, kt.item);
-    const int nblk = (ws.cu_kv[kt.b + 1] - ws.cu_kv[kt.b]) / g.block_size;
-    const int64_t local = kt.item - ws.item_base[kt.b];
-    kt.n2 = (int)(local / nblk);
-    const int kb = (int)(local % nblk);
+    const int halves = g.halves;
+    int half, kb, nblk;
+    if (g.windowed) {
+        kt.b = batch_of_item(ws.unit_base, g.batch, u);
+        nblk = (ws.cu_kv[kt.b + 1] - ws.cu_kv[kt.b]) / g.block_size;
+        const int nwin = n_windows(g, ws.cu_q, kt.b);
+        const int64_t local = u - ws.unit_base[kt.b];
+        const int64_t per_head = (int64_t)nwin * nblk * halves;
+        kt.n2 = (int)(local / per_head);
+        const int64_t rem = local % per_head;
+        const int w = (int)(rem / (nblk * halves));
+        const int rem2 = (int)(rem % (nblk * halves));
+        kb = rem2 / halves;
+        half = rem2 % halves;
+        kt.item = ws.item_base[kt.b] + (int64_t)kt.n2 * nblk + kb;
+        const int32_t *tab = ws.wtab + ws.wtab_base[kt.b] + (kt.item - ws.item_base[kt.b]) * (int64_t)(nwin + 1);
+        kt.e0 = tab[w];
+        kt.ntok = tab[w + 1] - kt.e0;
+    } else {
+        kt.item = u / halves;
+        half = (int)(u % halves);
+        kt.b = batch_of_item(ws.item_base, g.batch, kt.item);
+        nblk = (ws.cu_kv[kt.b + 1] - ws.cu_kv[kt.b]) / g.block_size;
+        const int64_t local = kt.item - ws.item_base[kt.b];
+        kt.n2 = (int)(local / nblk);
+        kb = (int)(local % nblk);
+        const int e_end = ws.offset[kt.item + 1];
+        if (g.tok_lo == 0 && g.tok_hi == g.t1) {
+            kt.e0 = ws.offset[kt.item];
+            kt.ntok = e_end - kt.e0;
+        } else {
+            kt.e0 = lower_bound_token(ws.entries, ws.offset[kt.item], e_end, g.tok_lo, g.block_count);
+            kt.ntok = lower_bound_token(ws.entries, kt.e0, e_end, g.tok_hi, g.block_count) - kt.e0;
+        }
+    }
     kt.koff = half * nk;
     kt.key0 = ws.cu_kv[kt.b] + (int64_t)kb * g.block_size + kt.koff;
-    const int e_end = ws.offset[kt.item + 1];
-    kt.e0 = lower_bound_token(ws.entries, ws.offset[kt.item], e_end, g.tok_lo, g.block_count);
-    const int e1 = lower_bound_token(ws.entries, kt.e0, e_end, g.tok_hi, g.block_count);
-    kt.ntok = e1 - kt.e0;
     kt.ntiles = (kt.ntok + tpt - 1) / tpt;
     return kt;
 }
@@ -185,10 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::prefetch_tmap(&map_v);
         }
         const int oob_row = g.t1 * g.n1;   // out of range: the TMA fills zeros
+        // small groups: one box per token would be a single row, so rows are
+        // fetched four at a time (tile::gather4) instead
+        const bool gather = G <= 4 && 4 % G == 0;
         int ne = 0, tc_i = 0;
         bool ok = true;
-        for (int64_t ti = blockIdx.x; ti < A.n_titems && ok; ti += gridDim.x) {
-            const KeyTile kt = decode(g, ws, ti, A.halves, nk, tpt);
+        for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
+            const KeyTile kt = decode(g, ws, ti, nk, tpt);
             if (kt.ntok == 0) continue;
             if (ne > 0 && !tc::mbar_wait(&bars[B_KV_EMPTY], (ne - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
             if (lane == 0) {
@@ -211,10 +241,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) tc::mbar_arrive_expect_tx(&bars[B_Q_FULL0 + s], (uint32_t)tpt * G * DQK * 2);
                 __syncwarp();
                 uint8_t *qdst = smem + L::OFF_Q + s * L::Q_STAGE;
-                for (int tt = lane; tt < tpt; tt += 32) {
-                    const int y = tt < nt ? (m[tt] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
+                if (gather) {
+                    // G in {1, 2, 4}: lane k fetches tile rows 4k..4k+3 with one gather4 per chunk
+                    int y[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int row = 4 * lane + j, tk = row / G;
+                        // rows past the last token re-read the first token's row (their P and dS are 0)
+                        y[j] = (m[tk < nt ? tk : 0] / g.block_count) * g.n1 + kt.n2 * G + row % G;
+                    }
                     for (int c = 0; c < KC; ++c)
-                        tc::tma_load_2d(qdst + c * 16384 + tt * G * 128, &map_q, c * 64, y, &bars[B_Q_FULL0 + s]);
+                        tc::tma_gather4(qdst + c * 16384 + lane * 512, &map_q, c * 64, y[0], y[1], y[2], y[3],
+                                        &bars[B_Q_FULL0 + s]);
+                } else {
+                    for (int tt = lane; tt < tpt; tt += 32) {
+                        const int y = tt < nt ? (m[tt] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
+                        for (int c = 0; c < KC; ++c)
+                            tc::tma_load_2d(qdst + c * 16384 + tt * G * 128, &map_q, c * 64, y, &bars[B_Q_FULL0 + s]);
+                    }
                 }
                 const int d = tc_i % DOS;
                 if (tc_i >= DOS &&
@@ -225,10 +269,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) tc::mbar_arrive_expect_tx(&bars[B_DO_FULL0 + d], (uint32_t)tpt * G * DV * 2);
                 __syncwarp();
                 uint8_t *ddst = smem + L::OFF_DO + d * L::DO_STAGE;
-                for (int tt = lane; tt < tpt; tt += 32) {
-                    const int y = tt < nt ? (m[tt] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
+                if (gather) {
+                    int y[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int row = 4 * lane + j, tk = row / G;
+                        // rows past the last token re-read the first token's row (their P and dS are 0)
+                        y[j] = (m[tk < nt ? tk : 0] / g.block_count) * g.n1 + kt.n2 * G + row % G;
+                    }
                     for (int c = 0; c < 2; ++c)
-                        tc::tma_load_2d(ddst + c * 16384 + tt * G * 128, &map_do, c * 64, y, &bars[B_DO_FULL0 + d]);
+                        tc::tma_gather4(ddst + c * 16384 + lane * 512, &map_do, c * 64, y[0], y[1], y[2], y[3],
+                                        &bars[B_DO_FULL0 + d]);
+                } else {
+                    for (int tt = lane; tt < tpt; tt += 32) {
+                        const int y = tt < nt ? (m[tt] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
+                        for (int c = 0; c < 2; ++c)
+                            tc::tma_load_2d(ddst + c * 16384 + tt * G * 128, &map_do, c * 64, y, &bars[B_DO_FULL0 + d]);
+                    }
                 }
             }
             ++ne;
@@ -243,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t id_q = tc::idesc_f16(kRows, DQK, bf16, false, true);
             int ne = 0, tc_i = 0;
             bool ok = true;
-            for (int64_t ti = blockIdx.x; ti < A.n_titems && ok; ti += gridDim.x) {
-                const KeyTile kt = decode(g, ws, ti, A.halves, nk, tpt);
+            for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
+                const KeyTile kt = decode(g, ws, ti, nk, tpt);
                 if (kt.ntok == 0) continue;
                 if (!tc::mbar_wait(&bars[B_KV_FULL], ne & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 if (ne > 0 && !tc::mbar_wait(&bars[B_ACC_FREE], (ne - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
@@ -312,8 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tt = r / G, gg = r % G;
         int tc_i = 0;
         bool ok = true;
-        for (int64_t ti = blockIdx.x; ti < A.n_titems && ok; ti += gridDim.x) {
-            const KeyTile kt = decode(g, ws, ti, A.halves, nk, tpt);
+        for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
+            const KeyTile kt = decode(g, ws, ti, nk, tpt);
             if (kt.ntok == 0) continue;
             for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
                 const int s = tc_i & 1;
@@ -394,10 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int et = threadIdx.x - 192;                 // 0..127
         int ne = 0, tc_i = 0;
         bool ok = true;
-        for (int64_t ti = blockIdx.x; ti < A.n_titems && ok; ti += gridDim.x) {
-            const KeyTile kt = decode(g, ws, ti, A.halves, nk, tpt);
+        for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
+            const KeyTile kt = decode(g, ws, ti, nk, tpt);
             if (kt.ntok == 0) {
-                if (!g.chunked) {
+                if (!g.chunked && !g.windowed) {
                     for (int i = et; i < nk * (DQK + DV); i += 128) {
                         const int j = i / (DQK + DV), c = i % (DQK + DV);
                         const int64_t row = (kt.key0 + j) * g.n2 + kt.n2;
@@ -456,7 +513,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 16; ++j) {
                     const int64_t row = (kt.key0 + j0 + j) * g.n2 + kt.n2;
                     const float vv = __uint_as_float(av[j]), kv = __uint_as_float(ak[j]);
-                    if (g.chunked) {
+                    if (g.windowed) {
+                        // partial of one token window: other windows add to the same rows
+                        float *acc = ws.dkv_acc + row * (DQK + DV);
+                        atomicAdd(acc + r, kv);
+                        atomicAdd(acc + DQK + r, vv);
+                        if (DQK == 192 && r >= 64) atomicAdd(acc + 64 + r, __uint_as_float(ah[j]));
+                    } else if (g.chunked) {
                         float *acc = ws.dkv_acc + row * (DQK + DV);
                         acc[r] += kv;
                         acc[DQK + r] += vv;
@@ -504,10 +567,12 @@ static cudaError_t launch_tc_t(const Geometry &g, const Workspace &ws, const voi
     a.halves = g.block_size / nk;
     a.tpt = kRows / g.group;
     a.deterministic = det ? 1 : 0;
-    a.n_titems = g.n_items * a.halves;
+    a.n_titems = g.n_units;
     CUtensorMap mq, mdo, mk, mv;
-    if (!tmap_2d(&mq, q, kFp16, DQK, (uint64_t)g.t1 * g.n1, g.group) ||
-        !tmap_2d(&mdo, dy, kFp16, 128, (uint64_t)g.t1 * g.n1, g.group) ||
+    // G in {1, 2, 4}: one-row boxes for tile::gather4; otherwise one box per token (G rows)
+    const uint32_t box_rows = (g.group <= 4 && 4 % g.group == 0) ? 1 : g.group;
+    if (!tmap_2d(&mq, q, kFp16, DQK, (uint64_t)g.t1 * g.n1, box_rows) ||
+        !tmap_2d(&mdo, dy, kFp16, 128, (uint64_t)g.t1 * g.n1, box_rows) ||
         !tmap_3d(&mk, k, kFp16, DQK, g.n2, g.t2, nk) || !tmap_3d(&mv, v, kFp16, 128, g.n2, g.t2, nk))
         return cudaErrorInvalidValue;
     auto fn = k_bwd_tc<kFp16, DQK>;

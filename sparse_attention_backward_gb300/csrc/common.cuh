@@ -55,6 +55,15 @@ struct Geometry {
     float scale_log2;         // scale * log2(e): exp(scale*x - lse) = exp2(x*scale_log2 - lse2)
     int32_t tok_lo, tok_hi;   // query tokens handled by this launch (a chunk, or [0, T1))
     int32_t chunked;          // 1: dK/dV carried across launches in the fp32 accumulator
+    // Token windows (tensor-core default mode): the work of each (batch, KV
+    // head) is split into windows of `window` query tokens, processed window
+    // by window, so that one window's dQ accumulator rows stay in L2.  dK/dV
+    // then arrive as per-window partials, reduced into the fp32 accumulator.
+    int32_t windowed;         // 1: units are (batch, KV head, window, key tile)
+    int32_t window;           // tokens per window
+    int32_t halves;           // key tiles per block (block_size / key tile)
+    int32_t pad_;
+    int64_t n_units;          // work units of the main kernel
 };
 
 // Workspace header (first 256 bytes).
@@ -79,8 +88,17 @@ struct Workspace {
     float *lse2;              // [T1 * n1]  (max + ln sum) * log2(e)
     float *dq_acc;            // [T1 * n1 * d_qk] fp32 dQ accumulator (default mode)
     uint16_t *ds;             // [chunk tokens * n2 * count * G * bs] dS in the input dtype (deterministic)
-    float *dkv_acc;           // [T2 * n2 * (d_qk + d_v)] fp32 dK|dV carried across chunks
+    float *dkv_acc;           // [T2 * n2 * (d_qk + d_v)] fp32 dK|dV carried across chunks / windows
+    int64_t *unit_base;       // [B+1] first work unit of each batch (windowed)
+    int64_t *wtab_base;       // [B+1] first window-table entry of each batch (windowed)
+    int32_t *wtab;            // per item: nwin_b + 1 bucket positions, window starts (windowed)
 };
+
+// Windows of batch b: ceil(S1_b / window).
+__device__ __forceinline__ int n_windows(const Geometry &g, const int32_t *cu_q, int b) {
+    const int s1 = cu_q[b + 1] - cu_q[b];
+    return (s1 + g.window - 1) / g.window;
+}
 
 // First entry of a sorted bucket [lo, hi) whose token is >= t.
 __device__ __forceinline__ int lower_bound_token(const int32_t *e, int lo, int hi, int t, int cnt) {

@@ -201,8 +201,9 @@ __global__ void __launch_bounds__(256) k_fill(Geometry g, Workspace ws,
 // Sort each bucket ascending (token-major order).  Buckets of up to
 // kSortCap entries are sorted in shared memory (bitonic); larger ones by one
 // thread with heapsort in place (rare: needs more than kSortCap selections of
-// one key block).
-constexpr int kSortCap = 8192;
+// one key block).  With token windows, each item then records where every
+// window of its batch starts inside its sorted bucket.
+constexpr int kSortCap = 16384;
 
 __device__ void heap_sort_global(int32_t *a, int n) {
     auto sift = [&](int root, int end) {
@@ -225,35 +226,55 @@ __device__ void heap_sort_global(int32_t *a, int n) {
 }
 
 __global__ void __launch_bounds__(512) k_sort_buckets(Geometry g, Workspace ws) {
-    __shared__ int32_t keys[kSortCap];
+    extern __shared__ int32_t keys[];   // kSortCap entries
     for (int64_t item = blockIdx.x; item < g.n_items; item += gridDim.x) {
         const int off = ws.offset[item];
         const int n = ws.offset[item + 1] - off;
-        if (n <= 1) continue;
         int32_t *a = ws.entries + off;
-        if (n > kSortCap) {
-            if (threadIdx.x == 0) heap_sort_global(a, n);
-            __syncthreads();
-            continue;
-        }
-        int p2 = 1;
-        while (p2 < n) p2 <<= 1;
-        for (int i = threadIdx.x; i < p2; i += blockDim.x) keys[i] = i < n ? a[i] : INT32_MAX;
-        __syncthreads();
-        for (int k = 2; k <= p2; k <<= 1) {
-            for (int j = k >> 1; j > 0; j >>= 1) {
-                for (int i = threadIdx.x; i < p2; i += blockDim.x) {
-                    const int l = i ^ j;
-                    if (l > i) {
-                        const int32_t x = keys[i], y = keys[l];
-                        const bool up = (i & k) == 0;
-                        if ((x > y) == up) { keys[i] = y; keys[l] = x; }
+        const bool in_smem = n <= kSortCap;
+        if (n > 1) {
+            if (!in_smem) {
+                if (threadIdx.x == 0) heap_sort_global(a, n);
+                __syncthreads();
+            } else {
+                int p2 = 1;
+                while (p2 < n) p2 <<= 1;
+                for (int i = threadIdx.x; i < p2; i += blockDim.x) keys[i] = i < n ? a[i] : INT32_MAX;
+                __syncthreads();
+                for (int k = 2; k <= p2; k <<= 1) {
+                    for (int j = k >> 1; j > 0; j >>= 1) {
+                        for (int i = threadIdx.x; i < p2; i += blockDim.x) {
+                            const int l = i ^ j;
+                            if (l > i) {
+                                const int32_t x = keys[i], y = keys[l];
+                                const bool up = (i & k) == 0;
+                                if ((x > y) == up) { keys[i] = y; keys[l] = x; }
+                            }
+                        }
+                        __syncthreads();
                     }
                 }
-                __syncthreads();
+                for (int i = threadIdx.x; i < n; i += blockDim.x) a[i] = keys[i];
+            }
+        } else if (n == 1) {
+            if (threadIdx.x == 0) keys[0] = a[0];
+        }
+        __syncthreads();
+        if (g.windowed) {
+            const int b = batch_of_item(ws.item_base, g.batch, item);
+            const int nwin = n_windows(g, ws.cu_q, b);
+            const int32_t *src = in_smem ? keys : a;
+            int32_t *tab = ws.wtab + ws.wtab_base[b] + (item - ws.item_base[b]) * (int64_t)(nwin + 1);
+            for (int w = threadIdx.x; w <= nwin; w += blockDim.x) {
+                const int t0 = ws.cu_q[b] + w * g.window;   // first token of window w
+                int lo = 0, hi = n;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (src[mid] / g.block_count < t0) lo = mid + 1; else hi = mid;
+                }
+                tab[w] = off + lo;
             }
         }
-        for (int i = threadIdx.x; i < n; i += blockDim.x) a[i] = keys[i];
         __syncthreads();
     }
 }
@@ -313,7 +334,9 @@ cudaError_t launch_inversion(const Geometry &g, const Workspace &ws, const int32
     k_scan_apply<<<parts, kScanBlock, 0, s>>>(ws.count, g.n_items, ws.scan_part, ws.offset);
     if (sel > 0) {
         k_fill<<<grid_for(sel, 256, num_sms * 8), 256, 0, s>>>(g, ws, topk);
-        k_sort_buckets<<<grid_for(g.n_items, 1, num_sms * 4), 512, 0, s>>>(g, ws);
+        cudaFuncSetAttribute(k_sort_buckets, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kSortCap * sizeof(int32_t)));
+        k_sort_buckets<<<grid_for(g.n_items, 1, num_sms * 4), 512, kSortCap * sizeof(int32_t), s>>>(g, ws);
     }
     return cudaGetLastError();
 }

@@ -93,6 +93,43 @@ def test_full_parity_small(small_data, name, deterministic):
     assert np.all(S.f64(dk)[unsel] == 0) and np.all(S.f64(dv)[unsel] == 0)
 
 
+@pytest.mark.parametrize("window", [37, 300])
+@pytest.mark.parametrize("name", ["varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127"])
+def test_token_windows_parity(small_data, name, window, monkeypatch):
+    """Default mode with the work split into token windows (dK/dV as partials)."""
+    monkeypatch.setenv("SELATTN_WINDOW_TOKENS", str(window))
+    w, x, (rdq, rdk, rdv) = small_data(name)
+    desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
+                         sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, False)
+    assert sab.plan_info(desc).launches == 10   # windowed: the dK/dV cast runs too
+    dq, dk, dv = _run(w, x, False)
+    S.assert_close(f"{name} w{window} dq", S.f64(dq), rdq)
+    S.assert_close(f"{name} w{window} dk", S.f64(dk), rdk)
+    S.assert_close(f"{name} w{window} dv", S.f64(dv), rdv)
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("name", ["tiny", "varlen", "g32_bs128"])
+def test_cuda_core_kernel_parity(small_data, name, deterministic, monkeypatch):
+    """The CUDA-core kernel on shapes the tensor-core kernel also takes."""
+    monkeypatch.setenv("SELATTN_FORCE_CUDA_CORE", "1")
+    w, x, (rdq, rdk, rdv) = small_data(name)
+    desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
+                         sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, deterministic)
+    assert sab.plan_info(desc).main_kernel == 0
+    dq, dk, dv = _run(w, x, deterministic)
+    S.assert_close(f"{name} cuda-core dq", S.f64(dq), rdq)
+    S.assert_close(f"{name} cuda-core dk", S.f64(dk), rdk)
+    S.assert_close(f"{name} cuda-core dv", S.f64(dv), rdv)
+
+
+def test_tensor_core_kernel_is_selected():
+    for w in synth.WORKLOADS:
+        desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count,
+                             w.scale, sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, False)
+        assert sab.plan_info(desc).main_kernel == 1, w.name
+
+
 def test_duplicate_ids_count_twice():
     w = SMALL["tiny"].with_(name="dups", cu_q=(0, 20), cu_kv=(0, 128), n1=4, n2=2, block_size=16,
                            block_count=4, seed=15)
