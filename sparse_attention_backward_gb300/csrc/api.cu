@@ -331,7 +331,9 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
                           : launch_bwd_simt(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s,
                                             sms)) != cudaSuccess)
             return SAG_ERR_CUDA;
-        if ((e = launch_dq_from_ds(gc, ws, key, topk_indices, dq, p.fp16, s, sms)) != cudaSuccess)
+        if ((e = (p.use_tc && dq_tc_supported(gc)) ? launch_dq_tc(gc, ws, key, topk_indices, dq, p.fp16, s, sms)
+                                                    : launch_dq_from_ds(gc, ws, key, topk_indices, dq, p.fp16, s, sms)) !=
+            cudaSuccess)
             return SAG_ERR_CUDA;
     }
     if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SAG_ERR_CUDA;

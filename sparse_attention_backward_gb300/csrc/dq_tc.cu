@@ -1,0 +1,266 @@
+// Deterministic dQ on the tensor cores, from the dS the main kernel stored.
+//
+// dQ[t, n2*G + g] = scale * sum_slot sum_r dS[t][n2][slot][g][r] * K[row(slot, r), n2]
+// ("NsaSelectedAttentionGrad" README, function description: dQ = dS K / sqrt(d)
+// over the gathered rows).  One (token, KV head) pair at a time:
+//     dQ^T [Dqk x G] += K_slot^T [Dqk x bs] . dS_slot^T [bs x G]
+// as tcgen05.mma with M = Dqk rows (128, or 128 + the [64,192) half for 192),
+// N = G rounded up to 16 (columns past G are never read), K = bs keys; slots
+// and keys are accumulated in one fixed order, so the result is the same
+// bits on every run.  A persistent CTA: warp 0 loads each slot's key block and
+// dS tile with TMA into a 3-stage ring, warp 1 issues the MMAs into one of
+// two TMEM accumulators, warps 2-5 read the finished accumulator and write dQ.
+#include "kernels.cuh"
+#include "tc.cuh"
+#include "tmap.cuh"
+
+namespace sag {
+namespace {
+
+constexpr int kDqThreads = 192;
+constexpr int kStages = 3;
+constexpr uint64_t kDqWaitNs = 2000000000ull;
+
+template <int DQK, int BS>
+struct DqSmem {
+    static constexpr int KC = DQK / 64;
+    static constexpr int K_BYTES = KC * BS * 128;          // K block: KC chunks of BS rows x 128 B
+    static constexpr int DS_CHUNKS = BS / 64;
+    static constexpr int DS_BYTES = DS_CHUNKS * 32 * 128;  // dS tile: chunks of 32 rows x 128 B
+    static constexpr int STAGE = K_BYTES + DS_BYTES;
+    static constexpr int OFF_BAR = kStages * STAGE;
+    static constexpr int TOTAL = OFF_BAR + 256 + 1024;
+};
+
+enum DqBar { D_FULL0 = 0, D_EMPTY0 = kStages, D_ACC_FULL0 = 2 * kStages, D_ACC_FREE0 = 2 * kStages + 2,
+             D_COUNT = 2 * kStages + 4 };
+
+struct DqArgs {
+    Geometry g;
+    Workspace ws;
+    const int32_t *topk;
+    uint16_t *dq;
+    int n_pad;          // G rounded up to a multiple of 16
+};
+
+__device__ __forceinline__ bool slot_ok(const Geometry &g, const Workspace &ws, const int32_t *topk,
+                                        int64_t pair, int slot, int nblk) {
+    const int id = __ldg(topk + pair * g.block_count + slot);
+    return id >= 0 && id < nblk;
+}
+
+template <bool kFp16, int DQK, int BS>
+__global__ void __launch_bounds__(kDqThreads, 1)
+    k_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_ds, DqArgs A) {
+    using L = DqSmem<DQK, BS>;
+    constexpr int KC = L::KC;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_BAR + 8 * D_COUNT);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_BAR + 8 * D_COUNT + 4);
+    const Geometry &g = A.g;
+    const Workspace &ws = A.ws;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = g.group;
+    const int64_t npairs = (int64_t)(g.tok_hi - g.tok_lo) * g.n2;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(&bars[D_FULL0 + s], 1);
+            tc::mbar_init(&bars[D_EMPTY0 + s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&bars[D_ACC_FULL0 + b], 1);
+            tc::mbar_init(&bars[D_ACC_FREE0 + b], 128);
+        }
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 128);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        raise_error(&ws.hdr->error, SAG_ERR_TIMEOUT);
+    };
+    // accumulator b: dims [0,128) at column 64*b, dims [64,192) at 64*b + 32
+    auto acc_col = [&](int b, int hi) { return (uint32_t)(64 * b + 32 * hi); };
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tc::prefetch_tmap(&map_k);
+            tc::prefetch_tmap(&map_ds);
+            int it = 0;
+            bool ok = true;
+            for (int64_t cp = blockIdx.x; cp < npairs && ok; cp += gridDim.x) {
+                const int t = g.tok_lo + (int)(cp / g.n2), n2 = (int)(cp % g.n2);
+                const int64_t pair = (int64_t)t * g.n2 + n2;
+                const int b = batch_of(ws.cu_q, g.batch, t);
+                const int nblk = (ws.cu_kv[b + 1] - ws.cu_kv[b]) / g.block_size;
+                for (int slot = 0; slot < g.block_count; ++slot) {
+                    if (!slot_ok(g, ws, A.topk, pair, slot, nblk)) continue;
+                    const int s = it % kStages;
+                    if (it >= kStages &&
+                        !tc::mbar_wait(&bars[D_EMPTY0 + s], ((it / kStages) - 1) & 1, abort_flag, kDqWaitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const int id = __ldg(A.topk + pair * g.block_count + slot);
+                    const int key0 = ws.cu_kv[b] + id * BS;
+                    uint8_t *st = smem + s * L::STAGE;
+                    tc::mbar_arrive_expect_tx(&bars[D_FULL0 + s], (uint32_t)(BS * DQK * 2 + G * BS * 2));
+                    for (int c = 0; c < KC; ++c)
+                        tc::tma_load_3d(st + c * BS * 128, &map_k, c * 64, n2, key0, &bars[D_FULL0 + s]);
+                    const int dsrow = (int)(((int64_t)cp * g.block_count + slot) * G);
+                    for (int c = 0; c < L::DS_CHUNKS; ++c)
+                        tc::tma_load_2d(st + L::K_BYTES + c * 4096, &map_ds, c * 64, dsrow, &bars[D_FULL0 + s]);
+                    ++it;
+                }
+            }
+            if (!ok) fail();
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_f16(128, A.n_pad, !kFp16, true, false);
+            int it = 0, np = 0;
+            bool ok = true;
+            for (int64_t cp = blockIdx.x; cp < npairs && ok; cp += gridDim.x, ++np) {
+                const int t = g.tok_lo + (int)(cp / g.n2), n2 = (int)(cp % g.n2);
+                const int64_t pair = (int64_t)t * g.n2 + n2;
+                const int b = batch_of(ws.cu_q, g.batch, t);
+                const int nblk = (ws.cu_kv[b + 1] - ws.cu_kv[b]) / g.block_size;
+                const int ab = np & 1;
+                if (np >= 2 && !tc::mbar_wait(&bars[D_ACC_FREE0 + ab], ((np >> 1) - 1) & 1, abort_flag, kDqWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                bool first = true;
+                for (int slot = 0; slot < g.block_count; ++slot) {
+                    if (!slot_ok(g, ws, A.topk, pair, slot, nblk)) continue;
+                    const int s = it % kStages;
+                    if (!tc::mbar_wait(&bars[D_FULL0 + s], (it / kStages) & 1, abort_flag, kDqWaitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint32_t kst = tc::smem_u32(smem + s * L::STAGE);
+                    const uint32_t dst = kst + L::K_BYTES;
+                    for (int kk = 0; kk < BS / 16; ++kk) {
+                        // A = K^T (dims x keys, MN-major), B = dS^T (keys x G, K-major)
+                        const uint64_t bdesc = tc::sw128_desc(dst + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024);
+                        tc::mma_f16_ss(tmem + acc_col(ab, 0), tc::sw128_desc(kst + kk * 2048, BS * 128, 1024), bdesc,
+                                       idesc, !first || kk > 0);
+                        if (DQK == 192)
+                            tc::mma_f16_ss(tmem + acc_col(ab, 1),
+                                           tc::sw128_desc(kst + BS * 128 + kk * 2048, BS * 128, 1024), bdesc, idesc,
+                                           !first || kk > 0);
+                    }
+                    tc::mma_commit(&bars[D_EMPTY0 + s]);
+                    first = false;
+                    ++it;
+                }
+                if (!ok) break;
+                tc::mma_commit(&bars[D_ACC_FULL0 + ab]);
+            }
+            if (!ok) fail();
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int q4 = warp & 3;
+        const int d = q4 * 32 + lane;                  // TMEM lane = head dim
+        const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+        int np = 0;
+        bool ok = true;
+        for (int64_t cp = blockIdx.x; cp < npairs && ok; cp += gridDim.x, ++np) {
+            const int t = g.tok_lo + (int)(cp / g.n2), n2 = (int)(cp % g.n2);
+            const int64_t pair = (int64_t)t * g.n2 + n2;
+            const int b = batch_of(ws.cu_q, g.batch, t);
+            const int nblk = (ws.cu_kv[b + 1] - ws.cu_kv[b]) / g.block_size;
+            int nvalid = 0;
+            for (int slot = 0; slot < g.block_count; ++slot) nvalid += slot_ok(g, ws, A.topk, pair, slot, nblk);
+            const int ab = np & 1;
+            const bool w = tc::mbar_wait(&bars[D_ACC_FULL0 + ab], (np >> 1) & 1, abort_flag, kDqWaitNs);
+            ok = __all_sync(0xffffffffu, w);
+            if (!ok) break;
+            tc::tc_fence_after();
+            uint16_t *dqrow = A.dq + ((int64_t)t * g.n1 + (int64_t)n2 * G) * DQK;
+            for (int g0 = 0; g0 < G; g0 += 16) {
+                uint32_t lo[16], hi[16];
+                tc::tmem_ld16(trow + acc_col(ab, 0) + g0, lo);
+                if (DQK == 192) tc::tmem_ld16(trow + acc_col(ab, 1) + g0, hi);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    if (g0 + j >= G) break;
+                    const float vlo = nvalid ? __uint_as_float(lo[j]) : 0.f;
+                    dqrow[(int64_t)(g0 + j) * DQK + d] = f_to_u16<kFp16>(vlo * g.scale);
+                    if (DQK == 192 && d >= 64) {
+                        const float vhi = nvalid ? __uint_as_float(hi[j]) : 0.f;
+                        dqrow[(int64_t)(g0 + j) * DQK + 64 + d] = f_to_u16<kFp16>(vhi * g.scale);
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&bars[D_ACC_FREE0 + ab]);
+        }
+        if (!ok) fail();
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 128);
+    }
+}
+
+template <bool kFp16, int DQK, int BS>
+static cudaError_t launch_dq_tc_t(const Geometry &g, const Workspace &ws, const void *k, const int32_t *topk,
+                                  void *dq, cudaStream_t s, int num_sms) {
+    const int64_t npairs = (int64_t)(g.tok_hi - g.tok_lo) * g.n2;
+    if (npairs == 0) return cudaSuccess;
+    DqArgs a;
+    a.g = g;
+    a.ws = ws;
+    a.topk = topk;
+    a.dq = (uint16_t *)dq;
+    a.n_pad = (g.group + 15) / 16 * 16;
+    CUtensorMap mk, mds;
+    const uint64_t ds_rows = (uint64_t)npairs * g.block_count * g.group;
+    if (!tmap_3d(&mk, k, kFp16, DQK, g.n2, g.t2, BS) || !tmap_2d(&mds, ws.ds, kFp16, BS, ds_rows, g.group))
+        return cudaErrorInvalidValue;
+    auto fn = k_dq_tc<kFp16, DQK, BS>;
+    const int smem = DqSmem<DQK, BS>::TOTAL;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = npairs < num_sms ? npairs : num_sms;
+    fn<<<(int)grid, kDqThreads, smem, s>>>(mk, mds, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool dq_tc_supported(const Geometry &g) {
+    return (g.d_qk == 128 || g.d_qk == 192) && (g.block_size == 64 || g.block_size == 128) && g.group <= 32;
+}
+
+cudaError_t launch_dq_tc(const Geometry &g, const Workspace &ws, const void *k, const int32_t *topk, void *dq,
+                         bool fp16, cudaStream_t s, int num_sms) {
+#define SAG_DQ_CASE(F, D, B)                                                                 \
+    if (fp16 == F && g.d_qk == D && g.block_size == B) return launch_dq_tc_t<F, D, B>(g, ws, k, topk, dq, s, num_sms);
+    SAG_DQ_CASE(false, 192, 64) SAG_DQ_CASE(false, 192, 128) SAG_DQ_CASE(false, 128, 64)
+    SAG_DQ_CASE(false, 128, 128) SAG_DQ_CASE(true, 192, 64) SAG_DQ_CASE(true, 192, 128)
+    SAG_DQ_CASE(true, 128, 64) SAG_DQ_CASE(true, 128, 128)
+#undef SAG_DQ_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace sag

@@ -28,6 +28,11 @@ cudaError_t launch_bwd_tc(const Geometry &g, const Workspace &ws, const void *q,
 // dK/dV from the fp32 accumulator after the last token chunk.
 cudaError_t launch_cast_dkv(const Geometry &g, const Workspace &ws, void *dk, void *dv, bool fp16,
                             cudaStream_t s, int num_sms);
+// Tensor-core dQ from the stored dS, fixed order (deterministic mode):
+// d_qk in {128, 192}, block size 64 or 128.
+bool dq_tc_supported(const Geometry &g);
+cudaError_t launch_dq_tc(const Geometry &g, const Workspace &ws, const void *k, const int32_t *topk, void *dq,
+                         bool fp16, cudaStream_t s, int num_sms);
 // dQ from the stored dS, fixed order (deterministic mode).
 cudaError_t launch_dq_from_ds(const Geometry &g, const Workspace &ws, const void *k,
                               const int32_t *topk, void *dq, bool fp16, cudaStream_t s, int num_sms);
