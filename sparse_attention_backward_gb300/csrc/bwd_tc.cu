@@ -125,9 +125,17 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// a in the low half, b in the high half, both rounded to nearest even (one
+// paired conversion instead of two scalar ones)
 template <bool kFp16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
-    return (uint32_t)f_to_u16<kFp16>(a) | ((uint32_t)f_to_u16<kFp16>(b) << 16);
+    if constexpr (kFp16) {
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
 }
 
 // address of 16-byte chunk c of row r in a 128-byte-swizzled [rows x 128 B] tile
