@@ -184,8 +184,6 @@ def time_oracle(w, x, budget_s, seed=0):
 
 
 def run_reference(args, w, rank, world):
-    if rank != 0:
-        return
     x = synth.make_inputs(w, device="cpu" if w.t1 * w.n1 * w.d_qk < (1 << 27) else "cuda")
     if "o" not in x:
         x.update(synth.synthetic_forward_stats(w, torch.Generator(device=x["q"].device).manual_seed(w.seed + 7),
@@ -218,6 +216,32 @@ def workload_config(w, det):
             else "L2 flushed between steps (256 MB write)"}
 
 
+# ------------------------------------------------------------ ranks (weak scaling)
+def rank_seed(w, rank: int) -> int:
+    """Each rank draws its own independent problem of the full workload size."""
+    return w.seed + rank
+
+
+def max_over_ranks(v: float, device) -> float:
+    """The slowest rank's time (identity without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job TFLOP/s: every rank's work over the slowest rank's time."""
+    return flops_per_rank * world / (ms * 1e-3) / 1e12
+
+
+def runs_reference(rank: int) -> bool:
+    """The reference arm (the oracle on host cores) runs on rank 0 only."""
+    return rank == 0
+
+
 # --------------------------------------------------------------------- ours
 def main():
     args = parse()
@@ -229,9 +253,8 @@ def main():
         cu = tuple(args.seq * i for i in range(w.batch + 1))
         w = w.with_(name=f"{w.name}_seq{args.seq}", cu_q=cu, cu_kv=cu)
     if args.impl == "reference":
-        if world > 1 and rank != 0:
-            return
-        run_reference(args, w, rank, world)
+        if runs_reference(rank):
+            run_reference(args, w, rank, world)
         return
 
     import sparse_attention_backward_gb300 as sab
@@ -241,9 +264,9 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    x = synth.make_inputs(w, device=dev, seed=w.seed + rank)
+    x = synth.make_inputs(w, device=dev, seed=rank_seed(w, rank))
     if "o" not in x:   # workloads whose stats normally come from a forward
-        g = torch.Generator(device=dev).manual_seed(w.seed + 7 + rank)
+        g = torch.Generator(device=dev).manual_seed(rank_seed(w, rank) + 7)
         x.update(synth.synthetic_forward_stats(w, g, dev))
     stream = torch.cuda.current_stream(dev)
     desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count,
@@ -292,13 +315,10 @@ def main():
         torch.distributed.barrier()
     ms = t0.elapsed_time(t1) / K
     main_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(mk0, mk1))
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
 
     flops = w.flops()
-    value = flops * world / (ms * 1e-3) / 1e12
+    value = job_throughput(flops, world, ms)
     pk, pk_src = peaks()
     peak = float(pk["bf16_tflops"])
     roofline_ms = max(flops / (peak * 1e12), w.algorithmic_bytes() / (float(pk["hbm_gbs"]) * 1e9)) * 1e3
@@ -329,11 +349,8 @@ def main():
         b.record(stream)
         torch.cuda.synchronize()
         ems = a.elapsed_time(b) / ke
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": flops * world / (ems * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ems,
+        ems = max_over_ranks(ems, dev)
+        e2e = {"value": job_throughput(flops, world, ems), "unit": "TFLOP/s", "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None
