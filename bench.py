@@ -65,6 +65,27 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
+def host_cpu() -> str:
+    """Host CPU model as /proc/cpuinfo names it (Arm parts by implementer / part id)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return "unknown CPU"
+    for key in ("model name", "Model"):
+        for line in info.splitlines():
+            if line.split(":")[0].strip() == key:
+                return line.split(":", 1)[1].strip()
+    impl = part = None
+    for line in info.splitlines():
+        k = line.split(":")[0].strip()
+        if k == "CPU implementer" and impl is None:
+            impl = line.split(":", 1)[1].strip()
+        elif k == "CPU part" and part is None:
+            part = line.split(":", 1)[1].strip()
+    return f"Arm CPU implementer {impl} part {part}" if impl else "unknown CPU"
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for p in sorted(glob.glob(os.path.join(ROOT, "sparse_attention_backward_gb300", "csrc", "*"))):
@@ -198,7 +219,7 @@ def run_reference(args, w, rank, world):
         times.append(dt)
     value = statistics.median(vals)
     sample = (f"{n} query tokens x {w.group} heads of KV head 0, batch 0 (full backward of those rows) "
-              f"per step, ~{per_step:.1f} s each")
+              f"per step, ~{per_step:.1f} s each, one core of {host_cpu()} ({os.cpu_count()} cores)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -358,7 +379,7 @@ def main():
         v, dt, n = time_oracle(w, x, args.cpu_seconds)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                "sample": f"{n} query tokens x {w.group} heads (KV head 0, batch 0), full backward of those "
-                         f"rows, {dt:.1f} s on one host core"}
+                         f"rows, {dt:.1f} s on one core of {host_cpu()} ({os.cpu_count()} cores)"}
 
     if rank == 0:
         traffic = profiled_traffic(w.name, args.deterministic)
@@ -371,6 +392,8 @@ def main():
             "roofline_ms": roofline_ms,
             "roofline": {"bound": "tensor", "kernel": "main backward", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": f"{pk_src} bf16 burst",
+                         "peak_sustained": float(pk.get("bf16_tflops_sustained", peak)),
+                         "frac_sustained": achieved / float(pk.get("bf16_tflops_sustained", peak)),
                          "kernel_ms": main_ms, "traffic": traffic},
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(info.launches) * K,
