@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
+    ap.add_argument("--forward", action="store_true",
+                    help="time the selected-attention forward (O and the softmax stats) instead")
     ap.add_argument("--seq", type=int, default=0,
                     help="override every batch's query and key length (smaller profiling captures)")
     return ap.parse_args()
@@ -188,18 +190,26 @@ def oracle_sample(w, x, n_tokens, rng):
     return p, flops, len(toks)
 
 
-def time_oracle(w, x, budget_s, seed=0):
+def fwd_flops(w, n_rows) -> float:
+    """Forward: 2 * L * (d_qk + d_v) per query head per token (S and P V)."""
+    return 2.0 * w.selected_keys * (w.d_qk + w.d_v) * n_rows
+
+
+def time_oracle(w, x, budget_s, seed=0, forward=False):
     """TFLOP/s of the oracle on a sample sized to about budget_s seconds."""
     import oracle
+    run = oracle.forward if forward else oracle.backward
     rng = np.random.default_rng(seed)
     p, f, n = oracle_sample(w, x, 1, rng)
     t0 = time.perf_counter()
-    oracle.backward(p)
+    run(p)
     per_token = max(1e-4, time.perf_counter() - t0)
     n = max(1, int(budget_s / per_token))
     p, f, n = oracle_sample(w, x, n, rng)
+    if forward:
+        f = fwd_flops(w, n * w.group)
     t0 = time.perf_counter()
-    oracle.backward(p)
+    run(p)
     dt = time.perf_counter() - t0
     return f / dt / 1e12, dt, n
 
@@ -290,6 +300,9 @@ def main():
         g = torch.Generator(device=dev).manual_seed(rank_seed(w, rank) + 7)
         x.update(synth.synthetic_forward_stats(w, g, dev))
     stream = torch.cuda.current_stream(dev)
+    if args.forward:
+        run_forward(args, w, x, dev, stream, world, rank, local)
+        return
     desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count,
                          w.scale, sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, args.deterministic)
     info = sab.plan_info(desc)
@@ -398,6 +411,103 @@ def main():
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(info.launches) * K,
             "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_forward(args, w, x, dev, stream, world, rank, local):
+    """The forward: both tensor-core passes timed with events, the whole call
+    (init, inversion, passes, finalize) timed per step."""
+    import sparse_attention_backward_gb300 as sab
+    desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count,
+                         w.scale, sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, False)
+    need = sab.fwd_workspace_size(desc)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    o = torch.empty((w.t1, w.n1, w.d_v), dtype=x["q"].dtype, device=dev)
+    smax = torch.empty((w.t1, w.n1, 8), dtype=torch.float32, device=dev)
+    ssum = torch.empty_like(smax)
+    ins = [x[k] for k in ("q", "k", "v", "topk")]
+    outs = [o, smax, ssum]
+
+    def call(ev0=None, ev1=None):
+        sab.sel_attn_fwd(desc, *[t.data_ptr() for t in ins], *[t.data_ptr() for t in outs], ws.data_ptr(), need,
+                         stream.cuda_stream, ev0.cuda_event if ev0 is not None else None,
+                         ev1.cuda_event if ev1 is not None else None)
+
+    for _ in range(args.warmup):
+        call()
+    st = sab.query_error(ws.data_ptr(), stream.cuda_stream)
+    if st != sab.SAG_OK:
+        raise sab.SagError(st, "device")
+    K = args.steps
+    mk0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    mk1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in mk0 + mk1:
+        e.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    t0.record(stream)
+    for i in range(K):
+        call(mk0[i], mk1[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1) / K, dev)
+    pass_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(mk0, mk1))
+    flops = fwd_flops(w, w.t1 * w.n1)
+    pk, pk_src = peaks()
+    peak = float(pk["bf16_tflops"])
+    achieved = flops / (pass_ms * 1e-3) / 1e12
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.cpu().pin_memory() for t in ins]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def e2e_step():
+            for d, h in zip(ins, host_in):
+                d.copy_(h, non_blocking=True)
+            call()
+            for h, d in zip(host_out, outs):
+                h.copy_(d, non_blocking=True)
+        for _ in range(max(1, min(args.warmup, 3))):
+            e2e_step()
+        torch.cuda.synchronize()
+        ke = max(3, min(K, 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(a.elapsed_time(b) / ke, dev)
+        e2e = {"value": job_throughput(flops, world, ems), "unit": "TFLOP/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, n = time_oracle(w, x, args.cpu_seconds, forward=True)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} query tokens x {w.group} heads (KV head 0, batch 0), forward of those rows, "
+                         f"{dt:.1f} s on one core of {host_cpu()} ({os.cpu_count()} cores)"}
+    if rank == 0:
+        line = {
+            "metric": "selected-attn forward TFLOP/s and % of GB300 bf16 roofline; ms per call",
+            "value": job_throughput(flops, world, ms), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": dict(workload_config(w, False), mode="forward"),
+            "roofline": {"bound": "tensor", "kernel": "forward passes (max, sum + P V)", "achieved": achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{pk_src} bf16 burst", "kernel_ms": pass_ms, "traffic": None},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 10 * K, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

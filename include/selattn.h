@@ -212,6 +212,54 @@ sag_status sel_attn_grad_noalloc(const sag_desc *desc, const void *query, const 
                                  const float *softmax_sum, const int32_t *topk_indices, void *dq,
                                  void *dk, void *dv, void *stream);
 
+/*
+ * Forward of selected attention: the step before the backward, producing the
+ * attention_out, softmax_max and softmax_sum it takes ("NsaSelectedAttention-
+ * Grad" README, parameter table: the forward's outputs; the attention is the
+ * softmax(scale Q Ksel^T) Vsel of its function description over the rows the
+ * Gather formula selects, and the statistics follow the FlashAttention
+ * convention of "aclnnFlashAttentionUnpaddingScoreGradV3": the maximum of the
+ * scaled scores and the sum of exp(score - maximum)).
+ *
+ * Phase 1 (host only): validates `desc` as sel_attn_grad_workspace_size does
+ * and writes the forward's workspace size.  The forward runs on the tensor
+ * cores only: d_v == 128, d_qk in {128, 192}, block_size in {16, 32, 48, 64,
+ * 128}; other shapes return SAG_ERR_UNSUPPORTED, and so does
+ * desc->deterministic == 1 (the sums and O are reduced in an order that
+ * varies from run to run; the maxima are exact in any order).
+ */
+sag_status sel_attn_fwd_workspace_size(const sag_desc *desc, size_t *workspace_bytes);
+
+/*
+ * Phase 2: enqueues the forward on `stream` and returns without waiting.
+ *   query          [T1, n1, d_qk]          dtype
+ *   key            [T2, n2, d_qk]          dtype
+ *   value          [T2, n2, d_v]           dtype
+ *   topk_indices   [T1, n2, block_count]   int32, block ids local to the
+ *                  token's batch (as for sel_attn_grad)
+ *   attention_out  [T1, n1, d_v]           dtype, written
+ *   softmax_max    [T1, n1, 8]             fp32, written (8 equal lanes)
+ *   softmax_sum    [T1, n1, 8]             fp32, written (8 equal lanes)
+ *   workspace      device scratch of at least the forward's phase-1 size
+ * All pointers are device pointers, 16-byte aligned; the caller owns every
+ * buffer.  Returns SAG_OK once enqueued, a host-side status (nothing
+ * enqueued), or SAG_ERR_CUDA when a launch failed; out-of-range block ids are
+ * recorded on the device (sel_attn_grad_query_error) and skipped.
+ */
+sag_status sel_attn_fwd(const sag_desc *desc, const void *query, const void *key, const void *value,
+                        const int32_t *topk_indices, void *attention_out, float *softmax_max,
+                        float *softmax_sum, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * sel_attn_fwd with two optional cudaEvent_t handles recorded just before
+ * the first and just after the second tensor-core pass (NULL = not recorded).
+ */
+sag_status sel_attn_fwd_timed(const sag_desc *desc, const void *query, const void *key,
+                              const void *value, const int32_t *topk_indices, void *attention_out,
+                              float *softmax_max, float *softmax_sum, void *workspace,
+                              size_t workspace_bytes, void *stream, void *passes_start,
+                              void *passes_stop);
+
 /* Static, human-readable name of a status code. */
 const char *sel_attn_grad_status_string(int status);
 

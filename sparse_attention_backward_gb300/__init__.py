@@ -23,7 +23,8 @@ SAG_ERR_WORKSPACE, SAG_ERR_ALIGN, SAG_ERR_CUDA, SAG_ERR_INDEX, SAG_ERR_TIMEOUT =
 SAG_BF16, SAG_FP16 = 0, 1
 
 EXPORTED = ("sel_attn_grad_workspace_size", "sel_attn_grad", "sel_attn_grad_timed",
-            "sel_attn_grad_plan_info", "sel_attn_grad_query_error", "sel_attn_grad_status_string")
+            "sel_attn_grad_plan_info", "sel_attn_grad_query_error", "sel_attn_grad_status_string",
+            "sel_attn_fwd_workspace_size", "sel_attn_fwd", "sel_attn_fwd_timed")
 
 
 class SagDesc(ctypes.Structure):
@@ -76,6 +77,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sel_attn_grad_plan_info.restype = ctypes.c_int
     lib.sel_attn_grad_query_error.argtypes = [vp, vp]
     lib.sel_attn_grad_query_error.restype = ctypes.c_int
+    lib.sel_attn_fwd_workspace_size.argtypes = [D, ctypes.POINTER(sz)]
+    lib.sel_attn_fwd_workspace_size.restype = ctypes.c_int
+    lib.sel_attn_fwd.argtypes = [D] + [vp] * 7 + [vp, sz, vp]
+    lib.sel_attn_fwd.restype = ctypes.c_int
+    lib.sel_attn_fwd_timed.argtypes = [D] + [vp] * 7 + [vp, sz, vp, vp, vp]
+    lib.sel_attn_fwd_timed.restype = ctypes.c_int
     lib.sel_attn_grad_status_string.argtypes = [ctypes.c_int]
     lib.sel_attn_grad_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -180,3 +187,62 @@ def backward(q, k, v, o, dy, softmax_max, softmax_sum, topk, cu_seqlens_q, cu_se
         if st != SAG_OK:
             raise SagError(st, "device")
     return dq, dk, dv
+
+
+def fwd_workspace_size(desc: SagDesc) -> int:
+    """Forward phase 1: validate and return the forward's workspace size."""
+    n = ctypes.c_size_t(0)
+    st = load().sel_attn_fwd_workspace_size(ctypes.byref(desc), ctypes.byref(n))
+    if st != SAG_OK:
+        raise SagError(st, "sel_attn_fwd_workspace_size")
+    return n.value
+
+
+def sel_attn_fwd(desc: SagDesc, query, key, value, topk_indices, attention_out, softmax_max,
+                 softmax_sum, workspace, workspace_bytes: int, stream, passes_start=None,
+                 passes_stop=None) -> None:
+    """Forward phase 2 on raw device pointers (ints); raises on a non-OK status."""
+    lib = load()
+    if passes_start is None and passes_stop is None:
+        st = lib.sel_attn_fwd(ctypes.byref(desc), query, key, value, topk_indices, attention_out,
+                              softmax_max, softmax_sum, workspace, workspace_bytes, stream)
+    else:
+        st = lib.sel_attn_fwd_timed(ctypes.byref(desc), query, key, value, topk_indices,
+                                    attention_out, softmax_max, softmax_sum, workspace,
+                                    workspace_bytes, stream, passes_start, passes_stop)
+    if st != SAG_OK:
+        raise SagError(st, "sel_attn_fwd")
+
+
+def forward(q, k, v, topk, cu_seqlens_q, cu_seqlens_kv, scale, block_size, block_count,
+            out=None, workspace=None, stream=None, check=False):
+    """torch-tensor convenience over the forward's C ABI: returns
+    (attention_out [T1, n1, d_v], softmax_max [T1, n1, 8], softmax_sum [T1, n1, 8])."""
+    import torch
+    if not q.is_cuda:
+        raise ValueError("inputs must be CUDA tensors (there is no CPU path)")
+    dtype = SAG_FP16 if q.dtype == torch.float16 else SAG_BF16
+    t1, n1, d_qk = q.shape
+    _, n2, d_v = v.shape
+    desc = make_desc(cu_seqlens_q, cu_seqlens_kv, n1, n2, d_qk, d_v, block_size, block_count, scale,
+                     dtype, False)
+    need = fwd_workspace_size(desc)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = (torch.empty((t1, n1, d_v), dtype=q.dtype, device=q.device),
+               torch.empty((t1, n1, 8), dtype=torch.float32, device=q.device),
+               torch.empty((t1, n1, 8), dtype=torch.float32, device=q.device))
+    o, smax, ssum = out
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    for t in (q, k, v, topk, o, smax, ssum):
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    sel_attn_fwd(desc, q.data_ptr(), k.data_ptr(), v.data_ptr(), topk.data_ptr(), o.data_ptr(),
+                 smax.data_ptr(), ssum.data_ptr(), workspace.data_ptr(), need, stream.cuda_stream)
+    if check:
+        st = query_error(workspace.data_ptr(), stream.cuda_stream)
+        if st != SAG_OK:
+            raise SagError(st, "device")
+    return o, smax, ssum

@@ -71,7 +71,9 @@ sag_status validate(const sag_desc *d) {
     return SAG_OK;
 }
 
-sag_status make_plan(const sag_desc *d, Plan *p) {
+// forward: the same carve (dq_acc holds O, lse2 the row maxima, delta the
+// row sums); tensor-core shapes only, no token windows or chunks
+sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     sag_status st = validate(d);
     if (st != SAG_OK) return st;
     Geometry &g = p->g;
@@ -103,12 +105,17 @@ sag_status make_plan(const sag_desc *d, Plan *p) {
     // tensor-core one also covers (used to cross-check the two)
     const char *force = getenv("SELATTN_FORCE_CUDA_CORE");
     p->use_tc = bwd_tc_supported(g) && !(force && force[0] == '1');
+    if (forward) {
+        if (p->det) return SAG_ERR_UNSUPPORTED;   // the forward's sums are order-dependent
+        p->use_tc = fwd_tc_supported(g);
+        if (!p->use_tc) return SAG_ERR_UNSUPPORTED;
+    }
     g.halves = g.block_size > 64 ? g.block_size / 64 : 1;
     // token windows: tensor-core default mode on problems whose dQ accumulator
     // is well beyond L2.  SELATTN_WINDOW_TOKENS sets the window length (and
     // forces windows on smaller problems too).
     const char *wenv = getenv("SELATTN_WINDOW_TOKENS");
-    g.windowed = p->use_tc && !p->det && (rows * g.d_qk * 4 > kWindowMinAcc || (wenv && atoll(wenv) > 0));
+    g.windowed = !forward && p->use_tc && !p->det && (rows * g.d_qk * 4 > kWindowMinAcc || (wenv && atoll(wenv) > 0));
     {
         int64_t wtok = kWindowDqBytes / ((int64_t)g.group * g.d_qk * 4);
         if (wenv && atoll(wenv) > 0) wtok = atoll(wenv);
@@ -338,6 +345,67 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
     }
     if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SAG_ERR_CUDA;
     if (g.chunked && (e = launch_cast_dkv(g, ws, dk, dv, p.fp16, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
+    return SAG_OK;
+}
+
+extern "C" sag_status sel_attn_fwd_workspace_size(const sag_desc *desc, size_t *workspace_bytes) {
+    if (!workspace_bytes) return SAG_ERR_NULL;
+    Plan p;
+    sag_status st = make_plan(desc, &p, true);
+    if (st != SAG_OK) return st;
+    *workspace_bytes = p.total;
+    return SAG_OK;
+}
+
+extern "C" sag_status sel_attn_fwd(const sag_desc *desc, const void *query, const void *key, const void *value,
+                                   const int32_t *topk_indices, void *attention_out, float *softmax_max,
+                                   float *softmax_sum, void *workspace, size_t workspace_bytes, void *stream) {
+    return sel_attn_fwd_timed(desc, query, key, value, topk_indices, attention_out, softmax_max, softmax_sum,
+                              workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+extern "C" sag_status sel_attn_fwd_timed(const sag_desc *desc, const void *query, const void *key,
+                                         const void *value, const int32_t *topk_indices, void *attention_out,
+                                         float *softmax_max, float *softmax_sum, void *workspace,
+                                         size_t workspace_bytes, void *stream, void *passes_start,
+                                         void *passes_stop) {
+    cudaEvent_t ev0 = static_cast<cudaEvent_t>(passes_start), ev1 = static_cast<cudaEvent_t>(passes_stop);
+    Plan p;
+    sag_status st = make_plan(desc, &p, true);
+    if (st != SAG_OK) return st;
+    const void *ptrs[] = {query, key, value, topk_indices, attention_out, softmax_max, softmax_sum};
+    for (const void *x : ptrs)
+        if (!x) return SAG_ERR_NULL;
+    if (!workspace) return SAG_ERR_WORKSPACE;
+    for (const void *x : ptrs)
+        if (!aligned16(x)) return SAG_ERR_ALIGN;
+    if (!aligned16(workspace)) return SAG_ERR_ALIGN;
+    if (workspace_bytes < p.total) return SAG_ERR_WORKSPACE;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!bind_stream_device(s)) return SAG_ERR_CUDA;
+    const Geometry &g = p.g;
+    Workspace ws = carve(p, workspace);
+    const int sms = device_sms();
+    std::vector<char> meta(p.o_count - p.o_cu_q, 0);
+    memcpy(meta.data() + (p.o_cu_q - p.o_cu_q), desc->cu_seqlens_q, sizeof(int32_t) * (g.batch + 1));
+    memcpy(meta.data() + (p.o_cu_kv - p.o_cu_q), desc->cu_seqlens_kv, sizeof(int32_t) * (g.batch + 1));
+    memcpy(meta.data() + (p.o_item_base - p.o_cu_q), p.item_base.data(), sizeof(int64_t) * (g.batch + 1));
+    memcpy(meta.data() + (p.o_unit_base - p.o_cu_q), p.unit_base.data(), sizeof(int64_t) * (g.batch + 1));
+    memcpy(meta.data() + (p.o_wtab_base - p.o_cu_q), p.wtab_base.data(), sizeof(int64_t) * (g.batch + 1));
+    char *base = static_cast<char *>(workspace);
+    if (cudaMemsetAsync(base + p.o_hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return SAG_ERR_CUDA;
+    if (cudaMemcpyAsync(base + p.o_cu_q, meta.data(), meta.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return SAG_ERR_CUDA;
+    if (cudaMemsetAsync(base + p.o_count, 0, p.o_offset - p.o_count, s) != cudaSuccess) return SAG_ERR_CUDA;
+    if (launch_fwd_init(g, ws, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
+    if (launch_inversion(g, ws, topk_indices, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
+    if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return SAG_ERR_CUDA;
+    for (int pass = 1; pass <= 2; ++pass)
+        if (launch_fwd_tc(g, ws, query, key, value, pass, p.fp16, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
+    if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SAG_ERR_CUDA;
+    if (launch_fwd_finalize(g, ws, attention_out, softmax_max, softmax_sum, p.fp16, s, sms) != cudaSuccess)
+        return SAG_ERR_CUDA;
     return SAG_OK;
 }
 

@@ -33,6 +33,14 @@ cudaError_t launch_cast_dkv(const Geometry &g, const Workspace &ws, void *dk, vo
 bool dq_tc_supported(const Geometry &g);
 cudaError_t launch_dq_tc(const Geometry &g, const Workspace &ws, const void *k, const int32_t *topk, void *dq,
                          bool fp16, cudaStream_t s, int num_sms);
+// Forward (tensor cores, same shapes as the backward's tensor-core kernel):
+// row state init, pass 1 (row maxima) / pass 2 (row sums and O), finalize.
+bool fwd_tc_supported(const Geometry &g);
+cudaError_t launch_fwd_init(const Geometry &g, const Workspace &ws, cudaStream_t s, int num_sms);
+cudaError_t launch_fwd_tc(const Geometry &g, const Workspace &ws, const void *q, const void *k, const void *v,
+                          int pass, bool fp16, cudaStream_t s, int num_sms);
+cudaError_t launch_fwd_finalize(const Geometry &g, const Workspace &ws, void *o, float *smax, float *ssum, bool fp16,
+                                cudaStream_t s, int num_sms);
 // dQ from the stored dS, fixed order (deterministic mode).
 cudaError_t launch_dq_from_ds(const Geometry &g, const Workspace &ws, const void *k,
                               const int32_t *topk, void *dq, bool fp16, cudaStream_t s, int num_sms);

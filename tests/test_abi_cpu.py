@@ -26,7 +26,7 @@ def _declared():
     names = set()
     for h in hdrs:
         txt = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        names |= set(re.findall(r"\b(sel_attn_grad\w*)\s*\(", txt))
+        names |= set(re.findall(r"\b(sel_attn_\w*)\s*\(", txt))
     return names
 
 
@@ -116,3 +116,20 @@ def test_status_strings(lib):
 def test_golden_totals_match_limits():
     # the selection limit and stat lane count the validation encodes
     assert GOLD["selected_keys_below"] == 128 * 64 and GOLD["stat_lanes"] == 8
+
+
+def _fwd_status(d):
+    import ctypes
+    n = ctypes.c_size_t(0)
+    return sab.load().sel_attn_fwd_workspace_size(ctypes.byref(d), ctypes.byref(n)), n.value
+
+
+def test_forward_phase1(lib):
+    st, n = _fwd_status(_desc())
+    assert st == sab.SAG_OK and n > 0
+    # the forward's sums are order-dependent: no deterministic mode
+    assert _fwd_status(_desc(deterministic=True))[0] == sab.SAG_ERR_UNSUPPORTED
+    # tensor-core shapes only (d_v == 128)
+    assert _fwd_status(_desc(d_v=192))[0] == sab.SAG_ERR_UNSUPPORTED
+    # the backward's shape checks apply unchanged
+    assert _fwd_status(_desc(block_size=24))[0] == sab.SAG_ERR_SHAPE

@@ -1,0 +1,106 @@
+"""GPU parity of the forward (attention_out, softmax_max, softmax_sum) against
+the fp64 oracle forward, and the forward feeding the backward.
+
+Small cases are compared in full; the long-context workload is run at full
+size and compared on sampled query rows that the oracle computes from
+sub-problems of those rows.  Tolerance per output tensor as for the backward:
+relative Frobenius error <= 5e-3 and max abs error <= 2e-2 * max|ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_backward_gb300 as sab
+import synth
+from tests import _support as S
+from tests.test_parity_gpu import SMALL
+
+pytestmark = pytest.mark.gpu
+
+FWD_CASES = ["tiny", "varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127"]
+
+
+def _gpu_forward(w, x):
+    t = {k: v.cuda() for k, v in x.items()}
+    return sab.forward(t["q"], t["k"], t["v"], t["topk"], w.cu_q, w.cu_kv, w.scale, w.block_size,
+                       w.block_count, check=True)
+
+
+def _check_forward(o, smax, ssum, ref_o, ref_m, ref_l, shape):
+    t1, n1, d_v = shape
+    smax, ssum = smax.cpu(), ssum.cpu()
+    # the 8 lanes of each statistic are equal
+    assert torch.equal(smax, smax[..., :1].expand_as(smax))
+    assert torch.equal(ssum, ssum[..., :1].expand_as(ssum))
+    S.assert_close("attention_out", S.f64(o).reshape(-1, d_v), ref_o.reshape(-1, d_v))
+    S.assert_close("softmax_max", smax[..., 0].double().numpy().reshape(-1), ref_m.reshape(-1))
+    S.assert_close("softmax_sum", ssum[..., 0].double().numpy().reshape(-1), ref_l.reshape(-1))
+
+
+@pytest.mark.parametrize("name", FWD_CASES)
+def test_forward_parity_small(name):
+    w = SMALL[name]
+    x = synth.make_inputs(w, device="cpu")
+    p = S.problem(w, x, with_backward=False)
+    ref_o, ref_m, ref_l = oracle.forward(p)
+    o, smax, ssum = _gpu_forward(w, x)
+    _check_forward(o, smax, ssum, ref_o, ref_m, ref_l, (w.t1, w.n1, w.d_v))
+
+
+def test_forward_rejects_unsupported_value_dim():
+    w = SMALL["dv192"]
+    x = synth.make_inputs(w, device="cpu")
+    with pytest.raises(sab.SagError) as e:
+        _gpu_forward(w, x)
+    assert e.value.status == sab.SAG_ERR_UNSUPPORTED
+
+
+def test_forward_then_backward():
+    """The GPU forward's outputs as the backward's inputs: the GPU backward
+    matches the oracle backward given the same (GPU-produced) O and stats."""
+    w = SMALL["varlen"]
+    x = synth.make_inputs(w, device="cpu")
+    o, smax, ssum = _gpu_forward(w, x)
+    x = dict(x, o=o.cpu(), softmax_max=smax.cpu(), softmax_sum=ssum.cpu())
+    t = {k: v.cuda() for k, v in x.items()}
+    dq, dk, dv = sab.backward(t["q"], t["k"], t["v"], t["o"], t["dy"], t["softmax_max"], t["softmax_sum"],
+                              t["topk"], w.cu_q, w.cu_kv, w.scale, w.block_size, w.block_count, check=True)
+    ref = oracle.backward(S.problem(w, x))
+    for nm, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        S.assert_close(nm, S.f64(got), r)
+
+
+def test_forward_reports_out_of_range_ids():
+    w = SMALL["tiny"]
+    x = synth.make_inputs(w, device="cpu")
+    x["topk"] = x["topk"].clone()
+    x["topk"][5, 0, 1] = 10 ** 6
+    with pytest.raises(sab.SagError) as e:
+        _gpu_forward(w, x)
+    assert e.value.status == sab.SAG_ERR_INDEX
+
+
+def test_forward_long_context_sampled():
+    """Full-size long-context forward; 256 sampled query tokens of one KV head
+    per batch are checked against the oracle on their sub-problem."""
+    w = synth.WORKLOADS[2]
+    x = synth.make_inputs(w, device="cuda")
+    o, smax, ssum = sab.forward(x["q"], x["k"], x["v"], x["topk"], w.cu_q, w.cu_kv, w.scale, w.block_size,
+                                w.block_count, check=True)
+    rng = np.random.default_rng(7)
+    for b in range(w.batch):
+        n2 = int(rng.integers(w.n2))
+        toks = np.sort(rng.choice(np.arange(w.cu_q[b], w.cu_q[b + 1]), size=256, replace=False))
+        xs = {k: v.cpu() for k, v in x.items() if k in ("q", "k", "v", "dy", "topk")}
+        G = w.group
+        t = torch.as_tensor(toks)
+        hs = slice(n2 * G, (n2 + 1) * G)
+        k0, k1 = w.cu_kv[b], w.cu_kv[b + 1]
+        sub = {"q": xs["q"][t][:, hs], "dy": xs["dy"][t][:, hs], "topk": xs["topk"][t][:, n2:n2 + 1],
+               "k": xs["k"][k0:k1, n2:n2 + 1], "v": xs["v"][k0:k1, n2:n2 + 1]}
+        sw = w.with_(cu_q=(0, len(toks)), cu_kv=(0, k1 - k0), n1=G, n2=1)
+        p = S.problem(sw, sub, with_backward=False)
+        ref_o, ref_m, ref_l = S.par_forward_rows(p, np.arange(len(toks) * G))
+        _check_forward(o[t.cuda()][:, hs].contiguous(), smax[t.cuda()][:, hs].contiguous(),
+                       ssum[t.cuda()][:, hs].contiguous(), ref_o, ref_m, ref_l, (len(toks), G, w.d_v))
