@@ -104,3 +104,16 @@ def test_forward_long_context_sampled():
         ref_o, ref_m, ref_l = S.par_forward_rows(p, np.arange(len(toks) * G))
         _check_forward(o[t.cuda()][:, hs].contiguous(), smax[t.cuda()][:, hs].contiguous(),
                        ssum[t.cuda()][:, hs].contiguous(), ref_o, ref_m, ref_l, (len(toks), G, w.d_v))
+
+
+@pytest.mark.parametrize("window", [37, 300])
+@pytest.mark.parametrize("name", ["varlen", "ragged_fp16", "g32_bs128"])
+def test_forward_token_windows_parity(name, window, monkeypatch):
+    """Token windows (the default on problems whose O accumulator is far
+    beyond L2) forced small on small problems."""
+    monkeypatch.setenv("SELATTN_FWD_WINDOW_TOKENS", str(window))
+    w = SMALL[name]
+    x = synth.make_inputs(w, device="cpu")
+    ref_o, ref_m, ref_l = oracle.forward(S.problem(w, x, with_backward=False))
+    o, smax, ssum = _gpu_forward(w, x)
+    _check_forward(o, smax, ssum, ref_o, ref_m, ref_l, (w.t1, w.n1, w.d_v))
