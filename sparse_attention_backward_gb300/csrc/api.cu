@@ -323,9 +323,12 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
             cudaMemsetAsync(ws.dkv_acc, 0, sizeof(float) * (size_t)g.t2 * g.n2 * (g.d_qk + g.d_v), s) != cudaSuccess)
             return SAG_ERR_CUDA;
         if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return SAG_ERR_CUDA;
-        if ((e = p.use_tc ? launch_bwd_tc(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s, sms)
-                          : launch_bwd_simt(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s,
-                                            sms)) != cudaSuccess)
+        if ((e = !p.use_tc ? launch_bwd_simt(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s,
+                                             sms)
+                 : bwd_split_preferred(g)
+                     ? launch_bwd_tc_split(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s, sms)
+                     : launch_bwd_tc(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s, sms)) !=
+            cudaSuccess)
             return SAG_ERR_CUDA;
         if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SAG_ERR_CUDA;
         if ((e = launch_cast(ws.dq_acc, dq, (int64_t)g.t1 * g.n1 * g.d_qk, g.scale, p.fp16, s, sms)) !=
@@ -343,9 +346,12 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
         Geometry gc = g;
         gc.tok_lo = c * p.chunk_tokens;
         gc.tok_hi = gc.tok_lo + p.chunk_tokens < g.t1 ? gc.tok_lo + p.chunk_tokens : g.t1;
-        if ((e = p.use_tc ? launch_bwd_tc(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s, sms)
-                          : launch_bwd_simt(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s,
-                                            sms)) != cudaSuccess)
+        if ((e = !p.use_tc ? launch_bwd_simt(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s,
+                                             sms)
+                 : bwd_split_preferred(gc)
+                     ? launch_bwd_tc_split(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s, sms)
+                     : launch_bwd_tc(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s, sms)) !=
+            cudaSuccess)
             return SAG_ERR_CUDA;
         if ((e = (p.use_tc && dq_tc_supported(gc)) ? launch_dq_tc(gc, ws, key, topk_indices, dq, p.fp16, s, sms)
                                                     : launch_dq_from_ds(gc, ws, key, topk_indices, dq, p.fp16, s, sms)) !=

@@ -25,6 +25,12 @@ bool bwd_tc_supported(const Geometry &g);
 cudaError_t launch_bwd_tc(const Geometry &g, const Workspace &ws, const void *q, const void *k, const void *v,
                           const void *dy, void *dk, void *dv, bool fp16, bool deterministic, cudaStream_t s,
                           int num_sms);
+// The same backward with the softmax split in two phases (bwd_tc_split.cu),
+// preferred for small query groups.
+bool bwd_split_preferred(const Geometry &g);
+cudaError_t launch_bwd_tc_split(const Geometry &g, const Workspace &ws, const void *q, const void *k,
+                                const void *v, const void *dy, void *dk, void *dv, bool fp16, bool deterministic,
+                                cudaStream_t s, int num_sms);
 // dK/dV from the fp32 accumulator after the last token chunk.
 cudaError_t launch_cast_dkv(const Geometry &g, const Workspace &ws, void *dk, void *dv, bool fp16,
                             cudaStream_t s, int num_sms);

@@ -84,25 +84,6 @@ __device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
-// L2 eviction-priority policies for the cache-hinted forms below.
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
-                                                 uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
@@ -143,18 +124,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 
-// 16 lanes x 256 bit, 4 repetitions (32 columns) from TMEM lane base L:
-// thread t gets, for r = 0..3, r[4r..4r+1] = lane L + t/4, columns
-// 8r + 2(t%4) + {0,1}, and r[4r+2..4r+3] = lane L + 8 + t/4, same columns
-// (four consecutive threads hold 8 consecutive columns of one lane).
-__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
 
 // ---------------------------------------------------------------- MMA
 // Shared-memory matrix descriptor, 128-byte swizzle.  Start address, leading
@@ -190,6 +159,26 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Warp-convergent forms: every lane of the warp executes the call with the
+// same operands and one elected lane issues the instruction, so descriptors
+// stay warp-uniform (issuing from a single divergent lane measured slower).
+__device__ __forceinline__ void mma_f16_ss_warp(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
 // Arrive on `bar` once every earlier tcgen05 op of this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -197,19 +186,7 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                  : "memory");
 }
 
-// Red-add of 4 consecutive floats with an L2 eviction-priority policy.
-__device__ __forceinline__ void red_add_v4_hint(float *dst, float a, float b, float c, float d, uint64_t policy) {
-    asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(a), "f"(b),
-                 "f"(c), "f"(d), "l"(policy)
-                 : "memory");
-}
 
-// Red-add of 2 consecutive floats (8-byte aligned) with an L2 eviction policy.
-__device__ __forceinline__ void red_add_v2_hint(float *dst, uint32_t a, uint32_t b, uint64_t policy) {
-    asm volatile("red.global.add.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(dst), "f"(__uint_as_float(a)),
-                 "f"(__uint_as_float(b)), "l"(policy)
-                 : "memory");
-}
 
 // Red-add of 4 consecutive floats (16-byte aligned) into global memory.
 __device__ __forceinline__ void red_add_v4(float *dst, float a, float b, float c, float d) {

@@ -109,6 +109,20 @@ def test_token_windows_parity(small_data, name, window, monkeypatch):
 
 
 @pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("split", ["0", "1"])
+@pytest.mark.parametrize("name", ["tiny", "varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127"])
+def test_both_tensor_core_schedules(small_data, name, split, deterministic, monkeypatch):
+    """Both tensor-core schedules (softmax between the MMA groups, or split in
+    two phases beside them) forced on shapes either can take, both modes."""
+    monkeypatch.setenv("SELATTN_SPLIT_SOFTMAX", split)
+    w, x, (rdq, rdk, rdv) = small_data(name)
+    dq, dk, dv = _run(w, x, deterministic)
+    S.assert_close(f"{name} split={split} dq", S.f64(dq), rdq)
+    S.assert_close(f"{name} split={split} dk", S.f64(dk), rdk)
+    S.assert_close(f"{name} split={split} dv", S.f64(dv), rdv)
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
 @pytest.mark.parametrize("name", ["tiny", "varlen", "g32_bs128"])
 def test_cuda_core_kernel_parity(small_data, name, deterministic, monkeypatch):
     """The CUDA-core kernel on shapes the tensor-core kernel also takes."""
