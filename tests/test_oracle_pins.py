@@ -134,6 +134,7 @@ def test_dense_case_matches_dense_attention():
                       cnt=lens[0] // bs, order="shuffled", scale=1 / np.sqrt(16))
     _with_forward(p)
     dq, dk, dv = oracle.backward(p)
+    fo, fm, fl = oracle.forward(p)
     q = torch.tensor(p.q, requires_grad=True)
     k = torch.tensor(p.k, requires_grad=True)
     v = torch.tensor(p.v, requires_grad=True)
@@ -143,7 +144,15 @@ def test_dense_case_matches_dense_attention():
         qs = q[p.cu_q[b]:p.cu_q[b + 1]].transpose(0, 1)                      # [n1, S1, d]
         ks = k[p.cu_kv[b]:p.cu_kv[b + 1]].transpose(0, 1).repeat_interleave(G, 0)
         vs = v[p.cu_kv[b]:p.cu_kv[b + 1]].transpose(0, 1).repeat_interleave(G, 0)
-        o = torch.softmax(p.scale * qs @ ks.transpose(1, 2), -1) @ vs
+        sc = p.scale * qs @ ks.transpose(1, 2)
+        o = torch.softmax(sc, -1) @ vs
+        # the forward's outputs: dense attention, its row maxima and row sums
+        rows = slice(p.cu_q[b], p.cu_q[b + 1])
+        np.testing.assert_allclose(fo[rows], o.transpose(0, 1).detach().numpy(), rtol=0, atol=1e-12)
+        mx = sc.max(-1).values
+        np.testing.assert_allclose(fm[rows], mx.transpose(0, 1).detach().numpy(), rtol=0, atol=1e-12)
+        sm = torch.exp(sc - mx[..., None]).sum(-1)
+        np.testing.assert_allclose(fl[rows], sm.transpose(0, 1).detach().numpy(), rtol=1e-12, atol=0)
         loss = loss + (o.transpose(0, 1) * torch.tensor(p.dy[p.cu_q[b]:p.cu_q[b + 1]])).sum()
     loss.backward()
     np.testing.assert_allclose(dq, q.grad.numpy(), rtol=0, atol=1e-11)
