@@ -96,15 +96,16 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, det: bool):
-    """DRAM bytes per launch of the main kernel from a committed ncu summary,
-    used only while the kernel sources are unchanged since the capture."""
+def profiled_traffic(workload: str, det: bool, mode: str = ""):
+    """DRAM bytes per launch of the main kernel (per call of both forward
+    passes with mode "forward") from a committed ncu summary, used only while
+    the kernel sources are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    key = f"{workload}:{'deterministic' if det else 'default'}"
+    key = f"{workload}:{mode or ('deterministic' if det else 'default')}"
     e = d.get(key)
     if not e or e.get("kernel_source_hash") != kernel_source_hash():
         return None
@@ -506,7 +507,8 @@ def run_forward(args, w, x, dev, stream, world, rank, local):
             "config": dict(workload_config(w, False), mode="forward"),
             "roofline": {"bound": "tensor", "kernel": "forward passes (max, sum + P V)", "achieved": achieved,
                          "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_source": f"{pk_src} bf16 burst", "kernel_ms": pass_ms, "traffic": None},
+                         "peak_source": f"{pk_src} bf16 burst", "kernel_ms": pass_ms,
+                         "traffic": profiled_traffic(w.name, False, "forward")},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 10 * K, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
