@@ -304,26 +304,24 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
     memcpy(meta.data() + (p.o_unit_base - p.o_cu_q), p.unit_base.data(), sizeof(int64_t) * (g.batch + 1));
     memcpy(meta.data() + (p.o_wtab_base - p.o_cu_q), p.wtab_base.data(), sizeof(int64_t) * (g.batch + 1));
 
-    cudaError_t e;
-    (void)e;
     char *base = static_cast<char *>(workspace);
-    if ((e = cudaMemsetAsync(base + p.o_hdr, 0, sizeof(WsHeader), s)) != cudaSuccess) return SAG_ERR_CUDA;
-    if ((e = cudaMemcpyAsync(base + p.o_cu_q, meta.data(), meta.size(), cudaMemcpyHostToDevice, s)) !=
+    if ((cudaMemsetAsync(base + p.o_hdr, 0, sizeof(WsHeader), s)) != cudaSuccess) return SAG_ERR_CUDA;
+    if ((cudaMemcpyAsync(base + p.o_cu_q, meta.data(), meta.size(), cudaMemcpyHostToDevice, s)) !=
         cudaSuccess)
         return SAG_ERR_CUDA;
     // count and cursor are adjacent: one memset
-    if ((e = cudaMemsetAsync(base + p.o_count, 0, p.o_offset - p.o_count, s)) != cudaSuccess) return SAG_ERR_CUDA;
+    if ((cudaMemsetAsync(base + p.o_count, 0, p.o_offset - p.o_count, s)) != cudaSuccess) return SAG_ERR_CUDA;
 
-    if ((e = launch_preprocess(g, ws, attention_out, attention_out_grad, softmax_max, softmax_sum, p.fp16,
+    if ((launch_preprocess(g, ws, attention_out, attention_out_grad, softmax_max, softmax_sum, p.fp16,
                                !p.det, s, sms)) != cudaSuccess)
         return SAG_ERR_CUDA;
-    if ((e = launch_inversion(g, ws, topk_indices, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
+    if ((launch_inversion(g, ws, topk_indices, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
     if (!p.det) {
         if (g.windowed &&
             cudaMemsetAsync(ws.dkv_acc, 0, sizeof(float) * (size_t)g.t2 * g.n2 * (g.d_qk + g.d_v), s) != cudaSuccess)
             return SAG_ERR_CUDA;
         if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return SAG_ERR_CUDA;
-        if ((e = !p.use_tc ? launch_bwd_simt(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s,
+        if ((!p.use_tc ? launch_bwd_simt(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s,
                                              sms)
                  : bwd_split_preferred(g)
                      ? launch_bwd_tc_split(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s, sms)
@@ -331,10 +329,10 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
             cudaSuccess)
             return SAG_ERR_CUDA;
         if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SAG_ERR_CUDA;
-        if ((e = launch_cast(ws.dq_acc, dq, (int64_t)g.t1 * g.n1 * g.d_qk, g.scale, p.fp16, s, sms)) !=
+        if ((launch_cast(ws.dq_acc, dq, (int64_t)g.t1 * g.n1 * g.d_qk, g.scale, p.fp16, s, sms)) !=
             cudaSuccess)
             return SAG_ERR_CUDA;
-        if (g.windowed && (e = launch_cast_dkv(g, ws, dk, dv, p.fp16, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
+        if (g.windowed && (launch_cast_dkv(g, ws, dk, dv, p.fp16, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
         return SAG_OK;
     }
     // deterministic: token chunks in order; dS of a chunk -> its dQ
@@ -346,20 +344,20 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
         Geometry gc = g;
         gc.tok_lo = c * p.chunk_tokens;
         gc.tok_hi = gc.tok_lo + p.chunk_tokens < g.t1 ? gc.tok_lo + p.chunk_tokens : g.t1;
-        if ((e = !p.use_tc ? launch_bwd_simt(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s,
+        if ((!p.use_tc ? launch_bwd_simt(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s,
                                              sms)
                  : bwd_split_preferred(gc)
                      ? launch_bwd_tc_split(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s, sms)
                      : launch_bwd_tc(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s, sms)) !=
             cudaSuccess)
             return SAG_ERR_CUDA;
-        if ((e = (p.use_tc && dq_tc_supported(gc)) ? launch_dq_tc(gc, ws, key, topk_indices, dq, p.fp16, s, sms)
+        if (((p.use_tc && dq_tc_supported(gc)) ? launch_dq_tc(gc, ws, key, topk_indices, dq, p.fp16, s, sms)
                                                     : launch_dq_from_ds(gc, ws, key, topk_indices, dq, p.fp16, s, sms)) !=
             cudaSuccess)
             return SAG_ERR_CUDA;
     }
     if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SAG_ERR_CUDA;
-    if (g.chunked && (e = launch_cast_dkv(g, ws, dk, dv, p.fp16, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
+    if (g.chunked && (launch_cast_dkv(g, ws, dk, dv, p.fp16, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
     return SAG_OK;
 }
 
