@@ -133,3 +133,54 @@ def test_forward_phase1(lib):
     assert _fwd_status(_desc(d_v=192))[0] == sab.SAG_ERR_UNSUPPORTED
     # the backward's shape checks apply unchanged
     assert _fwd_status(_desc(block_size=24))[0] == sab.SAG_ERR_SHAPE
+
+
+# ------------------------------------------------ launch plans (host only)
+def test_plan_default_and_deterministic(lib):
+    d = _desc()
+    info = sab.plan_info(d)
+    # preprocess, histogram, 3 scan passes, fill, sort, main kernel, dQ cast
+    assert info.launches == 9 and info.token_chunks == 1 and info.main_kernel == 1
+    assert info.workspace_bytes == sab.workspace_size(d)
+    det = sab.plan_info(_desc(deterministic=True))
+    # one chunk: main kernel (stores dS) and the fixed-order dQ pass
+    assert det.token_chunks == 1 and det.launches == 7 + 2
+    # items: key blocks (batch, KV head, block id)
+    assert info.items == 256 // 16
+
+
+def test_plan_items_follow_batches_and_heads(lib):
+    d = _desc(cu_seqlens_q=[0, 100, 300], cu_seqlens_kv=[0, 256, 768], n1=8, n2=2, block_size=64,
+              block_count=4)
+    assert sab.plan_info(d).items == 2 * (256 // 64) + 2 * (512 // 64)
+
+
+def test_plan_kernel_choice(lib, monkeypatch):
+    assert sab.plan_info(_desc()).main_kernel == 1                    # tensor cores
+    assert sab.plan_info(_desc(d_qk=128, d_v=192)).main_kernel == 0   # Dv = 192: CUDA cores
+    monkeypatch.setenv("SELATTN_FORCE_CUDA_CORE", "1")
+    assert sab.plan_info(_desc()).main_kernel == 0
+
+
+def test_plan_token_windows(lib, monkeypatch):
+    monkeypatch.setenv("SELATTN_WINDOW_TOKENS", "64")
+    w = sab.plan_info(_desc())
+    # windowed: dK / dV reduced as partials, so their cast runs too
+    assert w.launches == 10
+    monkeypatch.delenv("SELATTN_WINDOW_TOKENS")
+    assert sab.plan_info(_desc()).launches == 9
+
+
+def test_deterministic_workspace_holds_ds_not_dq(lib):
+    # default: fp32 dQ accumulator [T1 * n1 * d_qk]; deterministic: dS in the
+    # dtype for the token chunk [T1, n2, count, G, bs] -- here 2 B * 256 * 1 * 4 *
+    # 4 * 16 = 131072 B against 4 B * 256 * 4 * 192 = 786432 B
+    dflt = sab.workspace_size(_desc())
+    det = sab.workspace_size(_desc(deterministic=True))
+    assert dflt - det == pytest.approx(786432 - 131072, abs=4 * 256)
+
+
+def test_forward_workspace_matches_default_backward(lib):
+    # the forward carves the same regions (O accumulator in the dQ slot)
+    assert _fwd_status(_desc())[1] == sab.workspace_size(_desc())
+    assert _fwd_status(_desc(d_qk=128))[1] == sab.workspace_size(_desc(d_qk=128))
