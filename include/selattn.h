@@ -151,7 +151,10 @@ sag_status sel_attn_grad_query_error(const void *workspace, void *stream);
  *   launches          kernels one call launches (memsets and copies excluded)
  *   items             key blocks (batch, KV head, block id) the work is split into
  *   token_chunks      query-token chunks the deterministic mode runs in (1 otherwise)
- *   main_kernel       0: CUDA-core kernel, 1: tensor-core (tcgen05) kernel
+ *   main_kernel       0: CUDA-core kernel, 1: tensor-core (tcgen05) kernel (one of
+ *                     two schedules: the softmax between the MMA groups, or, for
+ *                     query groups G = n1 / n2 of 1, 2 or 4, split in two phases
+ *                     beside them)
  */
 typedef struct sag_plan_info {
     uint64_t workspace_bytes;
