@@ -438,7 +438,7 @@ extern "C" const char *sel_attn_grad_status_string(int status) {
     case SAG_ERR_NULL: return "a required pointer is NULL";
     case SAG_ERR_SHAPE: return "a size or length is outside the operator's constraints";
     case SAG_ERR_DTYPE: return "dtype must be bf16 or fp16";
-    case SAG_ERR_UNSUPPORTED: return "allowed by the constraints but not supported by this build";
+    case SAG_ERR_UNSUPPORTED: return "allowed by the constraints but not supported by this library";
     case SAG_ERR_WORKSPACE: return "workspace missing or smaller than the phase-1 size";
     case SAG_ERR_ALIGN: return "a device pointer is not 16-byte aligned";
     case SAG_ERR_CUDA: return "a CUDA call or kernel launch failed";
