@@ -172,7 +172,9 @@ def _np16(t):
 def oracle_sample(w, x, n_tokens, rng):
     """A bounded sample of the workload: n_tokens query tokens of batch 0 with
     the G heads of KV head 0 against their batch's keys (a full backward of
-    those rows: dQ, and their dK / dV scatter)."""
+    those rows: dQ, and their dK / dV scatter).  When x carries no forward
+    outputs (the reference arm) they come from the oracle forward of the
+    sample, outside the timed call."""
     import oracle
     b, j, G = 0, 0, w.group
     q0, q1 = w.cu_q[b], w.cu_q[b + 1]
@@ -184,9 +186,17 @@ def oracle_sample(w, x, n_tokens, rng):
         cu_q=np.array([0, len(toks)], np.int32), cu_kv=np.array([0, k1 - k0], np.int32), n1=G, n2=1,
         d_qk=w.d_qk, d_v=w.d_v, block_size=w.block_size, block_count=w.block_count, scale=w.scale,
         topk=x["topk"][t][:, j:j + 1].cpu().numpy(), q=_np16(x["q"][t][:, hs]),
-        k=_np16(x["k"][k0:k1, j:j + 1]), v=_np16(x["v"][k0:k1, j:j + 1]), o=_np16(x["o"][t][:, hs]),
-        dy=_np16(x["dy"][t][:, hs]), smax=x["softmax_max"][t][:, hs].cpu().numpy(),
-        ssum=x["softmax_sum"][t][:, hs].cpu().numpy(), stat_stride=8, kind=w.dtype)
+        k=_np16(x["k"][k0:k1, j:j + 1]), v=_np16(x["v"][k0:k1, j:j + 1]), dy=_np16(x["dy"][t][:, hs]),
+        stat_stride=8, kind=w.dtype)
+    if "o" in x:
+        p.o = _np16(x["o"][t][:, hs])
+        p.smax = x["softmax_max"][t][:, hs].cpu().numpy()
+        p.ssum = x["softmax_sum"][t][:, hs].cpu().numpy()
+    else:
+        o, m, l = oracle.forward(p)
+        p.o = _np16(torch.from_numpy(o).to(w.torch_dtype))
+        p.smax = np.repeat(m[..., None], 8, axis=-1).astype(np.float32)
+        p.ssum = np.repeat(l[..., None], 8, axis=-1).astype(np.float32)
     flops = 2.0 * w.selected_keys * (3 * w.d_qk + 2 * w.d_v) * len(toks) * G
     return p, flops, len(toks)
 
@@ -217,9 +227,6 @@ def time_oracle(w, x, budget_s, seed=0, forward=False):
 
 def run_reference(args, w, rank, world):
     x = synth.make_inputs(w, device="cpu" if w.t1 * w.n1 * w.d_qk < (1 << 27) else "cuda")
-    if "o" not in x:
-        x.update(synth.synthetic_forward_stats(w, torch.Generator(device=x["q"].device).manual_seed(w.seed + 7),
-                                               x["q"].device))
     per_step = min(5.0, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         time_oracle(w, x, per_step)
@@ -297,13 +304,14 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     x = synth.make_inputs(w, device=dev, seed=rank_seed(w, rank))
-    if "o" not in x:   # workloads whose stats normally come from a forward
-        g = torch.Generator(device=dev).manual_seed(rank_seed(w, rank) + 7)
-        x.update(synth.synthetic_forward_stats(w, g, dev))
     stream = torch.cuda.current_stream(dev)
     if args.forward:
         run_forward(args, w, x, dev, stream, world, rank, local)
         return
+    # attentionOut and the [T1, N1, 8] stats: the library's forward (untimed)
+    o, smax, ssum = sab.forward(x["q"], x["k"], x["v"], x["topk"], w.cu_q, w.cu_kv, w.scale, w.block_size,
+                                w.block_count, check=True)
+    x.update(o=o, softmax_max=smax, softmax_sum=ssum)
     desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count,
                          w.scale, sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, args.deterministic)
     info = sab.plan_info(desc)

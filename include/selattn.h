@@ -42,6 +42,9 @@
  *     enqueued.  Problems found by the device (a block id out of range, a
  *     bounded wait that ran out) are recorded in the workspace and read back
  *     with sel_attn_grad_query_error.
+ *   - An entry point that takes a stream makes the device owning that stream
+ *     current for the length of the call and gives the calling thread its
+ *     previous current device back before returning.
  */
 #ifndef SELATTN_H
 #define SELATTN_H
@@ -104,7 +107,11 @@ typedef struct sag_desc {
  * Phase 1.  Validates the descriptor against the constraints (host only, no
  * CUDA call) and writes the workspace size in bytes the problem needs.
  * Returns SAG_OK, SAG_ERR_NULL, SAG_ERR_SHAPE, SAG_ERR_DTYPE or
- * SAG_ERR_UNSUPPORTED.
+ * SAG_ERR_UNSUPPORTED.  SAG_ERR_UNSUPPORTED marks a problem the constraints
+ * allow but this library does not take: more than 2^31 - 1 selections in all
+ * (T1 * n2 * block_count; the inverted index is 32-bit), or more key blocks
+ * in all (sum over batches of n2 * S2_b / block_size) than its scan holds
+ * (2^24).
  */
 sag_status sel_attn_grad_workspace_size(const sag_desc *desc, size_t *workspace_bytes);
 

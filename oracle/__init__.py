@@ -25,7 +25,7 @@ from __future__ import annotations
 import ctypes
 import os
 import subprocess
-from dataclasses import dataclass, field
+from dataclasses import dataclass
 
 import numpy as np
 
@@ -137,7 +137,6 @@ class Problem:
     ssum: object = None   # [T1, n1, stat_stride]
     stat_stride: int = 8
     kind: str | None = None   # "bf16"/"f16" when 16-bit data arrives as uint16
-    _keep: list = field(default_factory=list, repr=False)
 
     @property
     def batch(self) -> int:
@@ -151,7 +150,10 @@ class Problem:
     def t2(self) -> int:
         return int(self.cu_kv[-1])
 
-    def _c(self) -> _Problem:
+    def _c(self):
+        """(C struct, list of the arrays it points into).  The caller holds the
+        list for the duration of the C call; nothing is stored on the object,
+        so several threads may call into the oracle with one Problem."""
         keep = []
 
         def arr(x, dt=None):
@@ -178,8 +180,7 @@ class Problem:
             q=ten(self.q), k=ten(self.k), v=ten(self.v), o=ten(self.o), dy=ten(self.dy),
             smax=ten(self.smax), ssum=ten(self.ssum),
         )
-        self._keep = keep
-        return c
+        return c, keep
 
 
 def _check(rc: int, what: str):
@@ -193,7 +194,7 @@ def forward(p: Problem):
     o = np.zeros((p.t1, p.n1, p.d_v))
     m = np.zeros((p.t1, p.n1))
     l = np.zeros((p.t1, p.n1))
-    c = p._c()
+    c, _keep = p._c()
     _check(lib.sao_forward(ctypes.byref(c), o.ctypes.data, m.ctypes.data, l.ctypes.data), "forward")
     return o, m, l
 
@@ -205,7 +206,7 @@ def forward_rows(p: Problem, rows_th):
     o = np.zeros((len(rows), p.d_v))
     m = np.zeros(len(rows))
     l = np.zeros(len(rows))
-    c = p._c()
+    c, _keep = p._c()
     _check(lib.sao_forward_rows(ctypes.byref(c), len(rows), rows.ctypes.data, o.ctypes.data,
                                 m.ctypes.data, l.ctypes.data), "forward_rows")
     return o, m, l
@@ -217,7 +218,7 @@ def backward(p: Problem):
     dq = np.zeros((p.t1, p.n1, p.d_qk))
     dk = np.zeros((p.t2, p.n2, p.d_qk))
     dv = np.zeros((p.t2, p.n2, p.d_v))
-    c = p._c()
+    c, _keep = p._c()
     _check(lib.sao_backward(ctypes.byref(c), dq.ctypes.data, dk.ctypes.data, dv.ctypes.data), "backward")
     return dq, dk, dv
 
@@ -227,7 +228,7 @@ def dq_rows(p: Problem, rows_th):
     lib = _load()
     rows = np.ascontiguousarray(np.asarray(rows_th, dtype=np.int64))
     dq = np.zeros((len(rows), p.d_qk))
-    c = p._c()
+    c, _keep = p._c()
     _check(lib.sao_dq_rows(ctypes.byref(c), len(rows), rows.ctypes.data, dq.ctypes.data), "dq_rows")
     return dq
 
@@ -237,7 +238,7 @@ def dkdv_block(p: Problem, b: int, n2: int, kb: int):
     lib = _load()
     dk = np.zeros((p.block_size, p.d_qk))
     dv = np.zeros((p.block_size, p.d_v))
-    c = p._c()
+    c, _keep = p._c()
     _check(lib.sao_dkdv_block(ctypes.byref(c), b, n2, kb, dk.ctypes.data, dv.ctypes.data), "dkdv_block")
     return dk, dv
 
@@ -247,7 +248,7 @@ def dkdv_block_range(p: Problem, b: int, n2: int, kb: int, t_lo: int, t_hi: int)
     lib = _load()
     dk = np.zeros((p.block_size, p.d_qk))
     dv = np.zeros((p.block_size, p.d_v))
-    c = p._c()
+    c, _keep = p._c()
     _check(lib.sao_dkdv_block_range(ctypes.byref(c), b, n2, kb, t_lo, t_hi, dk.ctypes.data,
                                     dv.ctypes.data), "dkdv_block_range")
     return dk, dv

@@ -20,6 +20,8 @@ constexpr size_t kAlign = 256;
 // deterministic mode stores dS for at most this many bytes of query tokens at
 // once; larger problems run in token chunks
 constexpr int64_t kDsChunkBytes = 16LL << 30;
+// total selections T1 * N2 * count the 32-bit inverted index can hold
+constexpr int64_t kMaxSelections = INT32_MAX;
 // default mode: token windows are sized so one (batch, KV head) window's fp32
 // dQ rows take about this many bytes (they must stay resident in L2 while its
 // key tiles are processed); problems whose whole dQ accumulator is smaller
@@ -107,6 +109,8 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
 
     const int64_t rows = (int64_t)g.t1 * g.n1;
     const int64_t sel = (int64_t)g.t1 * g.n2 * g.block_count;
+    // bucket offsets and positions inside the inverted index are 32-bit
+    if (sel > kMaxSelections) return SAG_ERR_UNSUPPORTED;
     // SELATTN_FORCE_CUDA_CORE=1 selects the CUDA-core kernel for shapes the
     // tensor-core one also covers (used to cross-check the two)
     const char *force = getenv("SELATTN_FORCE_CUDA_CORE");
@@ -164,6 +168,10 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     p->o_dq_acc = p->det ? o : take(sizeof(float) * rows * g.d_qk);
     const int64_t ds_per_token = (int64_t)g.n2 * g.block_count * g.group * g.block_size * 2;
     int64_t chunk = kDsChunkBytes / ds_per_token;
+    // SELATTN_DS_CHUNK_TOKENS sets the chunk length (tests run the chunked
+    // path on small problems with it)
+    const char *cenv = getenv("SELATTN_DS_CHUNK_TOKENS");
+    if (cenv && atoll(cenv) > 0) chunk = atoll(cenv);
     if (chunk < 1) chunk = 1;
     if (chunk > g.t1) chunk = g.t1;
     p->chunk_tokens = p->det ? (int32_t)chunk : g.t1;
@@ -209,19 +217,24 @@ int device_sms() {
     return sms;
 }
 
-// Make the device that owns `s` current for this library's runtime (the
-// caller's framework may keep its own notion of the current device).  The
-// legacy default stream (NULL) keeps the current device.
-bool bind_stream_device(cudaStream_t s) {
+}  // namespace
+
+bool DeviceGuard::bind(cudaStream_t s) {
     if (s == nullptr) return true;
     int dev = 0;
     if (cudaStreamGetDevice(s, &dev) != cudaSuccess) return false;
     int cur = -1;
-    if (cudaGetDevice(&cur) == cudaSuccess && cur == dev) return true;
-    return cudaSetDevice(dev) == cudaSuccess;
+    if (cudaGetDevice(&cur) != cudaSuccess) return false;
+    if (cur == dev) return true;
+    if (cudaSetDevice(dev) != cudaSuccess) return false;
+    saved_ = cur;
+    return true;
 }
 
-}  // namespace
+DeviceGuard::~DeviceGuard() {
+    if (saved_ >= 0) cudaSetDevice(saved_);
+}
+
 }  // namespace sag
 
 using namespace sag;
@@ -290,7 +303,8 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
     if (workspace_bytes < p.total) return SAG_ERR_WORKSPACE;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (!bind_stream_device(s)) return SAG_ERR_CUDA;
+    DeviceGuard dg;
+    if (!dg.bind(s)) return SAG_ERR_CUDA;
     const Geometry &g = p.g;
     Workspace ws = carve(p, workspace);
     const int sms = device_sms();
@@ -396,7 +410,8 @@ extern "C" sag_status sel_attn_fwd_timed(const sag_desc *desc, const void *query
     if (workspace_bytes < p.total) return SAG_ERR_WORKSPACE;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (!bind_stream_device(s)) return SAG_ERR_CUDA;
+    DeviceGuard dg;
+    if (!dg.bind(s)) return SAG_ERR_CUDA;
     const Geometry &g = p.g;
     Workspace ws = carve(p, workspace);
     const int sms = device_sms();
@@ -425,7 +440,8 @@ extern "C" sag_status sel_attn_fwd_timed(const sag_desc *desc, const void *query
 extern "C" sag_status sel_attn_grad_query_error(const void *workspace, void *stream) {
     if (!workspace) return SAG_ERR_NULL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (!bind_stream_device(s)) return SAG_ERR_CUDA;
+    DeviceGuard dg;
+    if (!dg.bind(s)) return SAG_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return SAG_ERR_CUDA;
     int32_t code = 0;
     if (cudaMemcpy(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) return SAG_ERR_CUDA;

@@ -58,7 +58,7 @@ struct Smem {
 
 enum Bar {
     B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL0, B_Q_FULL1, B_Q_EMPTY0, B_Q_EMPTY1, B_DO_FULL0, B_DO_FULL1,
-    B_DO_EMPTY0, B_DO_EMPTY1, B_S_FULL, B_P_FULL, B_MMA_DONE, B_DQ_FREE, B_ACC_FULL, B_ACC_FREE, B_COUNT
+    B_DO_EMPTY0, B_DO_EMPTY1, B_S_FULL, B_P_FULL, B_MMA_DONE, B_DQ_FREE, B_ACC_FULL, B_ACC_FREE, B_DRAIN, B_COUNT
 };
 
 struct TcArgs {
@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init(&bars[B_DQ_FREE], 128);
         tc::mbar_init(&bars[B_ACC_FULL], 1);
         tc::mbar_init(&bars[B_ACC_FREE], 128);
+        tc::mbar_init(&bars[B_DRAIN], 1);
         tc::fence_mbar_init();
     }
     // rows of a Q / dY tile no token fills (when G does not divide 128) must
@@ -142,11 +143,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // fetched four at a time (tile::gather4) instead
         const bool gather = G <= 4 && 4 % G == 0;
         int ne = 0, tc_i = 0;
+        uint32_t armed_kv = 0, armed_q[2] = {0, 0}, armed_do[2] = {0, 0};
         bool ok = true;
         for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
             const KeyTile kt = decode(g, ws, ti, nk, tpt);
             if (kt.ntok == 0) continue;
             if (ne > 0 && !tc::mbar_wait(&bars[B_KV_EMPTY], (ne - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            ++armed_kv;
             if (lane == 0) {
                 tc::mbar_arrive_expect_tx(&bars[B_KV_FULL], (uint32_t)nk * (DQK + DV) * 2);
                 for (int c = 0; c < KC; ++c)
@@ -164,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int *m = meta + (tc_i % kMeta) * kRows;
                 for (int tt = lane; tt < tpt; tt += 32) m[tt] = tt < nt ? ws.entries[kt.e0 + i * tpt + tt] : -1;
                 __syncwarp();
+                ++armed_q[s];
                 if (lane == 0) tc::mbar_arrive_expect_tx(&bars[B_Q_FULL0 + s], (uint32_t)tpt * G * DQK * 2);
                 __syncwarp();
                 uint8_t *qdst = smem + L::OFF_Q + s * L::Q_STAGE;
@@ -192,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                ++armed_do[d];
                 if (lane == 0) tc::mbar_arrive_expect_tx(&bars[B_DO_FULL0 + d], (uint32_t)tpt * G * DV * 2);
                 __syncwarp();
                 uint8_t *ddst = smem + L::OFF_DO + d * L::DO_STAGE;
@@ -217,6 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++ne;
         }
         if (!ok) fail();
+        // let every load this warp issued land before the CTA exits
+        bool drained = tc::drain_armed(&bars[B_KV_FULL], armed_kv, kWaitNs);
+        for (int i = 0; i < 2; ++i)
+            drained = tc::drain_armed(&bars[B_Q_FULL0 + i], armed_q[i], kWaitNs) &&
+                      tc::drain_armed(&bars[B_DO_FULL0 + i], armed_do[i], kWaitNs) && drained;
+        if (!drained) fail();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -286,6 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++ne;
             }
             if (!ok) fail();
+            // every MMA issued must be complete before TMEM is freed
+            tc::mma_commit(&bars[B_DRAIN]);
+            if (!tc::mbar_wait_drain(&bars[B_DRAIN], 0, kWaitNs)) fail();
         }
     } else if (warp < 6) {
         // ------------------------------------------------------ softmax / dS

@@ -57,7 +57,7 @@ struct Smem {
 enum Bar {
     B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL, B_Q_EMPTY0 = B_Q_FULL + 6, B_Q_EMPTY1, B_DO_FULL,
     B_DO_EMPTY0 = B_DO_FULL + 4, B_DO_EMPTY1, B_S_FULL, B_S_FREE, B_P_FULL, B_P_FREE, B_DP_FULL, B_DS_FULL,
-    B_DS_FREE, B_MMA_DONE, B_DQ_FREE, B_ACC_FULL, B_ACC_FREE, B_COUNT
+    B_DS_FREE, B_MMA_DONE, B_DQ_FREE, B_ACC_FULL, B_ACC_FREE, B_DRAIN, B_COUNT
 };
 
 struct TcArgs {
@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init(&bars[B_DQ_FREE], 128);
         tc::mbar_init(&bars[B_ACC_FULL], 1);
         tc::mbar_init(&bars[B_ACC_FREE], 128);
+        tc::mbar_init(&bars[B_DRAIN], 1);
         tc::fence_mbar_init();
     }
     // rows of a Q / dY tile no token fills (when G does not divide 128) must
@@ -165,11 +166,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 y[j] = ((e[j] >= 0 ? e[j] : e_first) / g.block_count) * g.n1 + kt.n2 * G + (4 * lane + j) % G;
         };
         int ne = 0, tc_i = 0;
+        uint32_t armed_kv = 0, armed_q[2] = {0, 0}, armed_do[2] = {0, 0};
         bool ok = true;
         for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
             const KeyTile kt = decode(g, ws, ti, nk, tpt);
             if (kt.ntok == 0) continue;
             if (ne > 0 && !tc::mbar_wait(&bars[B_KV_EMPTY], (ne - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            ++armed_kv;
             if (lane == 0) {
                 tc::mbar_arrive_expect_tx(&bars[B_KV_FULL], (uint32_t)nk * (DQK + DV) * 2);
                 for (int c = 0; c < KC; ++c)
@@ -192,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (tk < tpt && (!gather || (4 * lane + j) % G == 0)) m[tk] = e[j];
                 }
                 __syncwarp();
+                ++armed_q[s];
                 if (lane == 0)
                     for (int c = 0; c < KC; ++c)
                         tc::mbar_arrive_expect_tx(&bars[B_Q_FULL + s * 3 + c], (uint32_t)tpt * G * 64 * 2);
@@ -220,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                ++armed_do[d];
                 if (lane == 0)
                     for (int c = 0; c < 2; ++c)
                         tc::mbar_arrive_expect_tx(&bars[B_DO_FULL + d * 2 + c], (uint32_t)tpt * G * 64 * 2);
@@ -244,6 +249,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++ne;
         }
         if (!ok) fail();
+        // let every load this warp issued land before the CTA exits
+        bool drained = tc::drain_armed(&bars[B_KV_FULL], armed_kv, kWaitNs);
+        for (int i = 0; i < 2; ++i) {
+            for (int c = 0; c < KC; ++c)
+                drained = tc::drain_armed(&bars[B_Q_FULL + i * 3 + c], armed_q[i], kWaitNs) && drained;
+            for (int c = 0; c < 2; ++c)
+                drained = tc::drain_armed(&bars[B_DO_FULL + i * 2 + c], armed_do[i], kWaitNs) && drained;
+        }
+        if (!drained) fail();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         // Pipe order per query tile t:  S(t) | dK, dQ (t-1) | dP(t) | dV(t).
@@ -355,6 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++ne;
         }
         if (!ok && lane == 0) fail();
+        // every MMA issued must be complete before TMEM is freed
+        tc::mma_commit_warp(&bars[B_DRAIN]);
+        if (!__all_sync(0xffffffffu, tc::mbar_wait_drain(&bars[B_DRAIN], 0, kWaitNs)) && lane == 0) fail();
     } else if (warp < 6) {
         // ------------------------------------------------------ softmax / dS
         const int q4 = warp & 3;

@@ -33,7 +33,7 @@ struct DqSmem {
 };
 
 enum DqBar { D_FULL0 = 0, D_EMPTY0 = kStages, D_ACC_FULL0 = 2 * kStages, D_ACC_FREE0 = 2 * kStages + 2,
-             D_COUNT = 2 * kStages + 4 };
+             D_DRAIN = 2 * kStages + 4, D_COUNT = 2 * kStages + 5 };
 
 struct DqArgs {
     Geometry g;
@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             tc::mbar_init(&bars[D_ACC_FULL0 + b], 1);
             tc::mbar_init(&bars[D_ACC_FREE0 + b], 128);
         }
+        tc::mbar_init(&bars[D_DRAIN], 1);
         tc::fence_mbar_init();
     }
     if (warp == 1) {
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             tc::prefetch_tmap(&map_k);
             tc::prefetch_tmap(&map_ds);
             int it = 0;
+            uint32_t armed[kStages] = {};
             bool ok = true;
             for (int64_t cp = blockIdx.x; cp < npairs && ok; cp += gridDim.x) {
                 const int t = g.tok_lo + (int)(cp / g.n2), n2 = (int)(cp % g.n2);
@@ -115,6 +117,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     const int id = __ldg(A.topk + pair * g.block_count + slot);
                     const int key0 = ws.cu_kv[b] + id * BS;
                     uint8_t *st = smem + s * L::STAGE;
+                    ++armed[s];
                     tc::mbar_arrive_expect_tx(&bars[D_FULL0 + s], (uint32_t)(BS * DQK * 2 + G * BS * 2));
                     for (int c = 0; c < KC; ++c)
                         tc::tma_load_3d(st + c * BS * 128, &map_k, c * 64, n2, key0, &bars[D_FULL0 + s]);
@@ -125,6 +128,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 }
             }
             if (!ok) fail();
+            // let every load issued land before the CTA exits
+            bool drained = true;
+            for (int i = 0; i < kStages; ++i) drained = tc::drain_armed(&bars[D_FULL0 + i], armed[i], kDqWaitNs) && drained;
+            if (!drained) fail();
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
@@ -171,6 +178,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 tc::mma_commit(&bars[D_ACC_FULL0 + ab]);
             }
             if (!ok) fail();
+            // every MMA issued must be complete before TMEM is freed
+            tc::mma_commit(&bars[D_DRAIN]);
+            if (!tc::mbar_wait_drain(&bars[D_DRAIN], 0, kDqWaitNs)) fail();
         }
     } else {
         // ------------------------------------------------------ epilogue

@@ -49,7 +49,7 @@ struct FwdSmem {
 // in shared memory); O_DONE: the P V MMAs of a tile are done; O_FREE: drained.
 enum FBar {
     F_KV_FULL = 0, F_KV_EMPTY, F_Q_FULL, F_Q_EMPTY = F_Q_FULL + kQStages, F_S_FULL = F_Q_EMPTY + kQStages,
-    F_P_FULL, F_O_DONE, F_O_FREE, F_COUNT
+    F_P_FULL, F_O_DONE, F_O_FREE, F_DRAIN, F_COUNT
 };
 
 struct FwdArgs {
@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init(&bars[F_P_FULL], 128);
         tc::mbar_init(&bars[F_O_DONE], 1);
         tc::mbar_init(&bars[F_O_FREE], 128);
+        tc::mbar_init(&bars[F_DRAIN], 1);
         tc::fence_mbar_init();
     }
     // rows of a Q tile no token fills (when G does not divide 128) must hold
@@ -131,11 +132,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int oob_row = g.t1 * g.n1;   // out of range: the TMA fills zeros
         const bool gather = G <= 4 && 4 % G == 0;
         int ne = 0, tc_i = 0;
+        uint32_t armed_kv = 0, armed_q[kQStages] = {};
         bool ok = true;
         for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
             const KeyTile kt = decode(g, ws, ti, nk, tpt);
             if (kt.ntok == 0) continue;
             if (ne > 0 && !tc::mbar_wait(&bars[F_KV_EMPTY], (ne - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            ++armed_kv;
             if (lane == 0) {
                 tc::mbar_arrive_expect_tx(&bars[F_KV_FULL], (uint32_t)nk * (DQK + (PASS == 2 ? DV : 0)) * 2);
                 for (int c = 0; c < KC; ++c)
@@ -155,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int *m = meta + (tc_i % kMetaF) * kRows;
                 for (int tt = lane; tt < tpt; tt += 32) m[tt] = tt < nt ? ws.entries[kt.e0 + i * tpt + tt] : -1;
                 __syncwarp();
+                ++armed_q[s];
                 if (lane == 0) tc::mbar_arrive_expect_tx(&bars[F_Q_FULL + s], (uint32_t)tpt * G * DQK * 2);
                 __syncwarp();
                 uint8_t *qdst = smem + L::OFF_Q + s * L::Q_STAGE;
@@ -181,6 +185,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++ne;
         }
         if (!ok) fail();
+        // let every load this warp issued land before the CTA exits
+        bool drained = tc::drain_armed(&bars[F_KV_FULL], armed_kv, kWaitNs);
+        for (int i = 0; i < kQStages; ++i) drained = tc::drain_armed(&bars[F_Q_FULL + i], armed_q[i], kWaitNs) && drained;
+        if (!drained) fail();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -226,6 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++ne;
             }
             if (!ok) fail();
+            // every MMA issued must be complete before TMEM is freed
+            tc::mma_commit(&bars[F_DRAIN]);
+            if (!tc::mbar_wait_drain(&bars[F_DRAIN], 0, kWaitNs)) fail();
         }
     } else if (warp < 6) {
         // ------------------------------------------------------ softmax

@@ -5,6 +5,21 @@
 
 namespace sag {
 
+// Makes the device that owns a stream current for the length of one library
+// call and gives the calling thread its previous current device back when it
+// goes out of scope (the legacy default stream, NULL, keeps the current one).
+class DeviceGuard {
+public:
+    DeviceGuard() = default;
+    DeviceGuard(const DeviceGuard &) = delete;
+    DeviceGuard &operator=(const DeviceGuard &) = delete;
+    bool bind(cudaStream_t s);
+    ~DeviceGuard();
+
+private:
+    int saved_ = -1;
+};
+
 cudaError_t launch_preprocess(const Geometry &g, const Workspace &ws, const void *o, const void *dy,
                               const float *smax, const float *ssum, bool fp16, bool zero_dq,
                               cudaStream_t s, int num_sms);

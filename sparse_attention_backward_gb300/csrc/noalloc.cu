@@ -47,13 +47,10 @@ extern "C" sag_status sel_attn_grad_noalloc(const sag_desc *desc, const void *qu
     sag_status st = sel_attn_grad_workspace_size(desc, &need);
     if (st != SAG_OK) return st;
     if (need > kScratchBytes) return SAG_ERR_WORKSPACE;
-    // the scratch must belong to the device that runs the stream
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (s) {
-        int dev = 0;
-        if (cudaStreamGetDevice(s, &dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess)
-            return SAG_ERR_CUDA;
-    }
+    // the scratch must belong to the device that runs the stream; the
+    // caller's current device is restored on return
+    sag::DeviceGuard dg;
+    if (!dg.bind(static_cast<cudaStream_t>(stream))) return SAG_ERR_CUDA;
     void *scratch = nullptr;
     st = scratch_for_current_device(&scratch);
     if (st != SAG_OK) return st;

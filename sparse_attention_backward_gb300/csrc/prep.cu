@@ -198,30 +198,94 @@ __global__ void __launch_bounds__(256) k_fill(Geometry g, Workspace ws,
     }
 }
 
-// Sort each bucket ascending (token-major order).  Buckets of up to
-// kSortCap entries are sorted in shared memory (bitonic); larger ones by one
-// thread with heapsort in place (rare: needs more than kSortCap selections of
-// one key block).  With token windows, each item then records where every
-// window of its batch starts inside its sorted bucket.
+// Sort each bucket ascending (token-major order), so that the order of the
+// entries does not depend on the timing of the fill's atomics.  The network
+// is bitonic in its all-ascending form (the first step of every merge pairs
+// i with its mirror i ^ (k - 1), the later ones pair i with i ^ j), which
+// lets a bucket of n entries be padded virtually to the next power of two
+// with +infinity: such a pad never moves below index n, so pairs whose upper
+// index is >= n are skipped and nothing is written beyond the bucket.
+// Buckets of up to kSortCap entries are sorted whole in shared memory.
+// Larger ones (e.g. a block that every query of a long batch selects) are
+// sorted in place by the same CTA: every kSortCap chunk in shared memory, then
+// the merge steps whose stride spans chunks as passes over global memory, and
+// after each such step the short strides again chunk by chunk in shared memory.
+// With token windows, each item then records where every window of its batch
+// starts inside its sorted bucket.
 constexpr int kSortCap = 16384;
 
-__device__ void heap_sort_global(int32_t *a, int n) {
-    auto sift = [&](int root, int end) {
-        while (2 * root + 1 < end) {
-            int child = 2 * root + 1;
-            if (child + 1 < end && a[child] < a[child + 1]) ++child;
-            if (a[root] < a[child]) {
-                int tmp = a[root]; a[root] = a[child]; a[child] = tmp;
-                root = child;
-            } else {
-                return;
+// The steps of stage k whose strides are < kSortCap, on one chunk of the
+// bucket held in shared memory (keys[0 .. len) real, the rest +infinity).
+__device__ __forceinline__ void sort_steps_smem(int32_t *keys, int p2, int k_lo, int k_hi, bool mirror_first) {
+    for (int k = k_lo; k <= k_hi; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const bool mirror = mirror_first && j == (k >> 1);
+            for (int i = threadIdx.x; i < p2; i += blockDim.x) {
+                const int l = mirror ? (i ^ (k - 1)) : (i ^ j);
+                if (l > i) {
+                    const int32_t x = keys[i], y = keys[l];
+                    if (x > y) { keys[i] = y; keys[l] = x; }
+                }
             }
+            __syncthreads();
         }
-    };
-    for (int s = n / 2 - 1; s >= 0; --s) sift(s, n);
-    for (int end = n - 1; end > 0; --end) {
-        int tmp = a[0]; a[0] = a[end]; a[end] = tmp;
-        sift(0, end);
+    }
+}
+
+// Load chunk c of a (length n) into keys, padding with +infinity.
+__device__ __forceinline__ void chunk_load(int32_t *keys, const int32_t *a, int n, int c) {
+    for (int i = threadIdx.x; i < kSortCap; i += blockDim.x) {
+        const int gi = c * kSortCap + i;
+        keys[i] = gi < n ? a[gi] : INT32_MAX;
+    }
+    __syncthreads();
+}
+__device__ __forceinline__ void chunk_store(const int32_t *keys, int32_t *a, int n, int c) {
+    for (int i = threadIdx.x; i < kSortCap; i += blockDim.x) {
+        const int gi = c * kSortCap + i;
+        if (gi < n) a[gi] = keys[i];
+    }
+    __syncthreads();
+}
+
+__device__ void sort_large_bucket(int32_t *a, int n, int32_t *keys) {
+    int p2 = kSortCap;
+    while (p2 < n) p2 <<= 1;
+    const int nchunks = (n + kSortCap - 1) / kSortCap;
+    // stages k = 2 .. kSortCap: each chunk on its own
+    for (int c = 0; c < nchunks; ++c) {
+        chunk_load(keys, a, n, c);
+        sort_steps_smem(keys, kSortCap, 2, kSortCap, true);
+        chunk_store(keys, a, n, c);
+    }
+    for (int k = 2 * kSortCap; k <= p2; k <<= 1) {
+        // strides >= kSortCap in global memory (mirror step first)
+        for (int j = k >> 1; j >= kSortCap; j >>= 1) {
+            const bool mirror = j == (k >> 1);
+            for (int i = threadIdx.x; i < p2; i += blockDim.x) {
+                const int l = mirror ? (i ^ (k - 1)) : (i ^ j);
+                if (l > i && l < n) {
+                    const int32_t x = a[i], y = a[l];
+                    if (x > y) { a[i] = y; a[l] = x; }
+                }
+            }
+            __syncthreads();
+        }
+        // strides < kSortCap chunk by chunk (no mirror step: plain half-cleaners)
+        for (int c = 0; c < nchunks; ++c) {
+            chunk_load(keys, a, n, c);
+            for (int j = kSortCap >> 1; j > 0; j >>= 1) {
+                for (int i = threadIdx.x; i < kSortCap; i += blockDim.x) {
+                    const int l = i ^ j;
+                    if (l > i) {
+                        const int32_t x = keys[i], y = keys[l];
+                        if (x > y) { keys[i] = y; keys[l] = x; }
+                    }
+                }
+                __syncthreads();
+            }
+            chunk_store(keys, a, n, c);
+        }
     }
 }
 
@@ -234,26 +298,13 @@ __global__ void __launch_bounds__(512) k_sort_buckets(Geometry g, Workspace ws) 
         const bool in_smem = n <= kSortCap;
         if (n > 1) {
             if (!in_smem) {
-                if (threadIdx.x == 0) heap_sort_global(a, n);
-                __syncthreads();
+                sort_large_bucket(a, n, keys);
             } else {
                 int p2 = 1;
                 while (p2 < n) p2 <<= 1;
                 for (int i = threadIdx.x; i < p2; i += blockDim.x) keys[i] = i < n ? a[i] : INT32_MAX;
                 __syncthreads();
-                for (int k = 2; k <= p2; k <<= 1) {
-                    for (int j = k >> 1; j > 0; j >>= 1) {
-                        for (int i = threadIdx.x; i < p2; i += blockDim.x) {
-                            const int l = i ^ j;
-                            if (l > i) {
-                                const int32_t x = keys[i], y = keys[l];
-                                const bool up = (i & k) == 0;
-                                if ((x > y) == up) { keys[i] = y; keys[l] = x; }
-                            }
-                        }
-                        __syncthreads();
-                    }
-                }
+                sort_steps_smem(keys, p2, 2, p2, true);
                 for (int i = threadIdx.x; i < n; i += blockDim.x) a[i] = keys[i];
             }
         } else if (n == 1) {

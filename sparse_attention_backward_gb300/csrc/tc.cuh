@@ -58,6 +58,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// Wind-down wait: bounded by limit_ns but blind to the abort flag.  A role
+// that stops early still has to let the bulk copies and MMAs it issued land
+// before the CTA frees its TMEM and exits, so it waits here for the last
+// phase it armed on each of its barriers.  Returns false if the limit ran out.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+// A barrier whose phases complete only after its producer armed them
+// (arrive.expect_tx / tcgen05.commit, arrival count 1): after `armed` arms at
+// most `armed` phases can have completed, so waiting on the parity of phase
+// armed - 1 returns as soon as that phase is complete (at once if it already
+// is).
+__device__ __forceinline__ bool drain_armed(uint64_t *bar, uint32_t armed, uint64_t limit_ns) {
+    return armed == 0 || mbar_wait_drain(bar, (armed - 1) & 1, limit_ns);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
     asm volatile(

@@ -184,3 +184,17 @@ def test_forward_workspace_matches_default_backward(lib):
     # the forward carves the same regions (O accumulator in the dQ slot)
     assert _fwd_status(_desc())[1] == sab.workspace_size(_desc())
     assert _fwd_status(_desc(d_qk=128))[1] == sab.workspace_size(_desc(d_qk=128))
+
+
+def test_selections_beyond_the_32_bit_index_are_unsupported(lib):
+    """16 batches of 128K tokens (T1 = 2M, the documented maximum), N2 = 16
+    and 128 blocks of 16 are within the constraints, but make 2^32 selections:
+    more than the inverted index's 32-bit offsets hold."""
+    cu = [i * 128 * 1024 for i in range(17)]
+    big = dict(cu_seqlens_q=cu, cu_seqlens_kv=cu, n1=16, n2=16, d_qk=128, d_v=128, block_size=16,
+               block_count=128, scale=0.1)
+    assert _status(_desc(**big))[0] == sab.SAG_ERR_UNSUPPORTED
+    # half the heads: 2^31 selections, still one too many
+    assert _status(_desc(**dict(big, n1=8, n2=8)))[0] == sab.SAG_ERR_UNSUPPORTED
+    # a quarter: 2^30 selections fit
+    assert _status(_desc(**dict(big, n1=4, n2=4)))[0] == sab.SAG_OK

@@ -1,12 +1,10 @@
 """GPU parity of the forward (attention_out, softmax_max, softmax_sum) against
 the fp64 oracle forward, and the forward feeding the backward.
 
-Small cases are compared in full; the long-context workload is run at full
-size and compared on sampled query rows that the oracle computes from
-sub-problems of those rows.  Tolerance per output tensor as for the backward:
+Small cases are compared in full here; the three large workloads are run at
+full size in test_fullsize_gpu.py and compared on sampled query rows.  Tolerance per output tensor as for the backward:
 relative Frobenius error <= 5e-3 and max abs error <= 2e-2 * max|ref|.
 """
-import numpy as np
 import pytest
 import torch
 
@@ -79,31 +77,6 @@ def test_forward_reports_out_of_range_ids():
     with pytest.raises(sab.SagError) as e:
         _gpu_forward(w, x)
     assert e.value.status == sab.SAG_ERR_INDEX
-
-
-def test_forward_long_context_sampled():
-    """Full-size long-context forward; 256 sampled query tokens of one KV head
-    per batch are checked against the oracle on their sub-problem."""
-    w = synth.WORKLOADS[2]
-    x = synth.make_inputs(w, device="cuda")
-    o, smax, ssum = sab.forward(x["q"], x["k"], x["v"], x["topk"], w.cu_q, w.cu_kv, w.scale, w.block_size,
-                                w.block_count, check=True)
-    rng = np.random.default_rng(7)
-    for b in range(w.batch):
-        n2 = int(rng.integers(w.n2))
-        toks = np.sort(rng.choice(np.arange(w.cu_q[b], w.cu_q[b + 1]), size=256, replace=False))
-        xs = {k: v.cpu() for k, v in x.items() if k in ("q", "k", "v", "dy", "topk")}
-        G = w.group
-        t = torch.as_tensor(toks)
-        hs = slice(n2 * G, (n2 + 1) * G)
-        k0, k1 = w.cu_kv[b], w.cu_kv[b + 1]
-        sub = {"q": xs["q"][t][:, hs], "dy": xs["dy"][t][:, hs], "topk": xs["topk"][t][:, n2:n2 + 1],
-               "k": xs["k"][k0:k1, n2:n2 + 1], "v": xs["v"][k0:k1, n2:n2 + 1]}
-        sw = w.with_(cu_q=(0, len(toks)), cu_kv=(0, k1 - k0), n1=G, n2=1)
-        p = S.problem(sw, sub, with_backward=False)
-        ref_o, ref_m, ref_l = S.par_forward_rows(p, np.arange(len(toks) * G))
-        _check_forward(o[t.cuda()][:, hs].contiguous(), smax[t.cuda()][:, hs].contiguous(),
-                       ssum[t.cuda()][:, hs].contiguous(), ref_o, ref_m, ref_l, (len(toks), G, w.d_v))
 
 
 @pytest.mark.parametrize("window", [37, 300])

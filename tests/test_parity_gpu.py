@@ -1,11 +1,10 @@
 """GPU parity: the CUDA library against the fp64 oracle, element by element.
 
 Small cases (the tiny and varlen workloads plus ragged / edge shapes) are
-compared in full; the three large workloads are run at full size in the
-launch configuration the benchmark times and compared on sampled dQ rows and
-sampled key blocks (dK, dV) that the oracle computes one by one.  Tolerance
-per output tensor: relative Frobenius error <= 5e-3 and max abs error
-<= 2e-2 * max|ref|.
+compared in full, in both modes and under every schedule and switch the
+library has (the three large workloads are in test_fullsize_gpu.py).
+Tolerance per output tensor: relative Frobenius error <= 5e-3 and max abs
+error <= 2e-2 * max|ref|.
 """
 import numpy as np
 import pytest
@@ -183,72 +182,19 @@ def test_deterministic_mode_is_bitwise_reproducible(small_data, name):
         assert torch.equal(u.view(torch.int16), v.view(torch.int16))
 
 
-# ---------------------------------------------------------------- full size
-def _sampled_parity(w, x, outs, n_rows=512, n_blocks=4, seed=0):
-    dq, dk, dv = outs
-    rng = np.random.default_rng(seed)
-    # dQ rows: grouped by (batch, KV head) into sub-problems the oracle can run
-    rows = rng.choice(w.t1 * w.n1, n_rows, replace=False)
-    ref, got = [], []
-    tb = np.searchsorted(np.asarray(w.cu_q), rows // w.n1, side="right") - 1
-    for b in np.unique(tb):
-        for j in range(w.n2):
-            sel = rows[(tb == b) & ((rows % w.n1) // w.group == j)]
-            if sel.size == 0:
-                continue
-            toks = np.unique(sel // w.n1)
-            sub = S.sub_problem(w, x, int(b), j, toks)
-            pos = np.searchsorted(toks, sel // w.n1)
-            sub_rows = pos * w.group + (sel % w.n1) % w.group
-            ref.append(S.par_dq_rows(sub, sub_rows))
-            got.append(S.f64(dq.view(-1, w.d_qk)[torch.as_tensor(sel, device=dq.device)]))
-    S.assert_close(f"{w.name} dq (sampled rows)", np.concatenate(got), np.concatenate(ref))
-    # key blocks: random ones plus the most selected one
-    blocks = []
-    for i in range(n_blocks):
-        b = int(rng.integers(w.batch))
-        j = int(rng.integers(w.n2))
-        nblk = (w.cu_kv[b + 1] - w.cu_kv[b]) // w.block_size
-        kb = int(rng.integers(nblk))
-        if i == n_blocks - 1:
-            q0, q1 = w.cu_q[b], w.cu_q[b + 1]
-            cnt = torch.bincount(x["topk"][q0:q1, j].reshape(-1).long(), minlength=nblk)
-            kb = int(torch.argmax(cnt))
-        blocks.append((b, j, kb))
-    rk, rv, gk, gv = [], [], [], []
-    for (b, j, kb) in blocks:
-        toks = S.selecting_tokens(w, x, b, j, kb)
-        sub = S.sub_problem(w, x, b, j, toks)
-        bk, bv = S.par_dkdv_block(sub, 0, 0, kb)
-        r0 = w.cu_kv[b] + kb * w.block_size
-        rk.append(bk)
-        rv.append(bv)
-        gk.append(S.f64(dk[r0:r0 + w.block_size, j]))
-        gv.append(S.f64(dv[r0:r0 + w.block_size, j]))
-    S.assert_close(f"{w.name} dk (sampled blocks)", np.concatenate(gk), np.concatenate(rk))
-    S.assert_close(f"{w.name} dv (sampled blocks)", np.concatenate(gv), np.concatenate(rv))
-
-
-def _full_size(idx, deterministic):
-    w = synth.WORKLOADS[idx]
-    x = synth.make_inputs(w, device="cuda")
-    outs = sab.backward(x["q"], x["k"], x["v"], x["o"], x["dy"], x["softmax_max"], x["softmax_sum"],
-                        x["topk"], w.cu_q, w.cu_kv, w.scale, w.block_size, w.block_count,
-                        deterministic=deterministic, check=True)
-    torch.cuda.synchronize()
-    _sampled_parity(w, x, outs)
-    return w, x, outs
-
-
-@pytest.mark.parametrize("deterministic", [False, True])
-def test_long_context_sampled(deterministic):
-    _full_size(2, deterministic)
-
-
-@pytest.mark.parametrize("deterministic", [False, True])
-def test_max_selection_sampled(deterministic):
-    _full_size(3, deterministic)
-
-
-def test_small_group_stress_sampled():
-    _full_size(4, False)
+@pytest.mark.parametrize("name,chunk", [("varlen", 1000), ("g32_bs128", 7), ("ragged_fp16", 30)])
+def test_deterministic_token_chunks(small_data, name, chunk, monkeypatch):
+    """Deterministic mode run in several token chunks (dK / dV carried across
+    them in fp32): parity with the oracle, and bit-identical over two runs."""
+    monkeypatch.setenv("SELATTN_DS_CHUNK_TOKENS", str(chunk))
+    w, x, (rdq, rdk, rdv) = small_data(name)
+    desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
+                         sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, True)
+    assert sab.plan_info(desc).token_chunks == -(-w.t1 // chunk) >= 3
+    a = _run(w, x, True)
+    S.assert_close(f"{name} chunks dq", S.f64(a[0]), rdq)
+    S.assert_close(f"{name} chunks dk", S.f64(a[1]), rdk)
+    S.assert_close(f"{name} chunks dv", S.f64(a[2]), rdv)
+    b = _run(w, x, True)
+    for u, v in zip(a, b):
+        assert torch.equal(u.view(torch.int16), v.view(torch.int16))

@@ -10,6 +10,8 @@ file is collected last so that a stop-at-first-failure run has already run
 every other test.
 """
 import ctypes
+import os
+import re
 
 import pytest
 import torch
@@ -29,9 +31,17 @@ def _entry(lib):
 
 
 def _inputs(w, dev, seed):
-    x = synth.make_inputs(w, device=dev, seed=seed)
-    x.update(synth.synthetic_forward_stats(w, torch.Generator(device=dev).manual_seed(seed + 1), dev))
+    x = S.gpu_forward_inputs(w, synth.make_inputs(w, device=dev, seed=seed))
     return [x[k] for k in ("q", "k", "v", "o", "dy", "softmax_max", "softmax_sum", "topk")]
+
+
+def _scratch_limit() -> int:
+    """SEL_ATTN_GRAD_NOALLOC_MAX_SCRATCH as the library's header defines it."""
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "selattn.h")
+    with open(hdr) as f:
+        m = re.search(r"#define SEL_ATTN_GRAD_NOALLOC_MAX_SCRATCH \(\(size_t\)(\d+) << (\d+)\)", f.read())
+    assert m, "limit not found in include/selattn.h"
+    return int(m.group(1)) << int(m.group(2))
 
 
 def _desc(w, det):
@@ -66,7 +76,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     f = _entry(lib)
     w = synth.WORKLOADS[2]   # long context: its workspace is far above the fixed scratch
     need = sab.workspace_size(_desc(w, False))
-    assert need > (64 << 20)
+    assert need > _scratch_limit()
     dev = torch.device("cuda", 0)
     dummy = torch.empty(16, dtype=torch.uint8, device=dev)
     st = f(ctypes.byref(_desc(w, False)), *([dummy.data_ptr()] * 11),
