@@ -74,22 +74,48 @@ typedef enum sag_dtype { SAG_BF16 = 0, SAG_FP16 = 1 } sag_dtype;
 /*
  * Problem descriptor.
  *   batch          B >= 1
- *   cu_seqlens_q   host int32[B+1]: query prefix sums, [0] = 0, [B] = T1.  A
- *                  batch may have no query tokens.
- *   cu_seqlens_kv  host int32[B+1]: key prefix sums, [0] = 0, [B] = T2; every
+ *   cu_seqlens_q   host int32[B+1]: prefix sums of the query lengths, [0] = 0.
+ *                  A batch may have no query tokens.  In TND the last entry
+ *                  is T1; in BSND these are the valid lengths of the padded
+ *                  rows (see layout).
+ *   cu_seqlens_kv  host int32[B+1]: prefix sums of the key lengths; every
  *                  batch's S2 is a multiple of block_size and >= block_size *
  *                  block_count.
  *   n1, n2         query heads and key/value heads (N1 % N2 == 0, N1/N2 <= 32)
  *   d_qk, d_v      head dims of query/key and of value/attentionOut/dY
- *                  (each 128 or 192)
+ *                  (each 128 or 192; with d_rope, d_qk is the non-rope part
+ *                  and must be 128)
  *   block_size     selectedBlockSize (multiple of 16, <= 128)
  *   block_count    selectedBlockCount (1..128, block_size * block_count < 8192)
- *   scale          scaleValue
- *   dtype          sag_dtype of query, key, value, attentionOut, dY, dq, dk, dv
+ *   dtype          sag_dtype of every 16-bit tensor
  *   deterministic  0: default mode (dQ reduced with fp32 atomics, results may
  *                  differ in the last bits between runs); 1: every output is
  *                  bit-identical run to run
+ *   layout         SAG_LAYOUT_TND (0): tokens of all batches packed, rows
+ *                  cu_seqlens[b] .. cu_seqlens[b+1]-1 belong to batch b.
+ *                  SAG_LAYOUT_BSND (1): [B, S, N, D] with every batch padded
+ *                  to s1_max query rows and s2_max key rows: token s of batch b
+ *                  is row b * s1_max + s (b * s2_max + s for keys); only the
+ *                  first S1_b / S2_b rows (from cu_seqlens) are valid.  Padding
+ *                  rows are never read for the result (topk_indices rows of
+ *                  padding tokens are ignored) and get zero gradients.
+ *                  ("aclnnLightningIndexerGrad" page: TND or BSND layouts;
+ *                  "NsaSelectedAttentionGrad" README, calling section: a
+ *                  non-TND sample.)
+ *   scale          scaleValue
+ *   s1_max, s2_max BSND only (0 in TND): padded query / key length, <= 128K;
+ *                  s2_max a multiple of block_size; B * s1_max and B * s2_max
+ *                  <= 2M
+ *   d_rope         0, or 64: the query and key head dims are split into a
+ *                  d_qk part and a rope part held in separate tensors,
+ *                  Q = [query, queryRope], K = [key, keyRope] along D, with
+ *                  gradients dq / dqRope and dk / dkRope the matching column
+ *                  slices of dQ and dK ("aclnnFlashAttentionUnpaddingScore-
+ *                  GradV3" formula section).  Needs the tensor-core path:
+ *                  d_qk == 128, d_v == 128.
  */
+typedef enum sag_layout { SAG_LAYOUT_TND = 0, SAG_LAYOUT_BSND = 1 } sag_layout;
+
 typedef struct sag_desc {
     int32_t batch;
     int32_t n1, n2;
@@ -97,11 +123,45 @@ typedef struct sag_desc {
     int32_t block_size, block_count;
     int32_t dtype;
     int32_t deterministic;
-    int32_t reserved_;   /* must be 0 */
+    int32_t layout;
     double scale;
     const int32_t *cu_seqlens_q;
     const int32_t *cu_seqlens_kv;
+    int32_t s1_max, s2_max;
+    int32_t d_rope;
+    int32_t reserved_;   /* must be 0 */
 } sag_desc;
+
+/*
+ * Tensors of one call (device pointers, 16-byte aligned, dense).  Rows are
+ * tokens in the descriptor's layout: R1 = T1 (TND) or B * s1_max (BSND),
+ * R2 = T2 or B * s2_max.
+ *   query               [R1, n1, d_qk]   dtype
+ *   key                 [R2, n2, d_qk]   dtype
+ *   value               [R2, n2, d_v]    dtype
+ *   attention_out       [R1, n1, d_v]    dtype (backward; required: Delta needs it)
+ *   attention_out_grad  [R1, n1, d_v]    dtype (backward)
+ *   softmax_max         [R1, n1, 8]      fp32 (backward: lane 0 is read; forward: written)
+ *   softmax_sum         [R1, n1, 8]      fp32 (idem)
+ *   topk_indices        [R1, n2, block_count] int32, block ids local to the
+ *                       token's batch
+ *   query_rope          [R1, n1, d_rope] dtype, NULL unless d_rope
+ *   key_rope            [R2, n2, d_rope] dtype, NULL unless d_rope
+ *   dq, dk, dv          like query, key, value: written by the backward
+ *   dq_rope, dk_rope    like query_rope, key_rope: written (NULL unless d_rope)
+ * The forward writes attention_out, softmax_max and softmax_sum and ignores
+ * attention_out_grad and the gradients.
+ */
+typedef struct sag_io {
+    const void *query, *key, *value;
+    void *attention_out;              /* read (never written) by the backward, written by the forward */
+    const void *attention_out_grad;
+    float *softmax_max, *softmax_sum; /* likewise */
+    const int32_t *topk_indices;
+    const void *query_rope, *key_rope;
+    void *dq, *dk, *dv;
+    void *dq_rope, *dk_rope;
+} sag_io;
 
 /*
  * Phase 1.  Validates the descriptor against the constraints (host only, no
@@ -150,6 +210,16 @@ sag_status sel_attn_grad(const sag_desc *desc, const void *query, const void *ke
  * SAG_ERR_TIMEOUT.  SAG_ERR_CUDA if the wait or the read fails.
  */
 sag_status sel_attn_grad_query_error(const void *workspace, void *stream);
+
+/*
+ * Phase 2 with every tensor in one sag_io (the form that takes the rope
+ * tensors) and two optional cudaEvent_t handles recorded around the main
+ * kernel as in sel_attn_grad_timed (NULL = not recorded).  Arguments,
+ * ownership and errors are those of sel_attn_grad; SAG_ERR_NULL also when
+ * d_rope is set and a rope pointer is NULL.
+ */
+sag_status sel_attn_grad_ex(const sag_desc *desc, const sag_io *io, void *workspace,
+                            size_t workspace_bytes, void *stream, void *main_start, void *main_stop);
 
 /*
  * Launch plan of a problem (host only, no CUDA call): what sel_attn_grad will
@@ -269,6 +339,16 @@ sag_status sel_attn_fwd_timed(const sag_desc *desc, const void *query, const voi
                               float *softmax_max, float *softmax_sum, void *workspace,
                               size_t workspace_bytes, void *stream, void *passes_start,
                               void *passes_stop);
+
+/*
+ * Forward phase 2 with the tensors in one sag_io: reads query, key, value,
+ * topk_indices (and query_rope, key_rope when d_rope), writes attention_out,
+ * softmax_max and softmax_sum (padding rows of BSND get zeros in all three);
+ * optional cudaEvent_t handles as in sel_attn_fwd_timed.  Statuses as for
+ * sel_attn_fwd.
+ */
+sag_status sel_attn_fwd_ex(const sag_desc *desc, const sag_io *io, void *workspace, size_t workspace_bytes,
+                           void *stream, void *passes_start, void *passes_stop);
 
 /* Static, human-readable name of a status code. */
 const char *sel_attn_grad_status_string(int status);

@@ -49,6 +49,8 @@ class _Problem(ctypes.Structure):
         ("cu_q", ctypes.c_void_p), ("cu_kv", ctypes.c_void_p), ("topk", ctypes.c_void_p),
         ("q", _Tensor), ("k", _Tensor), ("v", _Tensor), ("o", _Tensor), ("dy", _Tensor),
         ("smax", _Tensor), ("ssum", _Tensor),
+        ("layout", ctypes.c_int32), ("s1_max", ctypes.c_int32), ("s2_max", ctypes.c_int32),
+        ("pad2_", ctypes.c_int32),
     ]
 
 
@@ -117,7 +119,14 @@ def as_array(x, kind: str | None = None):
 
 @dataclass
 class Problem:
-    """One selected-attention problem in TND layout (host arrays)."""
+    """One selected-attention problem (host arrays).
+
+    Layout TND (0): rows of batch b are cu_q[b] .. cu_q[b+1]-1 (keys: cu_kv).
+    Layout BSND (1): every batch padded to s1_max query / s2_max key rows,
+    batch b starting at row b * s1_max (b * s2_max); cu_q / cu_kv then hold the
+    prefix sums of the valid lengths.  The array shapes below use T1 / T2 for
+    the rows of the query / key axis in either layout.
+    """
     cu_q: np.ndarray
     cu_kv: np.ndarray
     n1: int
@@ -137,6 +146,9 @@ class Problem:
     ssum: object = None   # [T1, n1, stat_stride]
     stat_stride: int = 8
     kind: str | None = None   # "bf16"/"f16" when 16-bit data arrives as uint16
+    layout: int = 0           # 0 TND, 1 BSND
+    s1_max: int = 0           # BSND: padded query rows per batch
+    s2_max: int = 0           # BSND: padded key rows per batch
 
     @property
     def batch(self) -> int:
@@ -144,11 +156,13 @@ class Problem:
 
     @property
     def t1(self) -> int:
-        return int(self.cu_q[-1])
+        """Rows of the query axis."""
+        return self.batch * self.s1_max if self.layout else int(self.cu_q[-1])
 
     @property
     def t2(self) -> int:
-        return int(self.cu_kv[-1])
+        """Rows of the key axis."""
+        return self.batch * self.s2_max if self.layout else int(self.cu_kv[-1])
 
     def _c(self):
         """(C struct, list of the arrays it points into).  The caller holds the
@@ -179,6 +193,7 @@ class Problem:
             topk=arr(topk, np.int32),
             q=ten(self.q), k=ten(self.k), v=ten(self.v), o=ten(self.o), dy=ten(self.dy),
             smax=ten(self.smax), ssum=ten(self.ssum),
+            layout=int(self.layout), s1_max=int(self.s1_max), s2_max=int(self.s2_max), pad2_=0,
         )
         return c, keep
 

@@ -34,6 +34,12 @@
  *       dQ   = scale * sum_j dS_j k_j
  *       dK_j += scale * dS_j q,   dV_j += P_j dY   (scatter-add to key rows)
  *     with scale = scaleValue (the reciprocal of sqrt(d) in the formula).
+ *   - layouts (the lightning-indexer page allows TND or BSND; the README's
+ *     calling section has a non-TND sample): in TND the rows of batch b are
+ *     cu_q[b] .. cu_q[b+1]-1 (keys: cu_kv); in BSND every batch is padded to
+ *     s1_max query / s2_max key rows, batch b starts at row b * s1_max
+ *     (b * s2_max) and cu_q / cu_kv hold the prefix sums of the valid lengths.
+ *     Padding rows take no part in the result; their gradients stay zero.
  */
 #include <math.h>
 #include <stdint.h>
@@ -71,6 +77,9 @@ typedef struct {
     sao_tensor dy;            /* [T1, n1, d_v]  attentionOutGrad (backward only) */
     sao_tensor smax;          /* [T1, n1, stat_stride] softmaxMax (backward only) */
     sao_tensor ssum;          /* [T1, n1, stat_stride] softmaxSum (backward only) */
+    int32_t layout;           /* 0: TND; 1: BSND, every batch padded to s1_max / s2_max rows */
+    int32_t s1_max, s2_max;   /* BSND only */
+    int32_t pad_;
 } sao_problem;
 
 /* ---- element decoding (exact: every 16-bit and fp32 value is a double) ---- */
@@ -110,12 +119,23 @@ static double ld(const sao_tensor *t, int64_t i)
 
 /* ---- problem bookkeeping ---- */
 
-static int64_t total_q(const sao_problem *p) { return p->cu_q[p->batch]; }
+/* first query / key row of batch b, and its valid query rows */
+static int64_t q_row0(const sao_problem *p, int b) { return p->layout ? (int64_t)b * p->s1_max : p->cu_q[b]; }
+static int64_t kv_row0(const sao_problem *p, int b) { return p->layout ? (int64_t)b * p->s2_max : p->cu_kv[b]; }
+static int64_t q_len(const sao_problem *p, int b) { return p->cu_q[b + 1] - p->cu_q[b]; }
 
+/* rows along the query / key axis of the tensors */
+static int64_t total_q(const sao_problem *p) { return p->layout ? (int64_t)p->batch * p->s1_max : p->cu_q[p->batch]; }
+static int64_t total_kv(const sao_problem *p)
+{
+    return p->layout ? (int64_t)p->batch * p->s2_max : p->cu_kv[p->batch];
+}
+
+/* batch of a valid query row, -1 for a padding row or one out of range */
 static int batch_of_token(const sao_problem *p, int64_t t)
 {
     for (int b = 0; b < p->batch; ++b)
-        if (t >= p->cu_q[b] && t < p->cu_q[b + 1]) return b;
+        if (t >= q_row0(p, b) && t < q_row0(p, b) + q_len(p, b)) return b;
     return -1;
 }
 
@@ -125,8 +145,11 @@ static int check_problem(const sao_problem *p)
     if (p->d_qk < 1 || p->d_v < 1 || p->block_size < 1 || p->block_count < 1) return SAO_EARG;
     if (!p->cu_q || !p->cu_kv || !p->topk) return SAO_EARG;
     if (p->cu_q[0] != 0 || p->cu_kv[0] != 0) return SAO_EARG;
-    for (int b = 0; b < p->batch; ++b)
+    if (p->layout != 0 && p->layout != 1) return SAO_EARG;
+    for (int b = 0; b < p->batch; ++b) {
         if (p->cu_q[b + 1] < p->cu_q[b] || p->cu_kv[b + 1] < p->cu_kv[b]) return SAO_EARG;
+        if (p->layout && (q_len(p, b) > p->s1_max || p->cu_kv[b + 1] - p->cu_kv[b] > p->s2_max)) return SAO_EARG;
+    }
     return SAO_OK;
 }
 
@@ -145,7 +168,7 @@ static int gather_rows(const sao_problem *p, int b, int64_t t, int n2, int64_t *
     for (int i = 0; i < p->block_count; ++i) {
         int64_t id = ids[i];
         if (id < 0 || id >= nblk) return SAO_EINDEX;
-        for (int r = 0; r < p->block_size; ++r) rows[L++] = p->cu_kv[b] + id * p->block_size + r;
+        for (int r = 0; r < p->block_size; ++r) rows[L++] = kv_row0(p, b) + id * p->block_size + r;
     }
     return SAO_OK;
 }
@@ -220,7 +243,7 @@ int sao_forward(const sao_problem *p, double *o, double *m_out, double *l_out)
     double *s = malloc(sizeof(double) * L);
     if (!rows || !s) { free(rows); free(s); return SAO_ENOMEM; }
     for (int b = 0; b < p->batch && rc == SAO_OK; ++b)
-        for (int64_t t = p->cu_q[b]; t < p->cu_q[b + 1] && rc == SAO_OK; ++t)
+        for (int64_t t = q_row0(p, b); t < q_row0(p, b) + q_len(p, b) && rc == SAO_OK; ++t)
             for (int h = 0; h < p->n1 && rc == SAO_OK; ++h) {
                 int64_t r = (int64_t)t * p->n1 + h;
                 rc = row_forward(p, b, t, h, rows, s, o + r * p->d_v, m_out + r, l_out + r);
@@ -272,7 +295,7 @@ static int row_backward(const sao_problem *p, int b, int64_t t, int h, int64_t *
     int rc = gather_rows(p, b, t, n2, rows);
     if (rc) return rc;
     /* key row -> first element of its dK / dV row in the target arrays */
-    int64_t blk_row0 = only_block < 0 ? 0 : p->cu_kv[b] + (int64_t)only_block * p->block_size;
+    int64_t blk_row0 = only_block < 0 ? 0 : kv_row0(p, b) + (int64_t)only_block * p->block_size;
     int64_t srow = ((int64_t)t * p->n1 + h) * p->stat_stride;
     double m = ld(&p->smax, srow);       /* lane 0 */
     double l = ld(&p->ssum, srow);
@@ -309,14 +332,14 @@ int sao_backward(const sao_problem *p, double *dq, double *dk, double *dv)
 {
     int rc = check_problem(p);
     if (rc) return rc;
-    int64_t T2 = p->cu_kv[p->batch];
+    int64_t T2 = total_kv(p);
     memset(dk, 0, sizeof(double) * T2 * p->n2 * p->d_qk);
     memset(dv, 0, sizeof(double) * T2 * p->n2 * p->d_v);
     int64_t L = (int64_t)p->block_count * p->block_size;
     int64_t *rows = malloc(sizeof(int64_t) * L);
     if (!rows) return SAO_ENOMEM;
     for (int b = 0; b < p->batch && rc == SAO_OK; ++b)
-        for (int64_t t = p->cu_q[b]; t < p->cu_q[b + 1] && rc == SAO_OK; ++t)
+        for (int64_t t = q_row0(p, b); t < q_row0(p, b) + q_len(p, b) && rc == SAO_OK; ++t)
             for (int h = 0; h < p->n1 && rc == SAO_OK; ++h)
                 rc = row_backward(p, b, t, h, rows, dq + ((int64_t)t * p->n1 + h) * p->d_qk, dk, dv, -1);
     free(rows);
@@ -354,8 +377,8 @@ int sao_dkdv_block_range(const sao_problem *p, int b, int n2, int kb, int64_t t_
     int rc = check_problem(p);
     if (rc) return rc;
     if (b < 0 || b >= p->batch || n2 < 0 || n2 >= p->n2 || kb < 0) return SAO_EARG;
-    if (t_lo < p->cu_q[b]) t_lo = p->cu_q[b];
-    if (t_hi > p->cu_q[b + 1]) t_hi = p->cu_q[b + 1];
+    if (t_lo < q_row0(p, b)) t_lo = q_row0(p, b);
+    if (t_hi > q_row0(p, b) + q_len(p, b)) t_hi = q_row0(p, b) + q_len(p, b);
     int G = p->n1 / p->n2;
     int64_t L = (int64_t)p->block_count * p->block_size;
     memset(dk_blk, 0, sizeof(double) * p->block_size * p->d_qk);
@@ -378,5 +401,5 @@ int sao_dkdv_block_range(const sao_problem *p, int b, int n2, int kb, int64_t t_
 int sao_dkdv_block(const sao_problem *p, int b, int n2, int kb, double *dk_blk, double *dv_blk)
 {
     if (!p || b < 0 || b >= p->batch) return SAO_EARG;
-    return sao_dkdv_block_range(p, b, n2, kb, p->cu_q[b], p->cu_q[b + 1], dk_blk, dv_blk);
+    return sao_dkdv_block_range(p, b, n2, kb, q_row0(p, b), q_row0(p, b) + q_len(p, b), dk_blk, dv_blk);
 }

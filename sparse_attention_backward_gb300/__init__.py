@@ -9,6 +9,11 @@ if the library is missing, importing the binding's entry points raises.
     dq, dk, dv = sab.backward(q, k, v, o, dy, softmax_max, softmax_sum, topk,
                               cu_seqlens_q, cu_seqlens_kv, scale,
                               block_size, block_count, deterministic=False)
+
+Tensors are TND ([T, N, D]) or, given as 4-D tensors, BSND ([B, S, N, D] with
+every batch padded to S rows; cu_seqlens then give the valid lengths).  With
+``q_rope`` / ``k_rope`` the head dim is split (Q = [q, q_rope] along D) and
+the gradients come back as (dq, dk, dv, dq_rope, dk_rope).
 """
 from __future__ import annotations
 
@@ -21,10 +26,11 @@ LIB_PATH = os.path.join(_PKG, "libselattn.so")
 SAG_OK, SAG_ERR_NULL, SAG_ERR_SHAPE, SAG_ERR_DTYPE, SAG_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
 SAG_ERR_WORKSPACE, SAG_ERR_ALIGN, SAG_ERR_CUDA, SAG_ERR_INDEX, SAG_ERR_TIMEOUT = 5, 6, 7, 8, 9
 SAG_BF16, SAG_FP16 = 0, 1
+SAG_LAYOUT_TND, SAG_LAYOUT_BSND = 0, 1
 
-EXPORTED = ("sel_attn_grad_workspace_size", "sel_attn_grad", "sel_attn_grad_timed",
+EXPORTED = ("sel_attn_grad_workspace_size", "sel_attn_grad", "sel_attn_grad_timed", "sel_attn_grad_ex",
             "sel_attn_grad_plan_info", "sel_attn_grad_query_error", "sel_attn_grad_status_string",
-            "sel_attn_fwd_workspace_size", "sel_attn_fwd", "sel_attn_fwd_timed")
+            "sel_attn_fwd_workspace_size", "sel_attn_fwd", "sel_attn_fwd_timed", "sel_attn_fwd_ex")
 
 
 class SagDesc(ctypes.Structure):
@@ -33,11 +39,20 @@ class SagDesc(ctypes.Structure):
         ("batch", ctypes.c_int32), ("n1", ctypes.c_int32), ("n2", ctypes.c_int32),
         ("d_qk", ctypes.c_int32), ("d_v", ctypes.c_int32),
         ("block_size", ctypes.c_int32), ("block_count", ctypes.c_int32),
-        ("dtype", ctypes.c_int32), ("deterministic", ctypes.c_int32), ("reserved_", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("deterministic", ctypes.c_int32), ("layout", ctypes.c_int32),
         ("scale", ctypes.c_double),
         ("cu_seqlens_q", ctypes.POINTER(ctypes.c_int32)),
         ("cu_seqlens_kv", ctypes.POINTER(ctypes.c_int32)),
+        ("s1_max", ctypes.c_int32), ("s2_max", ctypes.c_int32), ("d_rope", ctypes.c_int32),
+        ("reserved_", ctypes.c_int32),
     ]
+
+
+class SagIo(ctypes.Structure):
+    """Mirror of ``sag_io`` in include/selattn.h (device pointers as ints)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "query", "key", "value", "attention_out", "attention_out_grad", "softmax_max", "softmax_sum",
+        "topk_indices", "query_rope", "key_rope", "dq", "dk", "dv", "dq_rope", "dk_rope")]
 
 
 class SagPlanInfo(ctypes.Structure):
@@ -73,6 +88,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sel_attn_grad.restype = ctypes.c_int
     lib.sel_attn_grad_timed.argtypes = [D] + [vp] * 11 + [vp, sz, vp, vp, vp]
     lib.sel_attn_grad_timed.restype = ctypes.c_int
+    IO = ctypes.POINTER(SagIo)
+    lib.sel_attn_grad_ex.argtypes = [D, IO, vp, sz, vp, vp, vp]
+    lib.sel_attn_grad_ex.restype = ctypes.c_int
+    lib.sel_attn_fwd_ex.argtypes = [D, IO, vp, sz, vp, vp, vp]
+    lib.sel_attn_fwd_ex.restype = ctypes.c_int
     lib.sel_attn_grad_plan_info.argtypes = [D, ctypes.POINTER(SagPlanInfo)]
     lib.sel_attn_grad_plan_info.restype = ctypes.c_int
     lib.sel_attn_grad_query_error.argtypes = [vp, vp]
@@ -94,17 +114,59 @@ def status_string(status: int) -> str:
 
 
 def make_desc(cu_seqlens_q, cu_seqlens_kv, n1, n2, d_qk, d_v, block_size, block_count, scale,
-              dtype=SAG_BF16, deterministic=False):
-    """Build a descriptor; keeps the host cu_seqlens arrays alive on the object."""
+              dtype=SAG_BF16, deterministic=False, layout=SAG_LAYOUT_TND, s1_max=0, s2_max=0, d_rope=0):
+    """Build a descriptor; keeps the host cu_seqlens arrays alive on the object.
+
+    ``d_qk`` is the head dim of the query / key tensors (without the rope
+    part when ``d_rope`` is set); BSND takes the padded lengths s1_max, s2_max.
+    """
     cq = (ctypes.c_int32 * len(cu_seqlens_q))(*[int(x) for x in cu_seqlens_q])
     ck = (ctypes.c_int32 * len(cu_seqlens_kv))(*[int(x) for x in cu_seqlens_kv])
     d = SagDesc(batch=len(cu_seqlens_q) - 1, n1=n1, n2=n2, d_qk=d_qk, d_v=d_v,
                 block_size=block_size, block_count=block_count, dtype=dtype,
-                deterministic=1 if deterministic else 0, reserved_=0, scale=float(scale),
+                deterministic=1 if deterministic else 0, layout=int(layout), scale=float(scale),
                 cu_seqlens_q=ctypes.cast(cq, ctypes.POINTER(ctypes.c_int32)),
-                cu_seqlens_kv=ctypes.cast(ck, ctypes.POINTER(ctypes.c_int32)))
+                cu_seqlens_kv=ctypes.cast(ck, ctypes.POINTER(ctypes.c_int32)),
+                s1_max=int(s1_max), s2_max=int(s2_max), d_rope=int(d_rope), reserved_=0)
     d._keep = (cq, ck)
     return d
+
+
+def make_io(**ptrs) -> SagIo:
+    """sag_io from device pointers (ints); names as in the C struct, others NULL."""
+    io = SagIo()
+    for k, v in ptrs.items():
+        setattr(io, k, v)
+    return io
+
+
+def sel_attn_grad_ex(desc: SagDesc, io: SagIo, workspace, workspace_bytes: int, stream, main_start=None,
+                     main_stop=None) -> None:
+    """Phase 2 with every tensor in one sag_io; raises on a non-OK status."""
+    st = load().sel_attn_grad_ex(ctypes.byref(desc), ctypes.byref(io), workspace, workspace_bytes, stream,
+                                 main_start, main_stop)
+    if st != SAG_OK:
+        raise SagError(st, "sel_attn_grad_ex")
+
+
+def sel_attn_fwd_ex(desc: SagDesc, io: SagIo, workspace, workspace_bytes: int, stream, passes_start=None,
+                    passes_stop=None) -> None:
+    """Forward phase 2 with every tensor in one sag_io; raises on a non-OK status."""
+    st = load().sel_attn_fwd_ex(ctypes.byref(desc), ctypes.byref(io), workspace, workspace_bytes, stream,
+                                passes_start, passes_stop)
+    if st != SAG_OK:
+        raise SagError(st, "sel_attn_fwd_ex")
+
+
+def _layout_of(q, k, q_rope):
+    """(layout, s1_max, s2_max, n1, d_qk, n2, d_rope) from the tensors' shapes."""
+    if q.dim() == 4:
+        if k.dim() != 4:
+            raise ValueError("BSND needs 4-D query and key tensors")
+        layout, s1_max, s2_max = SAG_LAYOUT_BSND, q.shape[1], k.shape[1]
+    else:
+        layout, s1_max, s2_max = SAG_LAYOUT_TND, 0, 0
+    return layout, s1_max, s2_max, q.shape[-2], q.shape[-1], k.shape[-2], (q_rope.shape[-1] if q_rope is not None else 0)
 
 
 def workspace_size(desc: SagDesc) -> int:
@@ -154,39 +216,45 @@ def query_error(workspace, stream) -> int:
 
 def backward(q, k, v, o, dy, softmax_max, softmax_sum, topk, cu_seqlens_q, cu_seqlens_kv, scale,
              block_size, block_count, deterministic=False, out=None, workspace=None, stream=None,
-             check=False):
+             check=False, q_rope=None, k_rope=None):
     """torch-tensor convenience over the C ABI (allocation and marshalling only).
 
-    All tensors must be CUDA tensors in TND layout; returns (dq, dk, dv).  With
-    ``check`` the device status is read back (this synchronizes the stream).
+    All tensors must be contiguous CUDA tensors, TND ([T, N, D]) or BSND
+    ([B, S, N, D], 4-D); returns (dq, dk, dv), or (dq, dk, dv, dq_rope,
+    dk_rope) with the rope split.  With ``check`` the device status is read
+    back (this synchronizes the stream).
     """
     import torch
     if not q.is_cuda:
         raise ValueError("inputs must be CUDA tensors (there is no CPU path)")
     dtype = SAG_FP16 if q.dtype == torch.float16 else SAG_BF16
-    t1, n1, d_qk = q.shape
-    _, n2, d_v = v.shape
+    layout, s1_max, s2_max, n1, d_qk, n2, d_rope = _layout_of(q, k, q_rope)
+    d_v = v.shape[-1]
     desc = make_desc(cu_seqlens_q, cu_seqlens_kv, n1, n2, d_qk, d_v, block_size, block_count, scale,
-                     dtype, deterministic)
+                     dtype, deterministic, layout, s1_max, s2_max, d_rope)
     need = workspace_size(desc)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     if out is None:
         out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
-    dq, dk, dv = out
+        if d_rope:
+            out = out + (torch.empty_like(q_rope), torch.empty_like(k_rope))
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    tensors = (q, k, v, o, dy, softmax_max, softmax_sum, topk, dq, dk, dv)
-    for t in tensors:
+    named = dict(query=q, key=k, value=v, attention_out=o, attention_out_grad=dy, softmax_max=softmax_max,
+                 softmax_sum=softmax_sum, topk_indices=topk, dq=out[0], dk=out[1], dv=out[2])
+    if d_rope:
+        named.update(query_rope=q_rope, key_rope=k_rope, dq_rope=out[3], dk_rope=out[4])
+    for t in named.values():
         if not t.is_contiguous():
             raise ValueError("all tensors must be contiguous")
-    sel_attn_grad(desc, *[t.data_ptr() for t in tensors], workspace.data_ptr(), need,
-                  stream.cuda_stream)
+    io = make_io(**{k_: t.data_ptr() for k_, t in named.items()})
+    sel_attn_grad_ex(desc, io, workspace.data_ptr(), need, stream.cuda_stream)
     if check:
         st = query_error(workspace.data_ptr(), stream.cuda_stream)
         if st != SAG_OK:
             raise SagError(st, "device")
-    return dq, dk, dv
+    return out
 
 
 def fwd_workspace_size(desc: SagDesc) -> int:
@@ -215,32 +283,37 @@ def sel_attn_fwd(desc: SagDesc, query, key, value, topk_indices, attention_out, 
 
 
 def forward(q, k, v, topk, cu_seqlens_q, cu_seqlens_kv, scale, block_size, block_count,
-            out=None, workspace=None, stream=None, check=False):
+            out=None, workspace=None, stream=None, check=False, q_rope=None, k_rope=None):
     """torch-tensor convenience over the forward's C ABI: returns
-    (attention_out [T1, n1, d_v], softmax_max [T1, n1, 8], softmax_sum [T1, n1, 8])."""
+    (attention_out [.., n1, d_v], softmax_max [.., n1, 8], softmax_sum [.., n1, 8])
+    in the layout of q (TND or 4-D BSND)."""
     import torch
     if not q.is_cuda:
         raise ValueError("inputs must be CUDA tensors (there is no CPU path)")
     dtype = SAG_FP16 if q.dtype == torch.float16 else SAG_BF16
-    t1, n1, d_qk = q.shape
-    _, n2, d_v = v.shape
+    layout, s1_max, s2_max, n1, d_qk, n2, d_rope = _layout_of(q, k, q_rope)
+    d_v = v.shape[-1]
     desc = make_desc(cu_seqlens_q, cu_seqlens_kv, n1, n2, d_qk, d_v, block_size, block_count, scale,
-                     dtype, False)
+                     dtype, False, layout, s1_max, s2_max, d_rope)
     need = fwd_workspace_size(desc)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    lead = tuple(q.shape[:-1])
     if out is None:
-        out = (torch.empty((t1, n1, d_v), dtype=q.dtype, device=q.device),
-               torch.empty((t1, n1, 8), dtype=torch.float32, device=q.device),
-               torch.empty((t1, n1, 8), dtype=torch.float32, device=q.device))
+        out = (torch.empty(lead + (d_v,), dtype=q.dtype, device=q.device),
+               torch.empty(lead + (8,), dtype=torch.float32, device=q.device),
+               torch.empty(lead + (8,), dtype=torch.float32, device=q.device))
     o, smax, ssum = out
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    for t in (q, k, v, topk, o, smax, ssum):
+    named = dict(query=q, key=k, value=v, topk_indices=topk, attention_out=o, softmax_max=smax, softmax_sum=ssum)
+    if d_rope:
+        named.update(query_rope=q_rope, key_rope=k_rope)
+    for t in named.values():
         if not t.is_contiguous():
             raise ValueError("all tensors must be contiguous")
-    sel_attn_fwd(desc, q.data_ptr(), k.data_ptr(), v.data_ptr(), topk.data_ptr(), o.data_ptr(),
-                 smax.data_ptr(), ssum.data_ptr(), workspace.data_ptr(), need, stream.cuda_stream)
+    io = make_io(**{k_: t.data_ptr() for k_, t in named.items()})
+    sel_attn_fwd_ex(desc, io, workspace.data_ptr(), need, stream.cuda_stream)
     if check:
         st = query_error(workspace.data_ptr(), stream.cuda_stream)
         if st != SAG_OK:

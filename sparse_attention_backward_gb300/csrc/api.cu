@@ -48,6 +48,11 @@ struct Plan {
         o_entries, o_wtab, o_delta, o_lse2, o_dq_acc, o_ds, o_dkv, total;
     int32_t chunk_tokens, n_chunks;
     bool use_tc;                      // tensor-core main kernel (else the CUDA-core one)
+    size_t o_q_end, o_kv_blocks;
+    std::vector<int32_t> row_q;       // host copy, B+1: first query row of each batch
+    std::vector<int32_t> row_kv;      // host copy, B+1: first key row of each batch
+    std::vector<int32_t> q_end;       // host copy, B: end of the valid query rows
+    std::vector<int32_t> kv_blocks;   // host copy, B: valid key blocks
     std::vector<int64_t> item_base;   // host copy, B+1
     std::vector<int64_t> unit_base;   // host copy, B+1 (windowed)
     std::vector<int64_t> wtab_base;   // host copy, B+1 (windowed)
@@ -57,22 +62,36 @@ sag_status validate(const sag_desc *d) {
     if (!d || !d->cu_seqlens_q || !d->cu_seqlens_kv) return SAG_ERR_NULL;
     if (d->dtype != SAG_BF16 && d->dtype != SAG_FP16) return SAG_ERR_DTYPE;
     if (d->reserved_ != 0 || (d->deterministic != 0 && d->deterministic != 1)) return SAG_ERR_SHAPE;
+    if (d->layout != SAG_LAYOUT_TND && d->layout != SAG_LAYOUT_BSND) return SAG_ERR_SHAPE;
     if (d->batch < 1 || d->batch > kMaxTokens) return SAG_ERR_SHAPE;
     if (d->n1 < 1 || d->n1 > 128 || d->n2 < 1 || d->n2 > 128 || d->n1 % d->n2 != 0) return SAG_ERR_SHAPE;
     if (d->n1 / d->n2 > 32) return SAG_ERR_SHAPE;
-    if ((d->d_qk != 128 && d->d_qk != 192) || (d->d_v != 128 && d->d_v != 192)) return SAG_ERR_SHAPE;
+    if (d->d_rope != 0 && d->d_rope != 64) return SAG_ERR_SHAPE;
+    const int d_qk = d->d_qk + d->d_rope;     // head dim of the attention
+    if ((d_qk != 128 && d_qk != 192) || (d->d_v != 128 && d->d_v != 192)) return SAG_ERR_SHAPE;
+    // the rope split is built for the tensor-core kernels' 128 + 64 layout
+    if (d->d_rope && (d->d_qk != 128 || d->d_v != 128)) return SAG_ERR_UNSUPPORTED;
     if (d->block_size < 16 || d->block_size > 128 || d->block_size % 16 != 0) return SAG_ERR_SHAPE;
     if (d->block_count < 1 || d->block_count > 128) return SAG_ERR_SHAPE;
     if ((int64_t)d->block_size * d->block_count >= 8192) return SAG_ERR_SHAPE;
     if (!(d->scale == d->scale) || d->scale > 1e30 || d->scale < -1e30) return SAG_ERR_SHAPE;
+    const bool bsnd = d->layout == SAG_LAYOUT_BSND;
+    if (bsnd) {
+        if (d->s1_max < 1 || d->s1_max > kMaxSeq || d->s2_max < 1 || d->s2_max > kMaxSeq) return SAG_ERR_SHAPE;
+        if (d->s2_max % d->block_size != 0) return SAG_ERR_SHAPE;
+        if ((int64_t)d->batch * d->s1_max > kMaxTokens || (int64_t)d->batch * d->s2_max > kMaxTokens)
+            return SAG_ERR_SHAPE;
+    } else if (d->s1_max != 0 || d->s2_max != 0) {
+        return SAG_ERR_SHAPE;
+    }
     const int32_t *cq = d->cu_seqlens_q, *ck = d->cu_seqlens_kv;
     if (cq[0] != 0 || ck[0] != 0) return SAG_ERR_SHAPE;
     const int64_t sel = (int64_t)d->block_size * d->block_count;
     for (int b = 0; b < d->batch; ++b) {
         const int64_t s1 = (int64_t)cq[b + 1] - cq[b];
         const int64_t s2 = (int64_t)ck[b + 1] - ck[b];
-        if (s1 < 0 || s1 > kMaxSeq) return SAG_ERR_SHAPE;
-        if (s2 < sel || s2 > kMaxSeq || s2 % d->block_size != 0) return SAG_ERR_SHAPE;
+        if (s1 < 0 || s1 > (bsnd ? d->s1_max : kMaxSeq)) return SAG_ERR_SHAPE;
+        if (s2 < sel || s2 > (bsnd ? d->s2_max : kMaxSeq) || s2 % d->block_size != 0) return SAG_ERR_SHAPE;
     }
     const int64_t t1 = cq[d->batch], t2 = ck[d->batch];
     if (t1 < 1 || t1 > kMaxTokens || t2 < 1 || t2 > kMaxTokens) return SAG_ERR_SHAPE;
@@ -85,13 +104,28 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     sag_status st = validate(d);
     if (st != SAG_OK) return st;
     Geometry &g = p->g;
+    const bool bsnd = d->layout == SAG_LAYOUT_BSND;
     g.batch = d->batch;
-    g.t1 = d->cu_seqlens_q[d->batch];
-    g.t2 = d->cu_seqlens_kv[d->batch];
+    // rows of the tensors: packed (TND) or every batch padded to s*_max (BSND)
+    p->row_q.assign(d->batch + 1, 0);
+    p->row_kv.assign(d->batch + 1, 0);
+    p->q_end.assign(d->batch, 0);
+    p->kv_blocks.assign(d->batch, 0);
+    for (int b = 0; b <= d->batch; ++b) {
+        p->row_q[b] = bsnd ? b * d->s1_max : d->cu_seqlens_q[b];
+        p->row_kv[b] = bsnd ? b * d->s2_max : d->cu_seqlens_kv[b];
+    }
+    for (int b = 0; b < d->batch; ++b) {
+        p->q_end[b] = p->row_q[b] + (d->cu_seqlens_q[b + 1] - d->cu_seqlens_q[b]);
+        p->kv_blocks[b] = (d->cu_seqlens_kv[b + 1] - d->cu_seqlens_kv[b]) / d->block_size;
+    }
+    g.t1 = p->row_q[d->batch];
+    g.t2 = p->row_kv[d->batch];
     g.n1 = d->n1;
     g.n2 = d->n2;
     g.group = d->n1 / d->n2;
-    g.d_qk = d->d_qk;
+    g.d_rope = d->d_rope;
+    g.d_qk = d->d_qk + d->d_rope;
     g.d_v = d->d_v;
     g.block_size = d->block_size;
     g.block_count = d->block_count;
@@ -101,7 +135,9 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     p->det = d->deterministic != 0;
     p->item_base.assign(d->batch + 1, 0);
     for (int b = 0; b < d->batch; ++b) {
-        const int64_t nblk = (d->cu_seqlens_kv[b + 1] - d->cu_seqlens_kv[b]) / d->block_size;
+        // every block of the (padded) key rows is an item: blocks no token may
+        // select (BSND padding) get empty buckets and zero gradients
+        const int64_t nblk = (p->row_kv[b + 1] - p->row_kv[b]) / d->block_size;
         p->item_base[b + 1] = p->item_base[b] + nblk * d->n2;
     }
     g.n_items = p->item_base[d->batch];
@@ -115,6 +151,7 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     // tensor-core one also covers (used to cross-check the two)
     const char *force = getenv("SELATTN_FORCE_CUDA_CORE");
     p->use_tc = bwd_tc_supported(g) && !(force && force[0] == '1');
+    if (g.d_rope && !p->use_tc) return SAG_ERR_UNSUPPORTED;
     if (forward) {
         if (p->det) return SAG_ERR_UNSUPPORTED;   // the forward's sums are order-dependent
         p->use_tc = fwd_tc_supported(g);
@@ -141,7 +178,7 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     p->wtab_base.assign(d->batch + 1, 0);
     if (g.windowed) {
         for (int b = 0; b < d->batch; ++b) {
-            const int64_t s1 = d->cu_seqlens_q[b + 1] - d->cu_seqlens_q[b];
+            const int64_t s1 = p->row_q[b + 1] - p->row_q[b];
             const int64_t nwin = (s1 + g.window - 1) / g.window;
             const int64_t items_b = p->item_base[b + 1] - p->item_base[b];
             p->unit_base[b + 1] = p->unit_base[b] + nwin * items_b * g.halves;
@@ -157,6 +194,8 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     p->o_item_base = take(sizeof(int64_t) * (g.batch + 1));
     p->o_unit_base = take(sizeof(int64_t) * (g.batch + 1));
     p->o_wtab_base = take(sizeof(int64_t) * (g.batch + 1));
+    p->o_q_end = take(sizeof(int32_t) * g.batch);
+    p->o_kv_blocks = take(sizeof(int32_t) * g.batch);
     p->o_count = take(sizeof(int32_t) * (g.n_items + 1));
     p->o_cursor = take(sizeof(int32_t) * g.n_items);
     p->o_offset = take(sizeof(int32_t) * (g.n_items + 1));
@@ -191,6 +230,8 @@ Workspace carve(const Plan &p, void *base) {
     w.hdr = reinterpret_cast<WsHeader *>(c + p.o_hdr);
     w.cu_q = reinterpret_cast<int32_t *>(c + p.o_cu_q);
     w.cu_kv = reinterpret_cast<int32_t *>(c + p.o_cu_kv);
+    w.q_end = reinterpret_cast<int32_t *>(c + p.o_q_end);
+    w.kv_blocks = reinterpret_cast<int32_t *>(c + p.o_kv_blocks);
     w.item_base = reinterpret_cast<int64_t *>(c + p.o_item_base);
     w.count = reinterpret_cast<int32_t *>(c + p.o_count);
     w.offset = reinterpret_cast<int32_t *>(c + p.o_offset);
@@ -271,6 +312,56 @@ extern "C" sag_status sel_attn_grad_plan_info(const sag_desc *desc, sag_plan_inf
     return SAG_OK;
 }
 
+namespace {
+
+// Checks shared by the backward and the forward: required pointers,
+// alignment, workspace size.
+sag_status check_io(const Plan &p, const void *const *ptrs, int n, const sag_io *io, void *workspace,
+                    size_t workspace_bytes) {
+    for (int i = 0; i < n; ++i)
+        if (!ptrs[i]) return SAG_ERR_NULL;
+    if (p.g.d_rope && (!io->query_rope || !io->key_rope)) return SAG_ERR_NULL;
+    if (!workspace) return SAG_ERR_WORKSPACE;
+    for (int i = 0; i < n; ++i)
+        if (!aligned16(ptrs[i])) return SAG_ERR_ALIGN;
+    if (p.g.d_rope && (!aligned16(io->query_rope) || !aligned16(io->key_rope))) return SAG_ERR_ALIGN;
+    if (!aligned16(workspace)) return SAG_ERR_ALIGN;
+    if (workspace_bytes < p.total) return SAG_ERR_WORKSPACE;
+    return SAG_OK;
+}
+
+// Header reset, the host metadata copy (row starts, valid ends, item and
+// window bases) and the bucket counters' memset.  The host buffer is
+// pageable: the copy has consumed it by the time cudaMemcpyAsync returns.
+sag_status stage_metadata(const Plan &p, void *workspace, cudaStream_t s) {
+    const Geometry &g = p.g;
+    std::vector<char> meta(p.o_count - p.o_cu_q, 0);
+    auto put = [&](size_t off, const void *src, size_t bytes) { memcpy(meta.data() + (off - p.o_cu_q), src, bytes); };
+    put(p.o_cu_q, p.row_q.data(), sizeof(int32_t) * (g.batch + 1));
+    put(p.o_cu_kv, p.row_kv.data(), sizeof(int32_t) * (g.batch + 1));
+    put(p.o_item_base, p.item_base.data(), sizeof(int64_t) * (g.batch + 1));
+    put(p.o_unit_base, p.unit_base.data(), sizeof(int64_t) * (g.batch + 1));
+    put(p.o_wtab_base, p.wtab_base.data(), sizeof(int64_t) * (g.batch + 1));
+    put(p.o_q_end, p.q_end.data(), sizeof(int32_t) * g.batch);
+    put(p.o_kv_blocks, p.kv_blocks.data(), sizeof(int32_t) * g.batch);
+    char *base = static_cast<char *>(workspace);
+    if (cudaMemsetAsync(base + p.o_hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return SAG_ERR_CUDA;
+    if (cudaMemcpyAsync(base + p.o_cu_q, meta.data(), meta.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return SAG_ERR_CUDA;
+    // count and cursor are adjacent: one memset
+    if (cudaMemsetAsync(base + p.o_count, 0, p.o_offset - p.o_count, s) != cudaSuccess) return SAG_ERR_CUDA;
+    return SAG_OK;
+}
+
+cudaError_t launch_main(const Plan &p, const Geometry &g, const Workspace &ws, const sag_io &io, bool det,
+                        cudaStream_t s, int sms) {
+    if (!p.use_tc) return launch_bwd_simt(g, ws, io, p.fp16, det, s, sms);
+    if (bwd_split_preferred(g)) return launch_bwd_tc_split(g, ws, io, p.fp16, det, s, sms);
+    return launch_bwd_tc(g, ws, io, p.fp16, det, s, sms);
+}
+
+}  // namespace
+
 extern "C" sag_status sel_attn_grad(const sag_desc *desc, const void *query, const void *key,
                                     const void *value, const void *attention_out,
                                     const void *attention_out_grad, const float *softmax_max,
@@ -288,19 +379,35 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
                                           const float *softmax_sum, const int32_t *topk_indices, void *dq,
                                           void *dk, void *dv, void *workspace, size_t workspace_bytes,
                                           void *stream, void *main_start, void *main_stop) {
+    sag_io io{};
+    io.query = query;
+    io.key = key;
+    io.value = value;
+    // the backward only reads these three
+    io.attention_out = const_cast<void *>(attention_out);
+    io.attention_out_grad = attention_out_grad;
+    io.softmax_max = const_cast<float *>(softmax_max);
+    io.softmax_sum = const_cast<float *>(softmax_sum);
+    io.topk_indices = topk_indices;
+    io.dq = dq;
+    io.dk = dk;
+    io.dv = dv;
+    return sel_attn_grad_ex(desc, &io, workspace, workspace_bytes, stream, main_start, main_stop);
+}
+
+extern "C" sag_status sel_attn_grad_ex(const sag_desc *desc, const sag_io *io, void *workspace,
+                                       size_t workspace_bytes, void *stream, void *main_start, void *main_stop) {
     cudaEvent_t ev0 = static_cast<cudaEvent_t>(main_start), ev1 = static_cast<cudaEvent_t>(main_stop);
     Plan p;
     sag_status st = make_plan(desc, &p);
     if (st != SAG_OK) return st;
-    const void *ptrs[] = {query, key, value, attention_out, attention_out_grad, softmax_max,
-                          softmax_sum, topk_indices, dq, dk, dv};
-    for (const void *x : ptrs)
-        if (!x) return SAG_ERR_NULL;
-    if (!workspace) return SAG_ERR_WORKSPACE;
-    for (const void *x : ptrs)
-        if (!aligned16(x)) return SAG_ERR_ALIGN;
-    if (!aligned16(workspace)) return SAG_ERR_ALIGN;
-    if (workspace_bytes < p.total) return SAG_ERR_WORKSPACE;
+    if (!io) return SAG_ERR_NULL;
+    const void *ptrs[] = {io->query, io->key, io->value, io->attention_out, io->attention_out_grad, io->softmax_max,
+                          io->softmax_sum, io->topk_indices, io->dq, io->dk, io->dv};
+    st = check_io(p, ptrs, 11, io, workspace, workspace_bytes);
+    if (st != SAG_OK) return st;
+    if (p.g.d_rope && (!io->dq_rope || !io->dk_rope)) return SAG_ERR_NULL;
+    if (p.g.d_rope && (!aligned16(io->dq_rope) || !aligned16(io->dk_rope))) return SAG_ERR_ALIGN;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     DeviceGuard dg;
@@ -308,45 +415,23 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
     const Geometry &g = p.g;
     Workspace ws = carve(p, workspace);
     const int sms = device_sms();
+    st = stage_metadata(p, workspace, s);
+    if (st != SAG_OK) return st;
 
-    // staged host metadata: cu_q, cu_kv, item_base (pageable source: the copy
-    // has consumed it by the time cudaMemcpyAsync returns)
-    std::vector<char> meta(p.o_count - p.o_cu_q, 0);
-    memcpy(meta.data() + (p.o_cu_q - p.o_cu_q), desc->cu_seqlens_q, sizeof(int32_t) * (g.batch + 1));
-    memcpy(meta.data() + (p.o_cu_kv - p.o_cu_q), desc->cu_seqlens_kv, sizeof(int32_t) * (g.batch + 1));
-    memcpy(meta.data() + (p.o_item_base - p.o_cu_q), p.item_base.data(), sizeof(int64_t) * (g.batch + 1));
-    memcpy(meta.data() + (p.o_unit_base - p.o_cu_q), p.unit_base.data(), sizeof(int64_t) * (g.batch + 1));
-    memcpy(meta.data() + (p.o_wtab_base - p.o_cu_q), p.wtab_base.data(), sizeof(int64_t) * (g.batch + 1));
-
-    char *base = static_cast<char *>(workspace);
-    if ((cudaMemsetAsync(base + p.o_hdr, 0, sizeof(WsHeader), s)) != cudaSuccess) return SAG_ERR_CUDA;
-    if ((cudaMemcpyAsync(base + p.o_cu_q, meta.data(), meta.size(), cudaMemcpyHostToDevice, s)) !=
-        cudaSuccess)
+    if ((launch_preprocess(g, ws, io->attention_out, io->attention_out_grad, io->softmax_max, io->softmax_sum,
+                           p.fp16, !p.det, s, sms)) != cudaSuccess)
         return SAG_ERR_CUDA;
-    // count and cursor are adjacent: one memset
-    if ((cudaMemsetAsync(base + p.o_count, 0, p.o_offset - p.o_count, s)) != cudaSuccess) return SAG_ERR_CUDA;
-
-    if ((launch_preprocess(g, ws, attention_out, attention_out_grad, softmax_max, softmax_sum, p.fp16,
-                               !p.det, s, sms)) != cudaSuccess)
-        return SAG_ERR_CUDA;
-    if ((launch_inversion(g, ws, topk_indices, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
+    if ((launch_inversion(g, ws, io->topk_indices, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
     if (!p.det) {
         if (g.windowed &&
             cudaMemsetAsync(ws.dkv_acc, 0, sizeof(float) * (size_t)g.t2 * g.n2 * (g.d_qk + g.d_v), s) != cudaSuccess)
             return SAG_ERR_CUDA;
         if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return SAG_ERR_CUDA;
-        if ((!p.use_tc ? launch_bwd_simt(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s,
-                                             sms)
-                 : bwd_split_preferred(g)
-                     ? launch_bwd_tc_split(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s, sms)
-                     : launch_bwd_tc(g, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, false, s, sms)) !=
-            cudaSuccess)
-            return SAG_ERR_CUDA;
+        if (launch_main(p, g, ws, *io, false, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
         if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SAG_ERR_CUDA;
-        if ((launch_cast(ws.dq_acc, dq, (int64_t)g.t1 * g.n1 * g.d_qk, g.scale, p.fp16, s, sms)) !=
-            cudaSuccess)
+        if ((launch_cast_dq(g, ws.dq_acc, io->dq, io->dq_rope, p.fp16, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
+        if (g.windowed && (launch_cast_dkv(g, ws, io->dk, io->dk_rope, io->dv, p.fp16, s, sms)) != cudaSuccess)
             return SAG_ERR_CUDA;
-        if (g.windowed && (launch_cast_dkv(g, ws, dk, dv, p.fp16, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
         return SAG_OK;
     }
     // deterministic: token chunks in order; dS of a chunk -> its dQ
@@ -358,20 +443,14 @@ extern "C" sag_status sel_attn_grad_timed(const sag_desc *desc, const void *quer
         Geometry gc = g;
         gc.tok_lo = c * p.chunk_tokens;
         gc.tok_hi = gc.tok_lo + p.chunk_tokens < g.t1 ? gc.tok_lo + p.chunk_tokens : g.t1;
-        if ((!p.use_tc ? launch_bwd_simt(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s,
-                                             sms)
-                 : bwd_split_preferred(gc)
-                     ? launch_bwd_tc_split(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s, sms)
-                     : launch_bwd_tc(gc, ws, query, key, value, attention_out_grad, dk, dv, p.fp16, true, s, sms)) !=
-            cudaSuccess)
-            return SAG_ERR_CUDA;
-        if (((p.use_tc && dq_tc_supported(gc)) ? launch_dq_tc(gc, ws, key, topk_indices, dq, p.fp16, s, sms)
-                                                    : launch_dq_from_ds(gc, ws, key, topk_indices, dq, p.fp16, s, sms)) !=
-            cudaSuccess)
+        if (launch_main(p, gc, ws, *io, true, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
+        if (((p.use_tc && dq_tc_supported(gc)) ? launch_dq_tc(gc, ws, *io, p.fp16, s, sms)
+                                                : launch_dq_from_ds(gc, ws, *io, p.fp16, s, sms)) != cudaSuccess)
             return SAG_ERR_CUDA;
     }
     if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SAG_ERR_CUDA;
-    if (g.chunked && (launch_cast_dkv(g, ws, dk, dv, p.fp16, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
+    if (g.chunked && (launch_cast_dkv(g, ws, io->dk, io->dk_rope, io->dv, p.fp16, s, sms)) != cudaSuccess)
+        return SAG_ERR_CUDA;
     return SAG_OK;
 }
 
@@ -396,18 +475,28 @@ extern "C" sag_status sel_attn_fwd_timed(const sag_desc *desc, const void *query
                                          float *softmax_max, float *softmax_sum, void *workspace,
                                          size_t workspace_bytes, void *stream, void *passes_start,
                                          void *passes_stop) {
+    sag_io io{};
+    io.query = query;
+    io.key = key;
+    io.value = value;
+    io.topk_indices = topk_indices;
+    io.attention_out = attention_out;
+    io.softmax_max = softmax_max;
+    io.softmax_sum = softmax_sum;
+    return sel_attn_fwd_ex(desc, &io, workspace, workspace_bytes, stream, passes_start, passes_stop);
+}
+
+extern "C" sag_status sel_attn_fwd_ex(const sag_desc *desc, const sag_io *io, void *workspace,
+                                      size_t workspace_bytes, void *stream, void *passes_start, void *passes_stop) {
     cudaEvent_t ev0 = static_cast<cudaEvent_t>(passes_start), ev1 = static_cast<cudaEvent_t>(passes_stop);
     Plan p;
     sag_status st = make_plan(desc, &p, true);
     if (st != SAG_OK) return st;
-    const void *ptrs[] = {query, key, value, topk_indices, attention_out, softmax_max, softmax_sum};
-    for (const void *x : ptrs)
-        if (!x) return SAG_ERR_NULL;
-    if (!workspace) return SAG_ERR_WORKSPACE;
-    for (const void *x : ptrs)
-        if (!aligned16(x)) return SAG_ERR_ALIGN;
-    if (!aligned16(workspace)) return SAG_ERR_ALIGN;
-    if (workspace_bytes < p.total) return SAG_ERR_WORKSPACE;
+    if (!io) return SAG_ERR_NULL;
+    const void *ptrs[] = {io->query, io->key, io->value, io->topk_indices, io->attention_out, io->softmax_max,
+                          io->softmax_sum};
+    st = check_io(p, ptrs, 7, io, workspace, workspace_bytes);
+    if (st != SAG_OK) return st;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     DeviceGuard dg;
@@ -415,24 +504,16 @@ extern "C" sag_status sel_attn_fwd_timed(const sag_desc *desc, const void *query
     const Geometry &g = p.g;
     Workspace ws = carve(p, workspace);
     const int sms = device_sms();
-    std::vector<char> meta(p.o_count - p.o_cu_q, 0);
-    memcpy(meta.data() + (p.o_cu_q - p.o_cu_q), desc->cu_seqlens_q, sizeof(int32_t) * (g.batch + 1));
-    memcpy(meta.data() + (p.o_cu_kv - p.o_cu_q), desc->cu_seqlens_kv, sizeof(int32_t) * (g.batch + 1));
-    memcpy(meta.data() + (p.o_item_base - p.o_cu_q), p.item_base.data(), sizeof(int64_t) * (g.batch + 1));
-    memcpy(meta.data() + (p.o_unit_base - p.o_cu_q), p.unit_base.data(), sizeof(int64_t) * (g.batch + 1));
-    memcpy(meta.data() + (p.o_wtab_base - p.o_cu_q), p.wtab_base.data(), sizeof(int64_t) * (g.batch + 1));
-    char *base = static_cast<char *>(workspace);
-    if (cudaMemsetAsync(base + p.o_hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return SAG_ERR_CUDA;
-    if (cudaMemcpyAsync(base + p.o_cu_q, meta.data(), meta.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return SAG_ERR_CUDA;
-    if (cudaMemsetAsync(base + p.o_count, 0, p.o_offset - p.o_count, s) != cudaSuccess) return SAG_ERR_CUDA;
+    st = stage_metadata(p, workspace, s);
+    if (st != SAG_OK) return st;
     if (launch_fwd_init(g, ws, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
-    if (launch_inversion(g, ws, topk_indices, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
+    if (launch_inversion(g, ws, io->topk_indices, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
     if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return SAG_ERR_CUDA;
     for (int pass = 1; pass <= 2; ++pass)
-        if (launch_fwd_tc(g, ws, query, key, value, pass, p.fp16, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
+        if (launch_fwd_tc(g, ws, *io, pass, p.fp16, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SAG_ERR_CUDA;
-    if (launch_fwd_finalize(g, ws, attention_out, softmax_max, softmax_sum, p.fp16, s, sms) != cudaSuccess)
+    if (launch_fwd_finalize(g, ws, io->attention_out, io->softmax_max, io->softmax_sum, p.fp16, s, sms) !=
+        cudaSuccess)
         return SAG_ERR_CUDA;
     return SAG_OK;
 }

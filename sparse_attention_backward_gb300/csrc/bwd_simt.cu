@@ -180,10 +180,12 @@ __global__ void __launch_bounds__(512) k_bwd_simt(Geometry g, Workspace ws,
 template <bool kFp16, int DQK>
 __global__ void __launch_bounds__(256) k_dq_from_ds(Geometry g, Workspace ws,
                                                     const uint16_t *__restrict__ k,
+                                                    const uint16_t *__restrict__ k_rope,
                                                     const int32_t *__restrict__ topk,
-                                                    uint16_t *__restrict__ dq) {
+                                                    uint16_t *__restrict__ dq, uint16_t *__restrict__ dq_rope) {
     extern __shared__ float smem[];
     const int bs = g.block_size, G = g.group;
+    const int d_main = DQK - g.d_rope;
     float *sk = smem;               // [bs][DQK]
     float *sds = sk + bs * DQK;     // [G][bs]
     const int64_t npairs = (int64_t)(g.tok_hi - g.tok_lo) * g.n2;
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(256) k_dq_from_ds(Geometry g, Workspace ws,
         const int t = g.tok_lo + (int)(cp / g.n2), n2 = (int)(cp % g.n2);
         const int64_t pair = (int64_t)t * g.n2 + n2;
         const int b = batch_of(ws.cu_q, g.batch, t);
-        const int nblk = (ws.cu_kv[b + 1] - ws.cu_kv[b]) / bs;
+        const int nblk = t < ws.q_end[b] ? ws.kv_blocks[b] : 0;   // ids must be below; none for padding
         // each thread owns outputs o = threadIdx.x + 256*i over G*DQK
         constexpr int kMaxPerThread = (32 * DQK + 255) / 256;
         float acc[kMaxPerThread];
@@ -204,7 +206,8 @@ __global__ void __launch_bounds__(256) k_dq_from_ds(Geometry g, Workspace ws,
             __syncthreads();
             for (int i = threadIdx.x; i < bs * DQK; i += blockDim.x) {
                 const int r = i / DQK, d = i % DQK;
-                sk[i] = u16_to_f<kFp16>(k[((key0 + r) * g.n2 + n2) * DQK + d]);
+                const int64_t krow = (key0 + r) * g.n2 + n2;
+                sk[i] = u16_to_f<kFp16>(d < d_main ? k[krow * d_main + d] : k_rope[krow * g.d_rope + d - d_main]);
             }
             const int64_t dbase = (cp * g.block_count + slot) * (int64_t)G * bs;
             for (int i = threadIdx.x; i < G * bs; i += blockDim.x) sds[i] = u16_to_f<kFp16>(ws.ds[dbase + i]);
@@ -225,7 +228,8 @@ __global__ void __launch_bounds__(256) k_dq_from_ds(Geometry g, Workspace ws,
             const int o = threadIdx.x + 256 * i;
             if (o < G * DQK) {
                 const int gg = o / DQK, d = o % DQK;
-                dq[((int64_t)t * g.n1 + n2 * G + gg) * DQK + d] = f_to_u16<kFp16>(acc[i] * g.scale);
+                *split_col(dq, dq_rope, (int64_t)t * g.n1 + n2 * G + gg, d, DQK, g.d_rope) =
+                    f_to_u16<kFp16>(acc[i] * g.scale);
             }
         }
         __syncthreads();
@@ -235,31 +239,34 @@ __global__ void __launch_bounds__(256) k_dq_from_ds(Geometry g, Workspace ws,
 // dK = scale * acc[:, :d_qk], dV = acc[:, d_qk:] after the last chunk.
 template <bool kFp16>
 __global__ void __launch_bounds__(256) k_cast_dkv(Geometry g, const float *__restrict__ acc,
-                                                  uint16_t *__restrict__ dk, uint16_t *__restrict__ dv) {
+                                                  uint16_t *__restrict__ dk, uint16_t *__restrict__ dk_rope,
+                                                  uint16_t *__restrict__ dv) {
     const int w = g.d_qk + g.d_v;
     const int64_t n = (int64_t)g.t2 * g.n2 * w;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t row = i / w;
         const int c = (int)(i % w);
-        if (c < g.d_qk) dk[row * g.d_qk + c] = f_to_u16<kFp16>(acc[i] * g.scale);
+        if (c < g.d_qk) *split_col(dk, dk_rope, row, c, g.d_qk, g.d_rope) = f_to_u16<kFp16>(acc[i] * g.scale);
         else dv[row * g.d_v + c - g.d_qk] = f_to_u16<kFp16>(acc[i]);
     }
 }
 
-cudaError_t launch_cast_dkv(const Geometry &g, const Workspace &ws, void *dk, void *dv, bool fp16,
+cudaError_t launch_cast_dkv(const Geometry &g, const Workspace &ws, void *dk, void *dk_rope, void *dv, bool fp16,
                             cudaStream_t s, int num_sms) {
     const int64_t n = (int64_t)g.t2 * g.n2 * (g.d_qk + g.d_v);
     int64_t grid = (n + 255) / 256;
     if (grid > (int64_t)num_sms * 8) grid = (int64_t)num_sms * 8;
-    if (fp16) k_cast_dkv<true><<<(int)grid, 256, 0, s>>>(g, ws.dkv_acc, (uint16_t *)dk, (uint16_t *)dv);
-    else k_cast_dkv<false><<<(int)grid, 256, 0, s>>>(g, ws.dkv_acc, (uint16_t *)dk, (uint16_t *)dv);
+    if (fp16)
+        k_cast_dkv<true><<<(int)grid, 256, 0, s>>>(g, ws.dkv_acc, (uint16_t *)dk, (uint16_t *)dk_rope, (uint16_t *)dv);
+    else
+        k_cast_dkv<false><<<(int)grid, 256, 0, s>>>(g, ws.dkv_acc, (uint16_t *)dk, (uint16_t *)dk_rope,
+                                                    (uint16_t *)dv);
     return cudaGetLastError();
 }
 
 template <bool kFp16, int DQK, int DV>
-static cudaError_t launch_simt_t(const Geometry &g, const Workspace &ws, const void *q, const void *k,
-                                 const void *v, const void *dy, void *dk, void *dv, bool det,
-                                 cudaStream_t s, int num_sms) {
+static cudaError_t launch_simt_t(const Geometry &g, const Workspace &ws, const sag_io &io, bool det, cudaStream_t s,
+                                 int num_sms) {
     const int threads = (g.block_size / kKeysPerWarp) * 32;
     const size_t smem = sizeof(float) * ((size_t)g.block_size * (DQK + DV) + kRowsPerStep * (DQK + DV) +
                                          2 * kRowsPerStep) + 2 * sizeof(int) * kRowsPerStep;
@@ -268,17 +275,17 @@ static cudaError_t launch_simt_t(const Geometry &g, const Workspace &ws, const v
     if (e != cudaSuccess) return e;
     int64_t grid = g.n_items;
     if (grid > (int64_t)num_sms * 64) grid = (int64_t)num_sms * 64;
-    fn<<<(int)grid, threads, smem, s>>>(g, ws, (const uint16_t *)q, (const uint16_t *)k, (const uint16_t *)v,
-                                        (const uint16_t *)dy, (uint16_t *)dk, (uint16_t *)dv, det ? 1 : 0);
+    fn<<<(int)grid, threads, smem, s>>>(g, ws, (const uint16_t *)io.query, (const uint16_t *)io.key,
+                                        (const uint16_t *)io.value, (const uint16_t *)io.attention_out_grad,
+                                        (uint16_t *)io.dk, (uint16_t *)io.dv, det ? 1 : 0);
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_simt(const Geometry &g, const Workspace &ws, const void *q, const void *k,
-                            const void *v, const void *dy, void *dk, void *dv, bool fp16,
-                            bool deterministic, cudaStream_t s, int num_sms) {
-#define SAG_SIMT_CASE(F, A, B)                                                                    \
-    if (fp16 == F && g.d_qk == A && g.d_v == B)                                                   \
-        return launch_simt_t<F, A, B>(g, ws, q, k, v, dy, dk, dv, deterministic, s, num_sms);
+cudaError_t launch_bwd_simt(const Geometry &g, const Workspace &ws, const sag_io &io, bool fp16, bool deterministic,
+                            cudaStream_t s, int num_sms) {
+    if (g.d_rope) return cudaErrorInvalidValue;   // the rope split runs on the tensor-core kernels only
+#define SAG_SIMT_CASE(F, A, B) \
+    if (fp16 == F && g.d_qk == A && g.d_v == B) return launch_simt_t<F, A, B>(g, ws, io, deterministic, s, num_sms);
     SAG_SIMT_CASE(false, 192, 128) SAG_SIMT_CASE(false, 128, 128) SAG_SIMT_CASE(false, 192, 192)
     SAG_SIMT_CASE(false, 128, 192) SAG_SIMT_CASE(true, 192, 128) SAG_SIMT_CASE(true, 128, 128)
     SAG_SIMT_CASE(true, 192, 192) SAG_SIMT_CASE(true, 128, 192)
@@ -287,8 +294,8 @@ cudaError_t launch_bwd_simt(const Geometry &g, const Workspace &ws, const void *
 }
 
 template <bool kFp16, int DQK>
-static cudaError_t launch_dq_t(const Geometry &g, const Workspace &ws, const void *k, const int32_t *topk,
-                               void *dq, cudaStream_t s, int num_sms) {
+static cudaError_t launch_dq_t(const Geometry &g, const Workspace &ws, const sag_io &io, cudaStream_t s,
+                               int num_sms) {
     const size_t smem = sizeof(float) * ((size_t)g.block_size * DQK + (size_t)g.group * g.block_size);
     auto fn = k_dq_from_ds<kFp16, DQK>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -296,16 +303,15 @@ static cudaError_t launch_dq_t(const Geometry &g, const Workspace &ws, const voi
     int64_t grid = (int64_t)(g.tok_hi - g.tok_lo) * g.n2;
     if (grid > (int64_t)num_sms * 32) grid = (int64_t)num_sms * 32;
     if (grid == 0) return cudaSuccess;
-    fn<<<(int)grid, 256, smem, s>>>(g, ws, (const uint16_t *)k, topk, (uint16_t *)dq);
+    fn<<<(int)grid, 256, smem, s>>>(g, ws, (const uint16_t *)io.key, (const uint16_t *)io.key_rope,
+                                    io.topk_indices, (uint16_t *)io.dq, (uint16_t *)io.dq_rope);
     return cudaGetLastError();
 }
 
-cudaError_t launch_dq_from_ds(const Geometry &g, const Workspace &ws, const void *k, const int32_t *topk,
-                              void *dq, bool fp16, cudaStream_t s, int num_sms) {
-    if (fp16) return g.d_qk == 192 ? launch_dq_t<true, 192>(g, ws, k, topk, dq, s, num_sms)
-                                   : launch_dq_t<true, 128>(g, ws, k, topk, dq, s, num_sms);
-    return g.d_qk == 192 ? launch_dq_t<false, 192>(g, ws, k, topk, dq, s, num_sms)
-                         : launch_dq_t<false, 128>(g, ws, k, topk, dq, s, num_sms);
+cudaError_t launch_dq_from_ds(const Geometry &g, const Workspace &ws, const sag_io &io, bool fp16, cudaStream_t s,
+                              int num_sms) {
+    if (fp16) return g.d_qk == 192 ? launch_dq_t<true, 192>(g, ws, io, s, num_sms) : launch_dq_t<true, 128>(g, ws, io, s, num_sms);
+    return g.d_qk == 192 ? launch_dq_t<false, 192>(g, ws, io, s, num_sms) : launch_dq_t<false, 128>(g, ws, io, s, num_sms);
 }
 
 }  // namespace sag

@@ -64,7 +64,7 @@ enum Bar {
 struct TcArgs {
     Geometry g;
     Workspace ws;
-    uint16_t *dk, *dv;
+    uint16_t *dk, *dv, *dk_rope;
     int nk, halves, tpt, deterministic;
     int64_t n_titems;
 };
@@ -72,7 +72,8 @@ struct TcArgs {
 template <bool kFp16, int DQK>
 __global__ void __launch_bounds__(kThreads, 1)
     k_bwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
-             const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v, TcArgs A) {
+             const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+             const __grid_constant__ CUtensorMap map_qr, const __grid_constant__ CUtensorMap map_kr, TcArgs A) {
     using L = Smem<DQK>;
     constexpr int DV = 128;
     constexpr int KC = L::KC;
@@ -89,6 +90,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nk = A.nk, tpt = A.tpt, G = g.group;
     const bool det = A.deterministic != 0;
     const uint32_t sbase = tc::smem_u32(smem);
+    // 64-column chunk c of a q / k row: the main tensor at column 64 c, or
+    // with the rope split chunk 2 from the rope tensor at column 0
+    const bool rope = g.d_rope != 0;
+    auto qmap = [&](int c) { return (rope && c == 2) ? &map_qr : &map_q; };
+    auto kmap = [&](int c) { return (rope && c == 2) ? &map_kr : &map_k; };
+    auto cx = [&](int c) { return (rope && c == 2) ? 0 : c * 64; };
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -137,6 +144,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::prefetch_tmap(&map_do);
             tc::prefetch_tmap(&map_k);
             tc::prefetch_tmap(&map_v);
+            if (rope) {
+                tc::prefetch_tmap(&map_qr);
+                tc::prefetch_tmap(&map_kr);
+            }
         }
         const int oob_row = g.t1 * g.n1;   // out of range: the TMA fills zeros
         // small groups: one box per token would be a single row, so rows are
@@ -153,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 tc::mbar_arrive_expect_tx(&bars[B_KV_FULL], (uint32_t)nk * (DQK + DV) * 2);
                 for (int c = 0; c < KC; ++c)
-                    tc::tma_load_3d(smem + L::OFF_K + c * 8192, &map_k, c * 64, kt.n2, (int)kt.key0, &bars[B_KV_FULL]);
+                    tc::tma_load_3d(smem + L::OFF_K + c * 8192, kmap(c), cx(c), kt.n2, (int)kt.key0, &bars[B_KV_FULL]);
                 for (int c = 0; c < 2; ++c)
                     tc::tma_load_3d(smem + L::OFF_V + c * 8192, &map_v, c * 64, kt.n2, (int)kt.key0, &bars[B_KV_FULL]);
             }
@@ -181,13 +192,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         y[j] = (m[tk < nt ? tk : 0] / g.block_count) * g.n1 + kt.n2 * G + row % G;
                     }
                     for (int c = 0; c < KC; ++c)
-                        tc::tma_gather4(qdst + c * 16384 + lane * 512, &map_q, c * 64, y[0], y[1], y[2], y[3],
+                        tc::tma_gather4(qdst + c * 16384 + lane * 512, qmap(c), cx(c), y[0], y[1], y[2], y[3],
                                         &bars[B_Q_FULL0 + s]);
                 } else {
                     for (int tt = lane; tt < tpt; tt += 32) {
                         const int y = tt < nt ? (m[tt] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
                         for (int c = 0; c < KC; ++c)
-                            tc::tma_load_2d(qdst + c * 16384 + tt * G * 128, &map_q, c * 64, y, &bars[B_Q_FULL0 + s]);
+                            tc::tma_load_2d(qdst + c * 16384 + tt * G * 128, qmap(c), cx(c), y, &bars[B_Q_FULL0 + s]);
                     }
                 }
                 const int d = tc_i % DOS;
@@ -398,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = et; i < nk * (DQK + DV); i += 128) {
                         const int j = i / (DQK + DV), c = i % (DQK + DV);
                         const int64_t row = (kt.key0 + j) * g.n2 + kt.n2;
-                        if (c < DQK) A.dk[row * DQK + c] = 0;
+                        if (c < DQK) *split_col(A.dk, A.dk_rope, row, c, DQK, g.d_rope) = 0;
                         else A.dv[row * DV + c - DQK] = 0;
                     }
                 }
@@ -465,9 +476,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         acc[DQK + r] += vv;
                         if (DQK == 192 && r >= 64) acc[64 + r] += __uint_as_float(ah[j]);
                     } else {
-                        A.dk[row * DQK + r] = f_to_u16<kFp16>(kv * g.scale);
+                        *split_col(A.dk, A.dk_rope, row, r, DQK, g.d_rope) = f_to_u16<kFp16>(kv * g.scale);
                         A.dv[row * DV + r] = f_to_u16<kFp16>(vv);
-                        if (DQK == 192 && r >= 64) A.dk[row * DQK + 64 + r] = f_to_u16<kFp16>(__uint_as_float(ah[j]) * g.scale);
+                        if (DQK == 192 && r >= 64)
+                            *split_col(A.dk, A.dk_rope, row, 64 + r, DQK, g.d_rope) =
+                                f_to_u16<kFp16>(__uint_as_float(ah[j]) * g.scale);
                     }
                 }
             }
@@ -495,25 +508,27 @@ bool bwd_tc_supported(const Geometry &g) {
 }
 
 template <bool kFp16, int DQK>
-static cudaError_t launch_tc_t(const Geometry &g, const Workspace &ws, const void *q, const void *k, const void *v,
-                               const void *dy, void *dk, void *dv, bool det, cudaStream_t s, int num_sms) {
+static cudaError_t launch_tc_t(const Geometry &g, const Workspace &ws, const sag_io &io, bool det, cudaStream_t s,
+                               int num_sms) {
     const int nk = g.block_size > 64 ? 64 : g.block_size;
     TcArgs a;
     a.g = g;
     a.ws = ws;
-    a.dk = (uint16_t *)dk;
-    a.dv = (uint16_t *)dv;
+    a.dk = (uint16_t *)io.dk;
+    a.dv = (uint16_t *)io.dv;
+    a.dk_rope = (uint16_t *)io.dk_rope;
     a.nk = nk;
     a.halves = g.block_size / nk;
     a.tpt = kRows / g.group;
     a.deterministic = det ? 1 : 0;
     a.n_titems = g.n_units;
-    CUtensorMap mq, mdo, mk, mv;
     // G in {1, 2, 4}: one-row boxes for tile::gather4; otherwise one box per token (G rows)
     const uint32_t box_rows = (g.group <= 4 && 4 % g.group == 0) ? 1 : g.group;
-    if (!tmap_2d(&mq, q, kFp16, DQK, (uint64_t)g.t1 * g.n1, box_rows) ||
-        !tmap_2d(&mdo, dy, kFp16, 128, (uint64_t)g.t1 * g.n1, box_rows) ||
-        !tmap_3d(&mk, k, kFp16, DQK, g.n2, g.t2, nk) || !tmap_3d(&mv, v, kFp16, 128, g.n2, g.t2, nk))
+    QkMaps m;
+    CUtensorMap mdo, mv;
+    if (!qk_maps(&m, g, io, kFp16, box_rows, nk) ||
+        !tmap_2d(&mdo, io.attention_out_grad, kFp16, 128, (uint64_t)g.t1 * g.n1, box_rows) ||
+        !tmap_3d(&mv, io.value, kFp16, 128, g.n2, g.t2, nk))
         return cudaErrorInvalidValue;
     auto fn = k_bwd_tc<kFp16, DQK>;
     const int smem = Smem<DQK>::TOTAL;
@@ -521,19 +536,18 @@ static cudaError_t launch_tc_t(const Geometry &g, const Workspace &ws, const voi
     if (e != cudaSuccess) return e;
     int64_t grid = a.n_titems < num_sms ? a.n_titems : num_sms;
     if (grid < 1) grid = 1;
-    fn<<<(int)grid, kThreads, smem, s>>>(mq, mdo, mk, mv, a);
+    fn<<<(int)grid, kThreads, smem, s>>>(m.q, mdo, m.k, mv, m.qr, m.kr, a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_tc(const Geometry &g, const Workspace &ws, const void *q, const void *k, const void *v,
-                          const void *dy, void *dk, void *dv, bool fp16, bool deterministic, cudaStream_t s,
-                          int num_sms) {
+cudaError_t launch_bwd_tc(const Geometry &g, const Workspace &ws, const sag_io &io, bool fp16, bool deterministic,
+                          cudaStream_t s, int num_sms) {
     if (!bwd_tc_supported(g)) return cudaErrorInvalidValue;
     if (fp16)
-        return g.d_qk == 192 ? launch_tc_t<true, 192>(g, ws, q, k, v, dy, dk, dv, deterministic, s, num_sms)
-                             : launch_tc_t<true, 128>(g, ws, q, k, v, dy, dk, dv, deterministic, s, num_sms);
-    return g.d_qk == 192 ? launch_tc_t<false, 192>(g, ws, q, k, v, dy, dk, dv, deterministic, s, num_sms)
-                         : launch_tc_t<false, 128>(g, ws, q, k, v, dy, dk, dv, deterministic, s, num_sms);
+        return g.d_qk == 192 ? launch_tc_t<true, 192>(g, ws, io, deterministic, s, num_sms)
+                             : launch_tc_t<true, 128>(g, ws, io, deterministic, s, num_sms);
+    return g.d_qk == 192 ? launch_tc_t<false, 192>(g, ws, io, deterministic, s, num_sms)
+                         : launch_tc_t<false, 128>(g, ws, io, deterministic, s, num_sms);
 }
 
 }  // namespace sag

@@ -62,7 +62,7 @@ struct Geometry {
     int32_t windowed;         // 1: units are (batch, KV head, window, key tile)
     int32_t window;           // tokens per window
     int32_t halves;           // key tiles per block (block_size / key tile)
-    int32_t pad_;
+    int32_t d_rope;           // columns [d_qk - d_rope, d_qk) of q / k live in the rope tensors
     int64_t n_units;          // work units of the main kernel
 };
 
@@ -76,8 +76,10 @@ struct WsHeader {
 // Device pointers carved out of the caller's workspace.
 struct Workspace {
     WsHeader *hdr;
-    int32_t *cu_q;            // [B+1]
-    int32_t *cu_kv;           // [B+1]
+    int32_t *cu_q;            // [B+1] first query row of each batch (TND: cu_seqlens_q; BSND: b * s1_max)
+    int32_t *cu_kv;           // [B+1] first key row of each batch (TND: cu_seqlens_kv; BSND: b * s2_max)
+    int32_t *q_end;           // [B]   end of the valid query rows of each batch
+    int32_t *kv_blocks;       // [B]   valid key blocks of each batch (ids must be below)
     int64_t *item_base;       // [B+1] first item id of each batch
     int32_t *count;           // [n_items + 1]  selections naming each item
     int32_t *offset;          // [n_items + 1]  exclusive prefix of count

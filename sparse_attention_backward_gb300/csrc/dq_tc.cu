@@ -39,7 +39,7 @@ struct DqArgs {
     Geometry g;
     Workspace ws;
     const int32_t *topk;
-    uint16_t *dq;
+    uint16_t *dq, *dq_rope;
     int n_pad;          // G rounded up to a multiple of 16
 };
 
@@ -51,7 +51,8 @@ __device__ __forceinline__ bool slot_ok(const Geometry &g, const Workspace &ws, 
 
 template <bool kFp16, int DQK, int BS>
 __global__ void __launch_bounds__(kDqThreads, 1)
-    k_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_ds, DqArgs A) {
+    k_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_ds,
+            const __grid_constant__ CUtensorMap map_kr, DqArgs A) {
     using L = DqSmem<DQK, BS>;
     constexpr int KC = L::KC;
     extern __shared__ uint8_t smem_raw[];
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (lane == 0) {
             tc::prefetch_tmap(&map_k);
             tc::prefetch_tmap(&map_ds);
+            if (g.d_rope) tc::prefetch_tmap(&map_kr);
             int it = 0;
             uint32_t armed[kStages] = {};
             bool ok = true;
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 const int t = g.tok_lo + (int)(cp / g.n2), n2 = (int)(cp % g.n2);
                 const int64_t pair = (int64_t)t * g.n2 + n2;
                 const int b = batch_of(ws.cu_q, g.batch, t);
-                const int nblk = (ws.cu_kv[b + 1] - ws.cu_kv[b]) / g.block_size;
+                const int nblk = t < ws.q_end[b] ? ws.kv_blocks[b] : 0;   // ids must be below; none for padding
                 for (int slot = 0; slot < g.block_count; ++slot) {
                     if (!slot_ok(g, ws, A.topk, pair, slot, nblk)) continue;
                     const int s = it % kStages;
@@ -120,7 +122,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     ++armed[s];
                     tc::mbar_arrive_expect_tx(&bars[D_FULL0 + s], (uint32_t)(BS * DQK * 2 + G * BS * 2));
                     for (int c = 0; c < KC; ++c)
-                        tc::tma_load_3d(st + c * BS * 128, &map_k, c * 64, n2, key0, &bars[D_FULL0 + s]);
+                        tc::tma_load_3d(st + c * BS * 128, (g.d_rope && c == 2) ? &map_kr : &map_k,
+                                        (g.d_rope && c == 2) ? 0 : c * 64, n2, key0, &bars[D_FULL0 + s]);
                     const int dsrow = (int)(((int64_t)cp * g.block_count + slot) * G);
                     for (int c = 0; c < L::DS_CHUNKS; ++c)
                         tc::tma_load_2d(st + L::K_BYTES + c * 4096, &map_ds, c * 64, dsrow, &bars[D_FULL0 + s]);
@@ -143,7 +146,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 const int t = g.tok_lo + (int)(cp / g.n2), n2 = (int)(cp % g.n2);
                 const int64_t pair = (int64_t)t * g.n2 + n2;
                 const int b = batch_of(ws.cu_q, g.batch, t);
-                const int nblk = (ws.cu_kv[b + 1] - ws.cu_kv[b]) / g.block_size;
+                const int nblk = t < ws.q_end[b] ? ws.kv_blocks[b] : 0;   // ids must be below; none for padding
                 const int ab = np & 1;
                 if (np >= 2 && !tc::mbar_wait(&bars[D_ACC_FREE0 + ab], ((np >> 1) - 1) & 1, abort_flag, kDqWaitNs)) {
                     ok = false;
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             const int t = g.tok_lo + (int)(cp / g.n2), n2 = (int)(cp % g.n2);
             const int64_t pair = (int64_t)t * g.n2 + n2;
             const int b = batch_of(ws.cu_q, g.batch, t);
-            const int nblk = (ws.cu_kv[b + 1] - ws.cu_kv[b]) / g.block_size;
+            const int nblk = t < ws.q_end[b] ? ws.kv_blocks[b] : 0;   // ids must be below; none for padding
             int nvalid = 0;
             for (int slot = 0; slot < g.block_count; ++slot) nvalid += slot_ok(g, ws, A.topk, pair, slot, nblk);
             const int ab = np & 1;
@@ -201,7 +204,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             ok = __all_sync(0xffffffffu, w);
             if (!ok) break;
             tc::tc_fence_after();
-            uint16_t *dqrow = A.dq + ((int64_t)t * g.n1 + (int64_t)n2 * G) * DQK;
+            const int64_t row0 = (int64_t)t * g.n1 + (int64_t)n2 * G;   // first dq row of the pair
             for (int g0 = 0; g0 < G; g0 += 16) {
                 uint32_t lo[16], hi[16];
                 tc::tmem_ld16(trow + acc_col(ab, 0) + g0, lo);
@@ -211,10 +214,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 for (int j = 0; j < 16; ++j) {
                     if (g0 + j >= G) break;
                     const float vlo = nvalid ? __uint_as_float(lo[j]) : 0.f;
-                    dqrow[(int64_t)(g0 + j) * DQK + d] = f_to_u16<kFp16>(vlo * g.scale);
+                    *split_col(A.dq, A.dq_rope, row0 + g0 + j, d, DQK, g.d_rope) = f_to_u16<kFp16>(vlo * g.scale);
                     if (DQK == 192 && d >= 64) {
                         const float vhi = nvalid ? __uint_as_float(hi[j]) : 0.f;
-                        dqrow[(int64_t)(g0 + j) * DQK + 64 + d] = f_to_u16<kFp16>(vhi * g.scale);
+                        *split_col(A.dq, A.dq_rope, row0 + g0 + j, 64 + d, DQK, g.d_rope) =
+                            f_to_u16<kFp16>(vhi * g.scale);
                     }
                 }
             }
@@ -233,26 +237,33 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 }
 
 template <bool kFp16, int DQK, int BS>
-static cudaError_t launch_dq_tc_t(const Geometry &g, const Workspace &ws, const void *k, const int32_t *topk,
-                                  void *dq, cudaStream_t s, int num_sms) {
+static cudaError_t launch_dq_tc_t(const Geometry &g, const Workspace &ws, const sag_io &io, cudaStream_t s,
+                                  int num_sms) {
     const int64_t npairs = (int64_t)(g.tok_hi - g.tok_lo) * g.n2;
     if (npairs == 0) return cudaSuccess;
     DqArgs a;
     a.g = g;
     a.ws = ws;
-    a.topk = topk;
-    a.dq = (uint16_t *)dq;
+    a.topk = io.topk_indices;
+    a.dq = (uint16_t *)io.dq;
+    a.dq_rope = (uint16_t *)io.dq_rope;
     a.n_pad = (g.group + 15) / 16 * 16;
-    CUtensorMap mk, mds;
+    CUtensorMap mk, mkr, mds;
     const uint64_t ds_rows = (uint64_t)npairs * g.block_count * g.group;
-    if (!tmap_3d(&mk, k, kFp16, DQK, g.n2, g.t2, BS) || !tmap_2d(&mds, ws.ds, kFp16, BS, ds_rows, g.group))
+    const uint64_t d_main = (uint64_t)(g.d_qk - g.d_rope);
+    if (!tmap_3d(&mk, io.key, kFp16, d_main, g.n2, g.t2, BS) || !tmap_2d(&mds, ws.ds, kFp16, BS, ds_rows, g.group))
         return cudaErrorInvalidValue;
+    if (g.d_rope) {
+        if (!tmap_3d(&mkr, io.key_rope, kFp16, g.d_rope, g.n2, g.t2, BS)) return cudaErrorInvalidValue;
+    } else {
+        mkr = mk;
+    }
     auto fn = k_dq_tc<kFp16, DQK, BS>;
     const int smem = DqSmem<DQK, BS>::TOTAL;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = npairs < num_sms ? npairs : num_sms;
-    fn<<<(int)grid, kDqThreads, smem, s>>>(mk, mds, a);
+    fn<<<(int)grid, kDqThreads, smem, s>>>(mk, mds, mkr, a);
     return cudaGetLastError();
 }
 
@@ -262,10 +273,10 @@ bool dq_tc_supported(const Geometry &g) {
     return (g.d_qk == 128 || g.d_qk == 192) && (g.block_size == 64 || g.block_size == 128) && g.group <= 32;
 }
 
-cudaError_t launch_dq_tc(const Geometry &g, const Workspace &ws, const void *k, const int32_t *topk, void *dq,
-                         bool fp16, cudaStream_t s, int num_sms) {
-#define SAG_DQ_CASE(F, D, B)                                                                 \
-    if (fp16 == F && g.d_qk == D && g.block_size == B) return launch_dq_tc_t<F, D, B>(g, ws, k, topk, dq, s, num_sms);
+cudaError_t launch_dq_tc(const Geometry &g, const Workspace &ws, const sag_io &io, bool fp16, cudaStream_t s,
+                         int num_sms) {
+#define SAG_DQ_CASE(F, D, B) \
+    if (fp16 == F && g.d_qk == D && g.block_size == B) return launch_dq_tc_t<F, D, B>(g, ws, io, s, num_sms);
     SAG_DQ_CASE(false, 192, 64) SAG_DQ_CASE(false, 192, 128) SAG_DQ_CASE(false, 128, 64)
     SAG_DQ_CASE(false, 128, 128) SAG_DQ_CASE(true, 192, 64) SAG_DQ_CASE(true, 192, 128)
     SAG_DQ_CASE(true, 128, 64) SAG_DQ_CASE(true, 128, 128)

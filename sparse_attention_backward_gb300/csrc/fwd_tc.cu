@@ -67,7 +67,8 @@ __device__ __forceinline__ void atomic_max_f32(float *addr, float v) {
 template <bool kFp16, int DQK, int PASS>
 __global__ void __launch_bounds__(kThreads, 1)
     k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-             const __grid_constant__ CUtensorMap map_v, FwdArgs A) {
+             const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_qr,
+             const __grid_constant__ CUtensorMap map_kr, FwdArgs A) {
     using L = FwdSmem<DQK>;
     constexpr int DV = 128;
     constexpr int KC = L::KC;
@@ -85,6 +86,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = A.nk, tpt = A.tpt, G = g.group;
     const uint32_t sbase = tc::smem_u32(smem);
+    // 64-column chunk c of a q / k row: the main tensor at column 64 c, or
+    // with the rope split chunk 2 from the rope tensor at column 0
+    const bool rope = g.d_rope != 0;
+    auto qmap = [&](int c) { return (rope && c == 2) ? &map_qr : &map_q; };
+    auto kmap = [&](int c) { return (rope && c == 2) ? &map_kr : &map_k; };
+    auto cx = [&](int c) { return (rope && c == 2) ? 0 : c * 64; };
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -127,6 +134,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tc::prefetch_tmap(&map_q);
             tc::prefetch_tmap(&map_k);
+            if (rope) {
+                tc::prefetch_tmap(&map_qr);
+                tc::prefetch_tmap(&map_kr);
+            }
             if (PASS == 2) tc::prefetch_tmap(&map_v);
         }
         const int oob_row = g.t1 * g.n1;   // out of range: the TMA fills zeros
@@ -142,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 tc::mbar_arrive_expect_tx(&bars[F_KV_FULL], (uint32_t)nk * (DQK + (PASS == 2 ? DV : 0)) * 2);
                 for (int c = 0; c < KC; ++c)
-                    tc::tma_load_3d(smem + L::OFF_K + c * 8192, &map_k, c * 64, kt.n2, (int)kt.key0, &bars[F_KV_FULL]);
+                    tc::tma_load_3d(smem + L::OFF_K + c * 8192, kmap(c), cx(c), kt.n2, (int)kt.key0, &bars[F_KV_FULL]);
                 if (PASS == 2)
                     for (int c = 0; c < 2; ++c)
                         tc::tma_load_3d(smem + L::OFF_V + c * 8192, &map_v, c * 64, kt.n2, (int)kt.key0,
@@ -172,13 +183,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         y[j] = (m[tk < nt ? tk : 0] / g.block_count) * g.n1 + kt.n2 * G + row % G;
                     }
                     for (int c = 0; c < KC; ++c)
-                        tc::tma_gather4(qdst + c * 16384 + lane * 512, &map_q, c * 64, y[0], y[1], y[2], y[3],
+                        tc::tma_gather4(qdst + c * 16384 + lane * 512, qmap(c), cx(c), y[0], y[1], y[2], y[3],
                                         &bars[F_Q_FULL + s]);
                 } else {
                     for (int tt = lane; tt < tpt; tt += 32) {
                         const int y = tt < nt ? (m[tt] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
                         for (int c = 0; c < KC; ++c)
-                            tc::tma_load_2d(qdst + c * 16384 + tt * G * 128, &map_q, c * 64, y, &bars[F_Q_FULL + s]);
+                            tc::tma_load_2d(qdst + c * 16384 + tt * G * 128, qmap(c), cx(c), y, &bars[F_Q_FULL + s]);
                     }
                 }
             }
@@ -393,26 +404,27 @@ __global__ void k_fwd_finalize(const float *__restrict__ mrow, const float *__re
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += nw) {
-        const float l = lrow[r], inv = 1.f / l;
+        // every valid row has l >= 1 (its maximum term is exp(0)); l == 0 marks a
+        // row that selected nothing (BSND padding): zeros in all outputs
+        const float l = lrow[r], inv = l > 0.f ? 1.f / l : 0.f;
         const float4 a = oacc[r * 32 + lane];
         o[r * 32 + lane] = make_uint2(pack2<kFp16>(a.x * inv, a.y * inv), pack2<kFp16>(a.z * inv, a.w * inv));
-        if (lane < 8) smax[r * 8 + lane] = mrow[r];
+        if (lane < 8) smax[r * 8 + lane] = l > 0.f ? mrow[r] : 0.f;
         else if (lane < 16) ssum[r * 8 + lane - 8] = l;
     }
 }
 
 template <bool kFp16, int DQK, int PASS>
-cudaError_t launch_fwd_t(const Geometry &g, const Workspace &ws, const void *q, const void *k, const void *v,
-                         cudaStream_t s, int num_sms) {
+cudaError_t launch_fwd_t(const Geometry &g, const Workspace &ws, const sag_io &io, cudaStream_t s, int num_sms) {
     FwdArgs a;
     a.g = g;
     a.ws = ws;
     a.nk = g.block_size > 64 ? 64 : g.block_size;
     a.tpt = kRows / g.group;
-    CUtensorMap mq, mk, mv;
+    QkMaps m;
+    CUtensorMap mv;
     const uint32_t box_rows = (g.group <= 4 && 4 % g.group == 0) ? 1 : g.group;
-    if (!tmap_2d(&mq, q, kFp16, DQK, (uint64_t)g.t1 * g.n1, box_rows) ||
-        !tmap_3d(&mk, k, kFp16, DQK, g.n2, g.t2, a.nk) || !tmap_3d(&mv, v, kFp16, 128, g.n2, g.t2, a.nk))
+    if (!qk_maps(&m, g, io, kFp16, box_rows, a.nk) || !tmap_3d(&mv, io.value, kFp16, 128, g.n2, g.t2, a.nk))
         return cudaErrorInvalidValue;
     auto fn = k_fwd_tc<kFp16, DQK, PASS>;
     const int smem = FwdSmem<DQK>::TOTAL;
@@ -420,15 +432,14 @@ cudaError_t launch_fwd_t(const Geometry &g, const Workspace &ws, const void *q, 
     if (e != cudaSuccess) return e;
     int64_t grid = g.n_units < num_sms ? g.n_units : num_sms;
     if (grid < 1) grid = 1;
-    fn<<<(int)grid, kThreads, smem, s>>>(mq, mk, mv, a);
+    fn<<<(int)grid, kThreads, smem, s>>>(m.q, m.k, mv, m.qr, m.kr, a);
     return cudaGetLastError();
 }
 
 template <bool kFp16, int PASS>
-cudaError_t launch_fwd_d(const Geometry &g, const Workspace &ws, const void *q, const void *k, const void *v,
-                         cudaStream_t s, int num_sms) {
-    return g.d_qk == 192 ? launch_fwd_t<kFp16, 192, PASS>(g, ws, q, k, v, s, num_sms)
-                         : launch_fwd_t<kFp16, 128, PASS>(g, ws, q, k, v, s, num_sms);
+cudaError_t launch_fwd_d(const Geometry &g, const Workspace &ws, const sag_io &io, cudaStream_t s, int num_sms) {
+    return g.d_qk == 192 ? launch_fwd_t<kFp16, 192, PASS>(g, ws, io, s, num_sms)
+                         : launch_fwd_t<kFp16, 128, PASS>(g, ws, io, s, num_sms);
 }
 
 }  // namespace
@@ -444,14 +455,11 @@ cudaError_t launch_fwd_init(const Geometry &g, const Workspace &ws, cudaStream_t
     return cudaGetLastError();
 }
 
-cudaError_t launch_fwd_tc(const Geometry &g, const Workspace &ws, const void *q, const void *k, const void *v,
-                          int pass, bool fp16, cudaStream_t s, int num_sms) {
+cudaError_t launch_fwd_tc(const Geometry &g, const Workspace &ws, const sag_io &io, int pass, bool fp16,
+                          cudaStream_t s, int num_sms) {
     if (!fwd_tc_supported(g) || (pass != 1 && pass != 2)) return cudaErrorInvalidValue;
-    if (fp16)
-        return pass == 1 ? launch_fwd_d<true, 1>(g, ws, q, k, v, s, num_sms)
-                         : launch_fwd_d<true, 2>(g, ws, q, k, v, s, num_sms);
-    return pass == 1 ? launch_fwd_d<false, 1>(g, ws, q, k, v, s, num_sms)
-                     : launch_fwd_d<false, 2>(g, ws, q, k, v, s, num_sms);
+    if (fp16) return pass == 1 ? launch_fwd_d<true, 1>(g, ws, io, s, num_sms) : launch_fwd_d<true, 2>(g, ws, io, s, num_sms);
+    return pass == 1 ? launch_fwd_d<false, 1>(g, ws, io, s, num_sms) : launch_fwd_d<false, 2>(g, ws, io, s, num_sms);
 }
 
 cudaError_t launch_fwd_finalize(const Geometry &g, const Workspace &ws, void *o, float *smax, float *ssum, bool fp16,

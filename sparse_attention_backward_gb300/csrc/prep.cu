@@ -61,14 +61,14 @@ __global__ void __launch_bounds__(256) k_preprocess(Geometry g, const uint16_t *
 }
 
 // ---------------------------------------------------------------------------
-// Item of a selection, or -1 (and the error flag) when the block id is out of
-// its batch's range.
-__device__ __forceinline__ int64_t item_of(const Geometry &g, const Workspace &ws, int t, int n2,
-                                           int id, int *b_out) {
+// Item of a selection: -1 (reported) when the block id is outside its
+// batch's valid blocks, -2 for a padding token (BSND rows past the batch's
+// valid length, whose lists are ignored).
+__device__ __forceinline__ int64_t item_of(const Geometry &g, const Workspace &ws, int t, int n2, int id) {
     const int b = batch_of(ws.cu_q, g.batch, t);
-    const int nblk = (ws.cu_kv[b + 1] - ws.cu_kv[b]) / g.block_size;
-    *b_out = b;
-    if (id < 0 || id >= nblk) return -1;
+    if (t >= ws.q_end[b]) return -2;
+    if (id < 0 || id >= ws.kv_blocks[b]) return -1;
+    const int nblk = (ws.cu_kv[b + 1] - ws.cu_kv[b]) / g.block_size;   // blocks of the (padded) key rows
     return ws.item_base[b] + (int64_t)n2 * nblk + id;
 }
 
@@ -79,9 +79,9 @@ __global__ void __launch_bounds__(256) k_histogram(Geometry g, Workspace ws,
          i += (int64_t)gridDim.x * blockDim.x) {
         const int t = (int)(i / ((int64_t)g.n2 * g.block_count));
         const int n2 = (int)((i / g.block_count) % g.n2);
-        int b;
-        const int64_t item = item_of(g, ws, t, n2, __ldg(topk + i), &b);
-        if (item < 0) { raise_error(&ws.hdr->error, SAG_ERR_INDEX); continue; }
+        const int64_t item = item_of(g, ws, t, n2, __ldg(topk + i));
+        if (item == -1) raise_error(&ws.hdr->error, SAG_ERR_INDEX);
+        if (item < 0) continue;
         atomicAdd(ws.count + item, 1);
     }
 }
@@ -190,8 +190,7 @@ __global__ void __launch_bounds__(256) k_fill(Geometry g, Workspace ws,
         const int t = (int)(i / ((int64_t)g.n2 * g.block_count));
         const int n2 = (int)((i / g.block_count) % g.n2);
         const int slot = (int)(i % g.block_count);
-        int b;
-        const int64_t item = item_of(g, ws, t, n2, __ldg(topk + i), &b);
+        const int64_t item = item_of(g, ws, t, n2, __ldg(topk + i));
         if (item < 0) continue;
         const int pos = ws.offset[item] + atomicAdd(ws.cursor + item, 1);
         ws.entries[pos] = t * g.block_count + slot;
@@ -330,19 +329,23 @@ __global__ void __launch_bounds__(512) k_sort_buckets(Geometry g, Workspace ws) 
     }
 }
 
-// fp32 -> 16-bit, scaled (used for dQ in default mode).
+// dQ = scale * the fp32 accumulator, rounded to 16 bits; with the rope split
+// the columns from d_qk - d_rope on go to dq_rope (a group of 4 never straddles
+// the boundary: both widths are multiples of 4).
 template <bool kFp16>
-__global__ void __launch_bounds__(256) k_cast(const float *__restrict__ in, uint16_t *__restrict__ out,
-                                              int64_t n4, float mul) {
+__global__ void __launch_bounds__(256) k_cast_dq(Geometry g, const float *__restrict__ in, uint16_t *__restrict__ out,
+                                                 uint16_t *__restrict__ out_rope, int64_t n4) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
          i += (int64_t)gridDim.x * blockDim.x) {
         const float4 v = reinterpret_cast<const float4 *>(in)[i];
         ushort4 o;
-        o.x = f_to_u16<kFp16>(v.x * mul);
-        o.y = f_to_u16<kFp16>(v.y * mul);
-        o.z = f_to_u16<kFp16>(v.z * mul);
-        o.w = f_to_u16<kFp16>(v.w * mul);
-        reinterpret_cast<ushort4 *>(out)[i] = o;
+        o.x = f_to_u16<kFp16>(v.x * g.scale);
+        o.y = f_to_u16<kFp16>(v.y * g.scale);
+        o.z = f_to_u16<kFp16>(v.z * g.scale);
+        o.w = f_to_u16<kFp16>(v.w * g.scale);
+        const int64_t row = (i * 4) / g.d_qk;
+        const int col = (int)((i * 4) % g.d_qk);
+        *reinterpret_cast<ushort4 *>(split_col(out, out_rope, row, col, g.d_qk, g.d_rope)) = o;
     }
 }
 
@@ -392,13 +395,13 @@ cudaError_t launch_inversion(const Geometry &g, const Workspace &ws, const int32
     return cudaGetLastError();
 }
 
-cudaError_t launch_cast(const float *in, void *out, int64_t n, float mul, bool fp16, cudaStream_t s,
-                        int num_sms) {
-    const int64_t n4 = n / 4;
+cudaError_t launch_cast_dq(const Geometry &g, const float *dq_acc, void *dq, void *dq_rope, bool fp16,
+                           cudaStream_t s, int num_sms) {
+    const int64_t n4 = (int64_t)g.t1 * g.n1 * g.d_qk / 4;
     if (n4 == 0) return cudaSuccess;
     const int grid = grid_for(n4, 256, num_sms * 8);
-    if (fp16) k_cast<true><<<grid, 256, 0, s>>>(in, (uint16_t *)out, n4, mul);
-    else k_cast<false><<<grid, 256, 0, s>>>(in, (uint16_t *)out, n4, mul);
+    if (fp16) k_cast_dq<true><<<grid, 256, 0, s>>>(g, dq_acc, (uint16_t *)dq, (uint16_t *)dq_rope, n4);
+    else k_cast_dq<false><<<grid, 256, 0, s>>>(g, dq_acc, (uint16_t *)dq, (uint16_t *)dq_rope, n4);
     return cudaGetLastError();
 }
 

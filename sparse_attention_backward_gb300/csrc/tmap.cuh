@@ -7,6 +7,8 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
+#include "common.cuh"
+
 namespace sag {
 
 // Looked up once per process (thread-safe static initialisation); nullptr if
@@ -54,6 +56,29 @@ inline bool tmap_3d(CUtensorMap *m, const void *base, bool fp16, uint64_t d0, ui
                const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Maps of the query and key tensors of a launch: q as [T1 * n1, d] rows with
+// boxes {64, q_box_rows}, k as [T2, n2, d] with boxes {64, 1, k_box}.  With
+// the rope split (g.d_rope = 64) q and k hold d_qk - 64 = 128 columns and the
+// rope tensors get maps of their own (qr, kr: 64 columns); otherwise qr / kr
+// repeat q / k and are never used.
+struct QkMaps {
+    CUtensorMap q, qr, k, kr;
+};
+inline bool qk_maps(QkMaps *m, const Geometry &g, const sag_io &io, bool fp16, uint32_t q_box_rows,
+                    uint32_t k_box) {
+    const uint64_t dq = (uint64_t)(g.d_qk - g.d_rope);
+    if (!tmap_2d(&m->q, io.query, fp16, dq, (uint64_t)g.t1 * g.n1, q_box_rows) ||
+        !tmap_3d(&m->k, io.key, fp16, dq, g.n2, g.t2, k_box))
+        return false;
+    if (!g.d_rope) {
+        m->qr = m->q;
+        m->kr = m->k;
+        return true;
+    }
+    return tmap_2d(&m->qr, io.query_rope, fp16, g.d_rope, (uint64_t)g.t1 * g.n1, q_box_rows) &&
+           tmap_3d(&m->kr, io.key_rope, fp16, g.d_rope, g.n2, g.t2, k_box);
 }
 
 }  // namespace sag

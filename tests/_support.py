@@ -86,12 +86,33 @@ def par_dkdv_block(p: oracle.Problem, b: int, n2: int, kb: int, n=None):
     return sum(a for a, _ in parts), sum(c for _, c in parts)
 
 
+def oracle_full_forward(w: synth.Workload, x: dict):
+    """Oracle forward of every row: O [T1, n1, d_v], max and sum [T1, n1]."""
+    p = problem(w, x, with_backward=False)
+    o, m, l = par_forward_rows(p, np.arange(w.t1 * w.n1))
+    return o.reshape(w.t1, w.n1, w.d_v), m.reshape(w.t1, w.n1), l.reshape(w.t1, w.n1)
+
+
+def oracle_full_backward(w: synth.Workload, x: dict):
+    """Oracle dq, dk, dv of the whole problem (rows and key blocks fanned out)."""
+    p = problem(w, x)
+    dq = par_dq_rows(p, np.arange(w.t1 * w.n1)).reshape(w.t1, w.n1, w.d_qk)
+    blocks = [(b, j, kb) for b in range(w.batch) for j in range(w.n2)
+              for kb in range((w.cu_kv[b + 1] - w.cu_kv[b]) // w.block_size)]
+    dk = np.zeros((w.t2, w.n2, w.d_qk))
+    dv = np.zeros((w.t2, w.n2, w.d_v))
+    for (b, j, kb), (bk, bv) in zip(blocks, par_dkdv_blocks(p, blocks)):
+        r0 = w.cu_kv[b] + kb * w.block_size
+        dk[r0:r0 + w.block_size, j] = bk
+        dv[r0:r0 + w.block_size, j] = bv
+    return dq, dk, dv
+
+
 # ------------------------------------------------------------------ inputs
 def forward_inputs(w: synth.Workload, x: dict) -> dict:
     """attentionOut and [T1,N1,8] stats from the oracle forward (host)."""
     p = problem(w, x, with_backward=False)
-    rows = np.arange(w.t1 * w.n1)
-    o, m, l = par_forward_rows(p, rows) if rows.size > 4096 else oracle.forward_rows(p, rows)
+    o, m, l = par_forward_rows(p, np.arange(w.t1 * w.n1))
     x = dict(x)
     x["o"] = torch.from_numpy(o.reshape(w.t1, w.n1, w.d_v)).to(w.torch_dtype)
     x["softmax_max"] = torch.from_numpy(m).float().view(w.t1, w.n1, 1).expand(-1, -1, 8).contiguous()

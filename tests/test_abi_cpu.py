@@ -198,3 +198,24 @@ def test_selections_beyond_the_32_bit_index_are_unsupported(lib):
     assert _status(_desc(**dict(big, n1=8, n2=8)))[0] == sab.SAG_ERR_UNSUPPORTED
     # a quarter: 2^30 selections fit
     assert _status(_desc(**dict(big, n1=4, n2=4)))[0] == sab.SAG_OK
+
+
+def test_bsnd_and_rope_descriptors(lib):
+    """Layout and rope fields of the descriptor: BSND takes padded lengths that
+    bound every batch's valid length; TND takes none; the rope part is 64 wide
+    on a 128-wide query / key (192 in all) with d_v = 128."""
+    bsnd = dict(cu_seqlens_q=[0, 100, 150], cu_seqlens_kv=[0, 256, 384], layout=sab.SAG_LAYOUT_BSND,
+                s1_max=128, s2_max=256)
+    assert _status(_desc(**bsnd))[0] == sab.SAG_OK
+    assert _status(_desc(**dict(bsnd, s1_max=99)))[0] == G          # a batch longer than its padding
+    assert _status(_desc(**dict(bsnd, s2_max=250)))[0] == G         # not a multiple of the block size
+    assert _status(_desc(**dict(bsnd, s1_max=0)))[0] == G
+    assert _status(_desc(s1_max=128))[0] == G                        # TND takes no padded lengths
+    assert _status(_desc(layout=2))[0] == G
+    rope = dict(d_qk=128, d_v=128, d_rope=64)
+    assert _status(_desc(**rope))[0] == sab.SAG_OK
+    assert _status(_desc(**dict(rope, d_rope=32)))[0] == G
+    assert _status(_desc(**dict(rope, d_v=192)))[0] == sab.SAG_ERR_UNSUPPORTED
+    assert _status(_desc(**dict(rope, d_qk=192)))[0] == G            # 256 in all
+    # the rope split: same workspace as the unsplit 192-wide problem
+    assert _status(_desc(**rope))[1] == _status(_desc(d_qk=192, d_v=128))[1]

@@ -8,7 +8,6 @@ relative Frobenius error <= 5e-3 and max abs error <= 2e-2 * max|ref|.
 import pytest
 import torch
 
-import oracle
 import sparse_attention_backward_gb300 as sab
 import synth
 from tests import _support as S
@@ -40,8 +39,7 @@ def _check_forward(o, smax, ssum, ref_o, ref_m, ref_l, shape):
 def test_forward_parity_small(name):
     w = SMALL[name]
     x = synth.make_inputs(w, device="cpu")
-    p = S.problem(w, x, with_backward=False)
-    ref_o, ref_m, ref_l = oracle.forward(p)
+    ref_o, ref_m, ref_l = S.oracle_full_forward(w, x)
     o, smax, ssum = _gpu_forward(w, x)
     _check_forward(o, smax, ssum, ref_o, ref_m, ref_l, (w.t1, w.n1, w.d_v))
 
@@ -64,7 +62,7 @@ def test_forward_then_backward():
     t = {k: v.cuda() for k, v in x.items()}
     dq, dk, dv = sab.backward(t["q"], t["k"], t["v"], t["o"], t["dy"], t["softmax_max"], t["softmax_sum"],
                               t["topk"], w.cu_q, w.cu_kv, w.scale, w.block_size, w.block_count, check=True)
-    ref = oracle.backward(S.problem(w, x))
+    ref = S.oracle_full_backward(w, x)
     for nm, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
         S.assert_close(nm, S.f64(got), r)
 
@@ -87,6 +85,6 @@ def test_forward_token_windows_parity(name, window, monkeypatch):
     monkeypatch.setenv("SELATTN_FWD_WINDOW_TOKENS", str(window))
     w = SMALL[name]
     x = synth.make_inputs(w, device="cpu")
-    ref_o, ref_m, ref_l = oracle.forward(S.problem(w, x, with_backward=False))
+    ref_o, ref_m, ref_l = S.oracle_full_forward(w, x)
     o, smax, ssum = _gpu_forward(w, x)
     _check_forward(o, smax, ssum, ref_o, ref_m, ref_l, (w.t1, w.n1, w.d_v))

@@ -262,3 +262,62 @@ def test_every_16bit_pattern_decodes_exactly(kind):
     assert np.array_equal(np.isnan(got), nan)
     np.testing.assert_array_equal(got[~nan], want[~nan])
     assert np.all(m == 0.0) and np.all(l == 1.0)
+
+
+def _to_bsnd(p, s1_max, s2_max, rng):
+    """The same problem in the padded BSND layout; every padding row holds
+    junk (random values, and block ids far out of range) that must not reach
+    the result."""
+    B = p.batch
+    lq, lk = np.diff(p.cu_q), np.diff(p.cu_kv)
+
+    def pad(x, lens, cu, smax, fill):
+        out = fill((B * smax,) + x.shape[1:])
+        for b in range(B):
+            out[b * smax:b * smax + lens[b]] = x[cu[b]:cu[b + 1]]
+        return out
+
+    junk = lambda shape: rng.standard_normal(shape) * 7.0
+    bad_ids = lambda shape: np.full(shape, 10 ** 6, np.int32)
+    return oracle.Problem(
+        cu_q=p.cu_q, cu_kv=p.cu_kv, n1=p.n1, n2=p.n2, d_qk=p.d_qk, d_v=p.d_v, block_size=p.block_size,
+        block_count=p.block_count, scale=p.scale, topk=pad(p.topk, lq, p.cu_q, s1_max, bad_ids),
+        q=pad(p.q, lq, p.cu_q, s1_max, junk), k=pad(p.k, lk, p.cu_kv, s2_max, junk),
+        v=pad(p.v, lk, p.cu_kv, s2_max, junk), dy=pad(p.dy, lq, p.cu_q, s1_max, junk),
+        o=pad(p.o, lq, p.cu_q, s1_max, junk), smax=pad(p.smax, lq, p.cu_q, s1_max, junk),
+        ssum=pad(p.ssum, lq, p.cu_q, s1_max, junk), stat_stride=p.stat_stride, layout=1, s1_max=s1_max,
+        s2_max=s2_max)
+
+
+def test_bsnd_layout_is_the_packed_problem_with_padding_ignored():
+    """BSND (every batch padded to s1_max / s2_max rows) against the same
+    data packed in TND: equal forward and gradients on the valid rows, zero
+    gradients on padding rows, and padding rows never read (their block ids
+    are out of range and would fail the call)."""
+    rng = np.random.default_rng(31)
+    p = _with_forward(_rand_problem(rng, lens_q=(5, 0, 7), lens_kv=(32, 16, 24)))
+    pb = _to_bsnd(p, s1_max=9, s2_max=40, rng=rng)
+    o, m, l = oracle.forward(p)
+    ob, mb, lb = oracle.forward(pb)
+    dq, dk, dv = oracle.backward(p)
+    dqb, dkb, dvb = oracle.backward(pb)
+    for b in range(p.batch):
+        q0, q1 = p.cu_q[b], p.cu_q[b + 1]
+        k0, k1 = p.cu_kv[b], p.cu_kv[b + 1]
+        r = slice(b * 9, b * 9 + q1 - q0)
+        kr = slice(b * 40, b * 40 + k1 - k0)
+        np.testing.assert_array_equal(ob[r], o[q0:q1])
+        np.testing.assert_array_equal(mb[r], m[q0:q1])
+        np.testing.assert_array_equal(lb[r], l[q0:q1])
+        np.testing.assert_array_equal(dqb[r], dq[q0:q1])
+        np.testing.assert_array_equal(dkb[kr], dk[k0:k1])
+        np.testing.assert_array_equal(dvb[kr], dv[k0:k1])
+        assert not dqb[b * 9 + q1 - q0:(b + 1) * 9].any()
+        assert not dkb[b * 40 + k1 - k0:(b + 1) * 40].any() and not dvb[b * 40 + k1 - k0:(b + 1) * 40].any()
+    # row-wise entry points address padded rows too
+    tok_bsnd = np.array([9 * 2 + 3, 0, 4])             # batch 2 token 3, batch 0 tokens 0 and 4
+    tok_tnd = np.array([p.cu_q[2] + 3, 0, 4])
+    np.testing.assert_array_equal(oracle.dq_rows(pb, tok_bsnd * p.n1 + 1), oracle.dq_rows(p, tok_tnd * p.n1 + 1))
+    np.testing.assert_array_equal(oracle.dkdv_block(pb, 2, 1, 2)[0], oracle.dkdv_block(p, 2, 1, 2)[0])
+    with pytest.raises(RuntimeError):
+        oracle.dq_rows(pb, np.array([9 * 0 + 6]) * p.n1)   # a padding row of batch 0 is not a query

@@ -10,7 +10,6 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 import sparse_attention_backward_gb300 as sab
 import synth
 from tests import _support as S
@@ -26,20 +25,7 @@ def _run(w, x, deterministic):
 
 
 def _oracle_full(w, x):
-    p = S.problem(w, x)
-    rows = np.arange(w.t1 * w.n1)
-    big = w.t1 * w.n1 * w.selected_keys > 2_000_000
-    dq = (S.par_dq_rows(p, rows) if big else oracle.dq_rows(p, rows)).reshape(w.t1, w.n1, w.d_qk)
-    blocks = [(b, j, kb) for b in range(w.batch) for j in range(w.n2)
-              for kb in range((w.cu_kv[b + 1] - w.cu_kv[b]) // w.block_size)]
-    res = S.par_dkdv_blocks(p, blocks) if big else [oracle.dkdv_block(p, *a) for a in blocks]
-    dk = np.zeros((w.t2, w.n2, w.d_qk))
-    dv = np.zeros((w.t2, w.n2, w.d_v))
-    for (b, j, kb), (bk, bv) in zip(blocks, res):
-        r0 = w.cu_kv[b] + kb * w.block_size
-        dk[r0:r0 + w.block_size, j] = bk
-        dv[r0:r0 + w.block_size, j] = bv
-    return dq, dk, dv
+    return S.oracle_full_backward(w, x)
 
 
 def _small_cases():
@@ -197,4 +183,29 @@ def test_deterministic_token_chunks(small_data, name, chunk, monkeypatch):
     S.assert_close(f"{name} chunks dv", S.f64(a[2]), rdv)
     b = _run(w, x, True)
     for u, v in zip(a, b):
+        assert torch.equal(u.view(torch.int16), v.view(torch.int16))
+
+
+def test_bucket_beyond_the_shared_memory_sort():
+    """Every one of 40000 query tokens selects block 0 (as NSA's always-kept
+    first block would be): a bucket of 40000 entries, sorted in place through
+    global memory.  Both modes against the oracle; the deterministic mode
+    bit-identical over two calls."""
+    w = SMALL["tiny"].with_(name="hot_block", cu_q=(0, 40000), cu_kv=(0, 512), n1=2, n2=1, d_qk=128, d_v=128,
+                            block_size=16, block_count=2, scale=128 ** -0.5, seed=16)
+    x = synth.make_inputs(w)
+    g = torch.Generator().manual_seed(17)
+    other = torch.randint(1, 32, (w.t1, 1), generator=g, dtype=torch.int32)
+    x["topk"] = torch.cat([torch.zeros_like(other), other], dim=1).view(w.t1, 1, 2).contiguous()
+    x = S.forward_inputs(w, x)
+    rdq, rdk, rdv = _oracle_full(w, x)
+    outs = {}
+    for det in (False, True):
+        dq, dk, dv = _run(w, x, det)
+        S.assert_close(f"hot block det={det} dq", S.f64(dq), rdq)
+        S.assert_close(f"hot block det={det} dk", S.f64(dk), rdk)
+        S.assert_close(f"hot block det={det} dv", S.f64(dv), rdv)
+        outs[det] = (dq, dk, dv)
+    again = _run(w, x, True)
+    for u, v in zip(outs[True], again):
         assert torch.equal(u.view(torch.int16), v.view(torch.int16))
