@@ -232,6 +232,10 @@ sag_status sel_attn_grad_ex(const sag_desc *desc, const sag_io *io, void *worksp
  *                     two schedules: the softmax between the MMA groups, or, for
  *                     query groups G = n1 / n2 of 1, 2 or 4, split in two phases
  *                     beside them)
+ *   dq_path           0: dQ reduced with fp32 atomics inside the main kernel;
+ *                     1: dS stored and dQ formed by a fixed-order pass (always
+ *                     in deterministic mode; in default mode when it moves
+ *                     fewer bytes by the library's count)
  */
 typedef struct sag_plan_info {
     uint64_t workspace_bytes;
@@ -239,7 +243,7 @@ typedef struct sag_plan_info {
     int32_t token_chunks;
     int64_t items;
     int32_t main_kernel;
-    int32_t reserved_;
+    int32_t dq_path;
 } sag_plan_info;
 
 sag_status sel_attn_grad_plan_info(const sag_desc *desc, sag_plan_info *info);

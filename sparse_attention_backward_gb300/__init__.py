@@ -59,7 +59,7 @@ class SagPlanInfo(ctypes.Structure):
     """Mirror of ``sag_plan_info`` in include/selattn.h."""
     _fields_ = [("workspace_bytes", ctypes.c_uint64), ("launches", ctypes.c_int32),
                 ("token_chunks", ctypes.c_int32), ("items", ctypes.c_int64),
-                ("main_kernel", ctypes.c_int32), ("reserved_", ctypes.c_int32)]
+                ("main_kernel", ctypes.c_int32), ("dq_path", ctypes.c_int32)]
 
 
 class SagError(RuntimeError):

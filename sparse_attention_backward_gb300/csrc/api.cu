@@ -40,9 +40,27 @@ constexpr int64_t kFwdWindowBytes = 32LL << 20;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// Default mode: reduce dQ with fp32 atomics inside the main kernel, or store
+// dS and form dQ by the fixed-order pass.  Bytes moved per query row:
+//   reductions: count * halves * d_qk * 4 (one fp32 partial per key tile)
+//   dS pass:    count * bs * 2 * 2 (dS out and back) + count * bs * d_qk * 2 / G
+//               (every selected key block re-read per (token, KV head))
+// The pass is taken only when it moves less than half the reductions' bytes:
+// measured on GB300 it has overheads the count misses (token chunks, its own
+// launch).  SELATTN_DQ_PASS=0 / 1 forces either.
+bool prefer_dq_pass(const Geometry &g) {
+    const char *env = getenv("SELATTN_DQ_PASS");
+    if (env && env[0] == '0') return false;
+    if (env && env[0] == '1') return true;
+    const double red = (double)g.block_count * g.halves * g.d_qk * 4;
+    const double pass = (double)g.block_count * g.block_size * 4 + (double)g.block_count * g.block_size * g.d_qk * 2 / g.group;
+    return pass < 0.5 * red;
+}
+
 struct Plan {
     Geometry g;
     bool fp16, det;
+    bool ds_path;                     // dQ from the stored dS by the fixed-order pass (else fp32 reductions)
     // byte offsets inside the workspace
     size_t o_hdr, o_cu_q, o_cu_kv, o_item_base, o_unit_base, o_wtab_base, o_count, o_offset, o_cursor, o_scan,
         o_entries, o_wtab, o_delta, o_lse2, o_dq_acc, o_ds, o_dkv, total;
@@ -133,6 +151,7 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     g.scale_log2 = (float)(d->scale * 1.4426950408889634);
     p->fp16 = d->dtype == SAG_FP16;
     p->det = d->deterministic != 0;
+    p->ds_path = p->det;
     p->item_base.assign(d->batch + 1, 0);
     for (int b = 0; b < d->batch; ++b) {
         // every block of the (padded) key rows is an item: blocks no token may
@@ -163,7 +182,8 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     // forces windows on smaller problems too).
     const char *wenv = getenv(forward ? "SELATTN_FWD_WINDOW_TOKENS" : "SELATTN_WINDOW_TOKENS");
     const int acc_cols = forward ? g.d_v : g.d_qk;
-    g.windowed = p->use_tc && !p->det &&
+    if (!forward && !p->det) p->ds_path = prefer_dq_pass(g);
+    g.windowed = p->use_tc && !p->ds_path &&
                  (rows * acc_cols * 4 > (forward ? kFwdWindowMinAcc : kWindowMinAcc) || (wenv && atoll(wenv) > 0));
     if (wenv && atoll(wenv) < 0) g.windowed = false;
     {
@@ -204,7 +224,7 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     p->o_wtab = take(sizeof(int32_t) * (p->wtab_base.empty() ? 0 : p->wtab_base[g.batch]));
     p->o_delta = take(sizeof(float) * rows);
     p->o_lse2 = take(sizeof(float) * rows);
-    p->o_dq_acc = p->det ? o : take(sizeof(float) * rows * g.d_qk);
+    p->o_dq_acc = p->ds_path ? o : take(sizeof(float) * rows * g.d_qk);
     const int64_t ds_per_token = (int64_t)g.n2 * g.block_count * g.group * g.block_size * 2;
     int64_t chunk = kDsChunkBytes / ds_per_token;
     // SELATTN_DS_CHUNK_TOKENS sets the chunk length (tests run the chunked
@@ -213,9 +233,9 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     if (cenv && atoll(cenv) > 0) chunk = atoll(cenv);
     if (chunk < 1) chunk = 1;
     if (chunk > g.t1) chunk = g.t1;
-    p->chunk_tokens = p->det ? (int32_t)chunk : g.t1;
-    p->n_chunks = p->det ? (int32_t)((g.t1 + chunk - 1) / chunk) : 1;
-    p->o_ds = p->det ? take((size_t)ds_per_token * chunk) : o;
+    p->chunk_tokens = p->ds_path ? (int32_t)chunk : g.t1;
+    p->n_chunks = p->ds_path ? (int32_t)((g.t1 + chunk - 1) / chunk) : 1;
+    p->o_ds = p->ds_path ? take((size_t)ds_per_token * chunk) : o;
     p->o_dkv = (p->n_chunks > 1 || g.windowed) ? take(sizeof(float) * (int64_t)g.t2 * g.n2 * (g.d_qk + g.d_v)) : o;
     g.tok_lo = 0;
     g.tok_hi = g.t1;
@@ -240,8 +260,8 @@ Workspace carve(const Plan &p, void *base) {
     w.entries = reinterpret_cast<int32_t *>(c + p.o_entries);
     w.delta = reinterpret_cast<float *>(c + p.o_delta);
     w.lse2 = reinterpret_cast<float *>(c + p.o_lse2);
-    w.dq_acc = p.det ? nullptr : reinterpret_cast<float *>(c + p.o_dq_acc);
-    w.ds = p.det ? reinterpret_cast<uint16_t *>(c + p.o_ds) : nullptr;
+    w.dq_acc = p.ds_path ? nullptr : reinterpret_cast<float *>(c + p.o_dq_acc);
+    w.ds = p.ds_path ? reinterpret_cast<uint16_t *>(c + p.o_ds) : nullptr;
     w.dkv_acc = (p.n_chunks > 1 || p.g.windowed) ? reinterpret_cast<float *>(c + p.o_dkv) : nullptr;
     w.unit_base = reinterpret_cast<int64_t *>(c + p.o_unit_base);
     w.wtab_base = reinterpret_cast<int64_t *>(c + p.o_wtab_base);
@@ -293,7 +313,7 @@ namespace {
 int launches_of(const Plan &p) {
     // preprocess, histogram, 3 scan passes, fill, sort
     int n = 7;
-    if (!p.det) return n + 2 + (p.g.windowed ? 1 : 0);   // main, cast dQ (, cast dK/dV)
+    if (!p.ds_path) return n + 2 + (p.g.windowed ? 1 : 0);   // main, cast dQ (, cast dK/dV)
     return n + 2 * p.n_chunks + (p.n_chunks > 1);    // (main, dQ) per chunk, cast dK/dV
 }
 }  // namespace
@@ -308,7 +328,7 @@ extern "C" sag_status sel_attn_grad_plan_info(const sag_desc *desc, sag_plan_inf
     info->token_chunks = p.n_chunks;
     info->items = p.g.n_items;
     info->main_kernel = p.use_tc ? 1 : 0;
-    info->reserved_ = 0;
+    info->dq_path = p.ds_path ? 1 : 0;
     return SAG_OK;
 }
 
@@ -419,10 +439,10 @@ extern "C" sag_status sel_attn_grad_ex(const sag_desc *desc, const sag_io *io, v
     if (st != SAG_OK) return st;
 
     if ((launch_preprocess(g, ws, io->attention_out, io->attention_out_grad, io->softmax_max, io->softmax_sum,
-                           p.fp16, !p.det, s, sms)) != cudaSuccess)
+                           p.fp16, !p.ds_path, s, sms)) != cudaSuccess)
         return SAG_ERR_CUDA;
     if ((launch_inversion(g, ws, io->topk_indices, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
-    if (!p.det) {
+    if (!p.ds_path) {
         if (g.windowed &&
             cudaMemsetAsync(ws.dkv_acc, 0, sizeof(float) * (size_t)g.t2 * g.n2 * (g.d_qk + g.d_v), s) != cudaSuccess)
             return SAG_ERR_CUDA;
@@ -434,7 +454,8 @@ extern "C" sag_status sel_attn_grad_ex(const sag_desc *desc, const sag_io *io, v
             return SAG_ERR_CUDA;
         return SAG_OK;
     }
-    // deterministic: token chunks in order; dS of a chunk -> its dQ
+    // deterministic mode (or the dQ pass chosen for the default mode): token
+    // chunks in order; dS of a chunk -> its dQ
     if (g.chunked && cudaMemsetAsync(ws.dkv_acc, 0, sizeof(float) * (size_t)g.t2 * g.n2 * (g.d_qk + g.d_v), s) !=
                          cudaSuccess)
         return SAG_ERR_CUDA;

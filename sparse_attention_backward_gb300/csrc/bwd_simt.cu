@@ -177,62 +177,73 @@ __global__ void __launch_bounds__(512) k_bwd_simt(Geometry g, Workspace ws,
 
 // dQ[t, n2*G+g] = scale * sum_slot sum_r dS[t][n2][slot][g][r] * K[row(slot, r)]
 // in slot order then key order: one CTA per (t, n2).
+// Fixed-order dQ from the stored dS on CUDA cores (deterministic mode, for
+// shapes the tensor-core pass does not take):
+//     dQ[t, h] = scale * sum over slots in list order, keys in block order, of
+//                dS[t, h, slot, key] * K[key row]
+// One warp per (token, KV head) and group of up to kHeadsPerWarp query heads;
+// lane l owns head dims [l * DQK/32, (l + 1) * DQK/32) of those heads.  No
+// shared memory and no block barrier: a key row is one coalesced warp load,
+// the dS value of a head a broadcast load.
+constexpr int kHeadsPerWarp = 8;
+
 template <bool kFp16, int DQK>
 __global__ void __launch_bounds__(256) k_dq_from_ds(Geometry g, Workspace ws,
                                                     const uint16_t *__restrict__ k,
                                                     const uint16_t *__restrict__ k_rope,
                                                     const int32_t *__restrict__ topk,
                                                     uint16_t *__restrict__ dq, uint16_t *__restrict__ dq_rope) {
-    extern __shared__ float smem[];
+    constexpr int DPL = DQK / 32;                       // dims per lane: 4 or 6
     const int bs = g.block_size, G = g.group;
     const int d_main = DQK - g.d_rope;
-    float *sk = smem;               // [bs][DQK]
-    float *sds = sk + bs * DQK;     // [G][bs]
-    const int64_t npairs = (int64_t)(g.tok_hi - g.tok_lo) * g.n2;
-    for (int64_t cp = blockIdx.x; cp < npairs; cp += gridDim.x) {
+    const int lane = threadIdx.x & 31;
+    const int hgroups = (G + kHeadsPerWarp - 1) / kHeadsPerWarp;
+    const int64_t nwork = (int64_t)(g.tok_hi - g.tok_lo) * g.n2 * hgroups;
+    const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t wk = (((int64_t)blockIdx.x * blockDim.x) >> 5) + (threadIdx.x >> 5); wk < nwork; wk += warps) {
+        const int64_t cp = wk / hgroups;                // pair index inside the chunk
+        const int h0 = (int)(wk % hgroups) * kHeadsPerWarp;
+        const int nh = min(kHeadsPerWarp, G - h0);
         const int t = g.tok_lo + (int)(cp / g.n2), n2 = (int)(cp % g.n2);
         const int64_t pair = (int64_t)t * g.n2 + n2;
         const int b = batch_of(ws.cu_q, g.batch, t);
         const int nblk = t < ws.q_end[b] ? ws.kv_blocks[b] : 0;   // ids must be below; none for padding
-        // each thread owns outputs o = threadIdx.x + 256*i over G*DQK
-        constexpr int kMaxPerThread = (32 * DQK + 255) / 256;
-        float acc[kMaxPerThread];
+        float acc[kHeadsPerWarp][DPL];
 #pragma unroll
-        for (int i = 0; i < kMaxPerThread; ++i) acc[i] = 0.f;
+        for (int h = 0; h < kHeadsPerWarp; ++h)
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
         for (int slot = 0; slot < g.block_count; ++slot) {
-            const int id = topk[pair * g.block_count + slot];
+            const int id = __ldg(topk + pair * g.block_count + slot);
             if (id < 0 || id >= nblk) continue;       // reported by the histogram
             const int64_t key0 = ws.cu_kv[b] + (int64_t)id * bs;
-            __syncthreads();
-            for (int i = threadIdx.x; i < bs * DQK; i += blockDim.x) {
-                const int r = i / DQK, d = i % DQK;
+            const uint16_t *dsrow = ws.ds + ((cp * g.block_count + slot) * (int64_t)G + h0) * bs;
+            for (int r = 0; r < bs; ++r) {
                 const int64_t krow = (key0 + r) * g.n2 + n2;
-                sk[i] = u16_to_f<kFp16>(d < d_main ? k[krow * d_main + d] : k_rope[krow * g.d_rope + d - d_main]);
-            }
-            const int64_t dbase = (cp * g.block_count + slot) * (int64_t)G * bs;
-            for (int i = threadIdx.x; i < G * bs; i += blockDim.x) sds[i] = u16_to_f<kFp16>(ws.ds[dbase + i]);
-            __syncthreads();
+                float kv[DPL];
 #pragma unroll
-            for (int i = 0; i < kMaxPerThread; ++i) {
-                const int o = threadIdx.x + 256 * i;
-                if (o < G * DQK) {
-                    const int gg = o / DQK, d = o % DQK;
-                    float a = acc[i];
-                    for (int r = 0; r < bs; ++r) a = fmaf(sds[gg * bs + r], sk[r * DQK + d], a);
-                    acc[i] = a;
+                for (int e = 0; e < DPL; ++e) {
+                    const int d = lane * DPL + e;
+                    kv[e] = u16_to_f<kFp16>(d < d_main ? __ldg(k + krow * d_main + d)
+                                                       : __ldg(k_rope + krow * g.d_rope + d - d_main));
+                }
+#pragma unroll
+                for (int h = 0; h < kHeadsPerWarp; ++h) {
+                    if (h >= nh) break;
+                    const float sv = u16_to_f<kFp16>(dsrow[(int64_t)h * bs + r]);
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(sv, kv[e], acc[h][e]);
                 }
             }
         }
 #pragma unroll
-        for (int i = 0; i < kMaxPerThread; ++i) {
-            const int o = threadIdx.x + 256 * i;
-            if (o < G * DQK) {
-                const int gg = o / DQK, d = o % DQK;
-                *split_col(dq, dq_rope, (int64_t)t * g.n1 + n2 * G + gg, d, DQK, g.d_rope) =
-                    f_to_u16<kFp16>(acc[i] * g.scale);
-            }
+        for (int h = 0; h < kHeadsPerWarp; ++h) {
+            if (h >= nh) break;
+            const int64_t row = (int64_t)t * g.n1 + (int64_t)n2 * G + h0 + h;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e)
+                *split_col(dq, dq_rope, row, lane * DPL + e, DQK, g.d_rope) = f_to_u16<kFp16>(acc[h][e] * g.scale);
         }
-        __syncthreads();
     }
 }
 
@@ -296,15 +307,13 @@ cudaError_t launch_bwd_simt(const Geometry &g, const Workspace &ws, const sag_io
 template <bool kFp16, int DQK>
 static cudaError_t launch_dq_t(const Geometry &g, const Workspace &ws, const sag_io &io, cudaStream_t s,
                                int num_sms) {
-    const size_t smem = sizeof(float) * ((size_t)g.block_size * DQK + (size_t)g.group * g.block_size);
-    auto fn = k_dq_from_ds<kFp16, DQK>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    int64_t grid = (int64_t)(g.tok_hi - g.tok_lo) * g.n2;
-    if (grid > (int64_t)num_sms * 32) grid = (int64_t)num_sms * 32;
+    const int hgroups = (g.group + kHeadsPerWarp - 1) / kHeadsPerWarp;
+    const int64_t warps = (int64_t)(g.tok_hi - g.tok_lo) * g.n2 * hgroups;
+    int64_t grid = (warps + 7) / 8;
+    if (grid > (int64_t)num_sms * 16) grid = (int64_t)num_sms * 16;
     if (grid == 0) return cudaSuccess;
-    fn<<<(int)grid, 256, smem, s>>>(g, ws, (const uint16_t *)io.key, (const uint16_t *)io.key_rope,
-                                    io.topk_indices, (uint16_t *)io.dq, (uint16_t *)io.dq_rope);
+    k_dq_from_ds<kFp16, DQK><<<(int)grid, 256, 0, s>>>(g, ws, (const uint16_t *)io.key, (const uint16_t *)io.key_rope,
+                                                       io.topk_indices, (uint16_t *)io.dq, (uint16_t *)io.dq_rope);
     return cudaGetLastError();
 }
 

@@ -32,6 +32,9 @@ namespace sag {
 namespace {
 
 constexpr int kMeta = 4;            // depth of the tile-metadata ring
+constexpr int kSoftmaxWarps = 4;    // one per TMEM lane quarter
+constexpr int kEpiWarp0 = 2 + kSoftmaxWarps;
+constexpr int kBwdThreads = (kEpiWarp0 + 4) * 32;
 
 // TMEM columns (512 allocated)
 constexpr uint32_t kColS = 0, kColDP = 64, kColDV = 128, kColDKlo = 192, kColDKhi = 256, kColDQ = 320;
@@ -70,7 +73,7 @@ struct TcArgs {
 };
 
 template <bool kFp16, int DQK>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     k_bwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
              const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
              const __grid_constant__ CUtensorMap map_qr, const __grid_constant__ CUtensorMap map_kr, TcArgs A) {
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(&bars[B_DO_EMPTY0 + s], 1);
         }
         tc::mbar_init(&bars[B_S_FULL], 1);
-        tc::mbar_init(&bars[B_P_FULL], 128);
+        tc::mbar_init(&bars[B_P_FULL], kSoftmaxWarps * 32);
         tc::mbar_init(&bars[B_MMA_DONE], 1);
         tc::mbar_init(&bars[B_DQ_FREE], 128);
         tc::mbar_init(&bars[B_ACC_FULL], 1);
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows of a Q / dY tile no token fills (when G does not divide 128) must
     // hold finite values: zero the staging buffers once
     if (tpt * G < kRows) {
-        for (int i = threadIdx.x; i < (2 * L::Q_STAGE + DOS * L::DO_STAGE) / 16; i += kThreads)
+        for (int i = threadIdx.x; i < (2 * L::Q_STAGE + DOS * L::DO_STAGE) / 16; i += kBwdThreads)
             reinterpret_cast<uint4 *>(smem + L::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
         tc::fence_proxy_async_smem();
     }
@@ -255,8 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ne > 0 && !tc::mbar_wait(&bars[B_ACC_FREE], (ne - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
                     const int s = tc_i & 1, d = tc_i % DOS;
-                    if (!tc::mbar_wait(&bars[B_Q_FULL0 + s], (tc_i >> 1) & 1, abort_flag, kWaitNs) ||
-                        !tc::mbar_wait(&bars[B_DO_FULL0 + d], (tc_i / DOS) & 1, abort_flag, kWaitNs)) {
+                    if (!tc::mbar_wait(&bars[B_Q_FULL0 + s], (tc_i >> 1) & 1, abort_flag, kWaitNs)) {
                         ok = false;
                         break;
                     }
@@ -264,10 +266,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t qs = sbase + L::OFF_Q + s * L::Q_STAGE;
                     const uint32_t ds_ = sbase + L::OFF_DO + d * L::DO_STAGE;
                     const uint32_t ks = sbase + L::OFF_K, vs = sbase + L::OFF_V;
-                    // S = Q K^T, dP = dY V^T (both operands K-major)
+                    // S = Q K^T, dP = dY V^T (both operands K-major); S is issued
+                    // before dY has landed
                     for (int kk = 0; kk < DQK / 16; ++kk)
                         tc::mma_f16_ss(tmem + kColS, tc::sw128_desc(qs + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                                        tc::sw128_desc(ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+                    if (!tc::mbar_wait(&bars[B_DO_FULL0 + d], (tc_i / DOS) & 1, abort_flag, kWaitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
                     for (int kk = 0; kk < DV / 16; ++kk)
                         tc::mma_f16_ss(tmem + kColDP, tc::sw128_desc(ds_ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                                        tc::sw128_desc(vs + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
@@ -312,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_commit(&bars[B_DRAIN]);
             if (!tc::mbar_wait_drain(&bars[B_DRAIN], 0, kWaitNs)) fail();
         }
-    } else if (warp < 6) {
+    } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------ softmax / dS
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;                      // query row = TMEM lane
@@ -339,25 +347,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = tc::mbar_wait(&bars[B_S_FULL], tc_i & 1, abort_flag, kWaitNs);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc::tc_fence_after();
+                // S and dP in two rounds of 32 keys, each round's loads in flight
+                // before one wait
                 uint32_t pk[32], dk2[32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (c >= nk / 16) break;
-                    uint32_t sv[16], dv[16];
-                    tc::tmem_ld16(trow + kColS + c * 16, sv);
-                    tc::tmem_ld16(trow + kColDP + c * 16, dv);
+                for (int h = 0; h < 2; ++h) {
+                    if (32 * h >= nk) break;
+                    uint32_t sv[4][8], dv[4][8];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (32 * h + 8 * j < nk) {
+                            tc::tmem_ld8(trow + kColS + 32 * h + 8 * j, sv[j]);
+                            tc::tmem_ld8(trow + kColDP + 32 * h + 8 * j, dv[j]);
+                        }
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        float p0 = 0.f, p1 = 0.f, d0 = 0.f, d1 = 0.f;
-                        if (valid) {
-                            p0 = ex2(fmaf(__uint_as_float(sv[j]), g.scale_log2, -lse2));
-                            p1 = ex2(fmaf(__uint_as_float(sv[j + 1]), g.scale_log2, -lse2));
-                            d0 = p0 * (__uint_as_float(dv[j]) - delta);
-                            d1 = p1 * (__uint_as_float(dv[j + 1]) - delta);
+                    for (int j = 0; j < 4; ++j) {
+                        if (32 * h + 8 * j >= nk) break;
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            float p0 = 0.f, p1 = 0.f, d0 = 0.f, d1 = 0.f;
+                            if (valid) {
+                                p0 = ex2(fmaf(__uint_as_float(sv[j][e]), g.scale_log2, -lse2));
+                                p1 = ex2(fmaf(__uint_as_float(sv[j][e + 1]), g.scale_log2, -lse2));
+                                d0 = p0 * (__uint_as_float(dv[j][e]) - delta);
+                                d1 = p1 * (__uint_as_float(dv[j][e + 1]) - delta);
+                            }
+                            pk[16 * h + j * 4 + e / 2] = pack2<kFp16>(p0, p1);
+                            dk2[16 * h + j * 4 + e / 2] = pack2<kFp16>(d0, d1);
                         }
-                        pk[c * 8 + j / 2] = pack2<kFp16>(p0, p1);
-                        dk2[c * 8 + j / 2] = pack2<kFp16>(d0, d1);
                     }
                 }
                 // the previous tile's MMAs must be done with the P / dS buffers
@@ -368,12 +386,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *prow = smem + L::OFF_P;
                 uint8_t *drow = smem + L::OFF_DS;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    if (c >= nk / 8) break;
-                    *reinterpret_cast<uint4 *>(prow + sw_off(r, c)) =
-                        make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
-                    *reinterpret_cast<uint4 *>(drow + sw_off(r, c)) =
-                        make_uint4(dk2[c * 4], dk2[c * 4 + 1], dk2[c * 4 + 2], dk2[c * 4 + 3]);
+                for (int j = 0; j < 8; ++j) {
+                    if (8 * j >= nk) break;
+                    *reinterpret_cast<uint4 *>(prow + sw_off(r, j)) =
+                        make_uint4(pk[j * 4], pk[j * 4 + 1], pk[j * 4 + 2], pk[j * 4 + 3]);
+                    *reinterpret_cast<uint4 *>(drow + sw_off(r, j)) =
+                        make_uint4(dk2[j * 4], dk2[j * 4 + 1], dk2[j * 4 + 2], dk2[j * 4 + 3]);
                 }
                 if (det && valid) {
                     // dS[t - tok_lo][n2][slot][g][key] in the input dtype
@@ -383,8 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         kt.koff;
                     uint4 *dst = reinterpret_cast<uint4 *>(ws.ds + base);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        if (c < nk / 8) dst[c] = make_uint4(dk2[c * 4], dk2[c * 4 + 1], dk2[c * 4 + 2], dk2[c * 4 + 3]);
+                    for (int j = 0; j < 8; ++j)
+                        if (8 * j < nk) dst[j] = make_uint4(dk2[j * 4], dk2[j * 4 + 1], dk2[j * 4 + 2], dk2[j * 4 + 3]);
                 }
                 tc::fence_proxy_async_smem();
                 tc::tc_fence_before();
@@ -398,8 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = q4 * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
         const int tt = r / G, gg = r % G;
-        uint8_t *stg = smem + L::OFF_STG + (warp - 6) * 4096;
-        const int et = threadIdx.x - 192;                 // 0..127
+        uint8_t *stg = smem + L::OFF_STG + (warp - kEpiWarp0) * 4096;
+        const int et = threadIdx.x - kEpiWarp0 * 32;      // 0..127
         int ne = 0, tc_i = 0;
         bool ok = true;
         for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
@@ -536,7 +554,7 @@ static cudaError_t launch_tc_t(const Geometry &g, const Workspace &ws, const sag
     if (e != cudaSuccess) return e;
     int64_t grid = a.n_titems < num_sms ? a.n_titems : num_sms;
     if (grid < 1) grid = 1;
-    fn<<<(int)grid, kThreads, smem, s>>>(m.q, mdo, m.k, mv, m.qr, m.kr, a);
+    fn<<<(int)grid, kBwdThreads, smem, s>>>(m.q, mdo, m.k, mv, m.qr, m.kr, a);
     return cudaGetLastError();
 }
 

@@ -219,3 +219,20 @@ def test_bsnd_and_rope_descriptors(lib):
     assert _status(_desc(**dict(rope, d_qk=192)))[0] == G            # 256 in all
     # the rope split: same workspace as the unsplit 192-wide problem
     assert _status(_desc(**rope))[1] == _status(_desc(d_qk=192, d_v=128))[1]
+
+
+def test_dq_path_of_the_plan(lib, monkeypatch):
+    """The deterministic mode always forms dQ by the fixed-order pass; the
+    default mode reduces it in the main kernel on the five workloads (the
+    pass would move more bytes on each), unless SELATTN_DQ_PASS forces it."""
+    import synth
+    for w in synth.WORKLOADS:
+        for det in (False, True):
+            d = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
+                              sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, det)
+            assert sab.plan_info(d).dq_path == (1 if det else 0), (w.name, det)
+    monkeypatch.setenv("SELATTN_DQ_PASS", "1")
+    w = synth.WORKLOADS[2]
+    d = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale)
+    info = sab.plan_info(d)
+    assert info.dq_path == 1 and info.token_chunks == 1 and info.launches == 9

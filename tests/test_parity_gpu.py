@@ -209,3 +209,18 @@ def test_bucket_beyond_the_shared_memory_sort():
     again = _run(w, x, True)
     for u, v in zip(outs[True], again):
         assert torch.equal(u.view(torch.int16), v.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127"])
+def test_default_mode_with_the_dq_pass(small_data, name, monkeypatch):
+    """The default mode with dQ formed from the stored dS by the fixed-order
+    pass (the plan's other dQ path), forced on."""
+    monkeypatch.setenv("SELATTN_DQ_PASS", "1")
+    w, x, (rdq, rdk, rdv) = small_data(name)
+    desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
+                         sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, False)
+    assert sab.plan_info(desc).dq_path == 1
+    dq, dk, dv = _run(w, x, False)
+    S.assert_close(f"{name} dq pass dq", S.f64(dq), rdq)
+    S.assert_close(f"{name} dq pass dk", S.f64(dk), rdk)
+    S.assert_close(f"{name} dq pass dv", S.f64(dv), rdv)
