@@ -15,6 +15,8 @@ marshals numpy arrays into it.  What each function follows on the pages:
 * ``backward``, ``dq_rows``, ``dkdv_block`` -- "NsaSelectedAttentionGrad"
   README, function description (dV = P^T dY, dQ = dS K / sqrt(d),
   dK = dS^T Q / sqrt(d) over the gathered rows, scatter-added back).
+* ``oracle.indexer`` -- the lightning-indexer backward of the
+  "aclnnLightningIndexerGrad" page (``indexer_oracle.c``).
 
 Every function is pinned by tests that do not reuse its formulas: central
 finite differences, torch fp64 autograd of the gathered and of the dense
@@ -31,6 +33,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "selattn_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "indexer_oracle.c")]
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
 F64, BF16, F16, F32 = 0, 1, 2, 3
@@ -56,10 +59,11 @@ class _Problem(ctypes.Structure):
 
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (host code only; same result on x86 and Arm)."""
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    if (force or not os.path.exists(_LIB_PATH)
+            or os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(f) for f in _SRCS)):
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-Wall", "-shared", "-fPIC",
-                               "-o", tmp, _SRC, "-lm"])
+                               "-o", tmp, *_SRCS, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 

@@ -174,3 +174,86 @@ def make_inputs(w: Workload, device="cpu", seed: int | None = None) -> dict:
         "dy": _normal((w.t1, w.n1, w.d_v), w.std, dt, gen, device),
         "topk": make_topk(w, gen, device),
     }
+
+
+# ------------------------------------------------------------ lightning indexer
+@dataclass(frozen=True)
+class IndexerWorkload:
+    """A lightning-indexer backward problem: query [T1, n1, d], key [T2, n2, d],
+    weights [T1, n1], indices / dy [T1, n2, topk] (dy fp32)."""
+    name: str
+    cu_q: tuple
+    cu_kv: tuple
+    n1: int
+    n2: int
+    d: int
+    topk: int
+    dtype: str
+    empty_frac: float     # fraction of slots set to -1 (empty)
+    seed: int
+
+    @property
+    def batch(self) -> int:
+        return len(self.cu_q) - 1
+
+    @property
+    def t1(self) -> int:
+        return self.cu_q[-1]
+
+    @property
+    def t2(self) -> int:
+        return self.cu_kv[-1]
+
+    @property
+    def group(self) -> int:
+        return self.n1 // self.n2
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float16
+
+    def flops(self) -> float:
+        """Three contractions of 2 * d flops per (query head, selected key):
+        scores, dQ and dK."""
+        return 3 * 2.0 * self.d * self.topk * self.t1 * self.n1
+
+    def with_(self, **kw) -> "IndexerWorkload":
+        d = dict(self.__dict__)
+        d.update(kw)
+        return IndexerWorkload(**d)
+
+
+INDEXER_WORKLOADS = [
+    IndexerWorkload("indexer_tiny", (0, 256), (0, 256), 16, 1, 128, 64, "bf16", 0.0, 20261000),
+    IndexerWorkload("indexer_varlen", (0, 300, 1000), (0, 300, 1000), 32, 1, 128, 128, "f16", 0.05, 20261001),
+    IndexerWorkload("indexer_long", (0, 8192), (0, 8192), 64, 1, 128, 2048, "bf16", 0.0, 20261002),
+]
+
+
+def make_indexer_inputs(w: IndexerWorkload, device="cpu", seed: int | None = None) -> dict:
+    """q, k, weights ~ N(0, 1) rounded to the dtype; dy ~ N(0, 1) fp32; per
+    (token, key head) topk distinct key positions of the token's batch, sorted,
+    a seeded fraction of slots then set to -1 (empty)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed if seed is None else seed)
+    dt = w.torch_dtype
+    x = {
+        "q": _normal((w.t1, w.n1, w.d), 1.0, dt, gen, device),
+        "k": _normal((w.t2, w.n2, w.d), 1.0, dt, gen, device),
+        "w": _normal((w.t1, w.n1), 1.0, dt, gen, device),
+        "dy": torch.randn((w.t1, w.n2, w.topk), generator=gen, device=device, dtype=torch.float32),
+    }
+    idx = torch.full((w.t1, w.n2, w.topk), -1, dtype=torch.int32, device=device)
+    for b in range(w.batch):
+        q0, q1 = w.cu_q[b], w.cu_q[b + 1]
+        s2 = w.cu_kv[b + 1] - w.cu_kv[b]
+        rows = (q1 - q0) * w.n2
+        if rows == 0:
+            continue
+        chunk = max(1, (1 << 28) // max(1, s2 * 4))
+        idx[q0:q1] = _distinct_sorted(rows, w.topk, s2, gen, device, chunk).view(q1 - q0, w.n2, w.topk)
+    if w.empty_frac > 0:
+        drop = torch.rand((w.t1, w.n2, w.topk), generator=gen, device=device) < w.empty_frac
+        idx = torch.where(drop, torch.full_like(idx, -1), idx)
+    x["idx"] = idx
+    return x
