@@ -354,6 +354,73 @@ sag_status sel_attn_fwd_timed(const sag_desc *desc, const void *query, const voi
 sag_status sel_attn_fwd_ex(const sag_desc *desc, const sag_io *io, void *workspace, size_t workspace_bytes,
                            void *stream, void *passes_start, void *passes_stop);
 
+/*
+ * Lightning-indexer backward ("aclnnLightningIndexerGrad", formula section):
+ *     S  = Relu(Matmul(Query, Gather(Key, Indices)))
+ *     Y  = Dy * Weights
+ *     dW = Reduce(S * dy)
+ *     dQ = Matmul(ReluGrad(Y, S), Gather(Key, Indices))
+ *     dK = ScatterAdd(Matmul(ReluGrad(Y, S), Q), Indices)
+ * i.e. with G = n1 / n2 query heads per key head (h uses key head h / G):
+ *     S[t,h,j] = relu(<q[t,h], k[idx[t,n2,j]]>)        (no scale)
+ *     R[t,h,j] = dy[t,n2,j] * w[t,h] where S[t,h,j] > 0, else 0
+ *     dW[t,h]  = sum_j S[t,h,j] * dy[t,n2,j]
+ *     dQ[t,h]  = sum_j R[t,h,j] * k[idx[t,n2,j]]
+ *     dK[idx[t,n2,j]] += sum_h R[t,h,j] * q[t,h]      (a position named twice adds twice)
+ * The page's parameter tables are lost; the shapes are this library's reading.
+ *
+ *   batch, layout, cu_seqlens_q / cu_seqlens_kv, s1_max / s2_max: as in
+ *                 sag_desc (TND, or BSND padded to s1_max / s2_max rows)
+ *   n1, n2        query heads and key heads (n1 % n2 == 0, G = n1 / n2 <= 64)
+ *   d             head dim of query and key (128)
+ *   topk          selections per (query token, key head), >= 1; every batch's
+ *                 key length is >= topk
+ *   dtype         SAG_BF16 / SAG_FP16 of query, key, weights, dq, dk, dweights
+ *   deterministic must be 0 (a bitwise-reproducible mode is not built: dK and
+ *                 dW are summed with fp32 atomics)
+ */
+typedef struct sli_desc {
+    int32_t batch;
+    int32_t n1, n2;
+    int32_t d;
+    int32_t topk;
+    int32_t dtype;
+    int32_t deterministic;
+    int32_t layout;
+    const int32_t *cu_seqlens_q;
+    const int32_t *cu_seqlens_kv;
+    int32_t s1_max, s2_max;
+} sli_desc;
+
+/*
+ * Tensors (device pointers, 16-byte aligned, dense; R1 / R2 rows as in sag_io):
+ *   query     [R1, n1, d]     dtype
+ *   key       [R2, n2, d]     dtype
+ *   weights   [R1, n1]        dtype
+ *   dy        [R1, n2, topk]  fp32: gradient of the index score at each selection
+ *   indices   [R1, n2, topk]  int32 key positions local to the token's batch;
+ *                             -1 marks an empty slot (skipped); any other id
+ *                             outside [0, S2_b) is reported (SAG_ERR_INDEX) and
+ *                             skipped
+ *   dq        [R1, n1, d], dk [R2, n2, d], dweights [R1, n1]: written (padding
+ *             rows and key rows nobody selected get zeros)
+ */
+typedef struct sli_io {
+    const void *query, *key, *weights;
+    const float *dy;
+    const int32_t *indices;
+    void *dq, *dk, *dweights;
+} sli_io;
+
+/* Phase 1 (host only): validation and workspace size.  SAG_ERR_UNSUPPORTED for
+ * d != 128, G > 64 or deterministic == 1. */
+sag_status lightning_indexer_grad_workspace_size(const sli_desc *desc, size_t *workspace_bytes);
+
+/* Phase 2: enqueue on `stream`; ownership, errors and device status as for
+ * sel_attn_grad (sel_attn_grad_query_error reads this call's workspace). */
+sag_status lightning_indexer_grad(const sli_desc *desc, const sli_io *io, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *sel_attn_grad_status_string(int status);
 

@@ -90,6 +90,8 @@ def _lib():
     if not getattr(lib, "_lio_ready", False):
         P, dp = ctypes.POINTER(_Lio), ctypes.c_void_p
         lib.lio_backward.argtypes = [P, dp, dp, dp]
+        lib.lio_backward_range.argtypes = [P, ctypes.c_int64, ctypes.c_int64, dp, dp, dp]
+        lib.lio_backward_range.restype = ctypes.c_int
         lib.lio_scores.argtypes = [P, dp]
         lib.lio_q_rows.argtypes = [P, ctypes.c_int64, dp, dp, dp]
         lib.lio_k_rows.argtypes = [P, ctypes.c_int64, dp, dp, dp]
@@ -111,6 +113,18 @@ def backward(p: Problem):
     dw = np.zeros((p.t1, p.n1))
     c, _keep = p._c()
     _check(_lib().lio_backward(ctypes.byref(c), dq.ctypes.data, dk.ctypes.data, dw.ctypes.data), "backward")
+    return dq, dk, dw
+
+
+def backward_range(p: Problem, t_lo: int, t_hi: int):
+    """The backward of the query rows [t_lo, t_hi) only (dk holds their
+    contributions); the ranges of a partition sum to ``backward``."""
+    dq = np.zeros((p.t1, p.n1, p.d))
+    dk = np.zeros((p.t2, p.n2, p.d))
+    dw = np.zeros((p.t1, p.n1))
+    c, _keep = p._c()
+    _check(_lib().lio_backward_range(ctypes.byref(c), int(t_lo), int(t_hi), dq.ctypes.data, dk.ctypes.data,
+                                     dw.ctypes.data), "backward_range")
     return dq, dk, dw
 
 

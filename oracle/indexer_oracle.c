@@ -93,10 +93,12 @@ static int check(const lio_problem *p)
 }
 
 /*
- * The whole backward.  dq [T1, n1, d], dk [T2, n2, d], dw [T1, n1] are
- * overwritten (padding rows and unselected key rows stay zero).
+ * The backward restricted to the query rows t in [t_lo, t_hi): their dq and
+ * dw rows and their contributions to dk.  dq [T1, n1, d], dk [T2, n2, d],
+ * dw [T1, n1] are overwritten (rows outside the range, padding rows and key
+ * rows no query in the range selected stay zero).
  */
-int lio_backward(const lio_problem *p, double *dq, double *dk, double *dw)
+int lio_backward_range(const lio_problem *p, int64_t t_lo, int64_t t_hi, double *dq, double *dk, double *dw)
 {
     int rc = check(p);
     if (rc) return rc;
@@ -106,7 +108,8 @@ int lio_backward(const lio_problem *p, double *dq, double *dk, double *dw)
     memset(dw, 0, sizeof(double) * rows_q(p) * p->n1);
     for (int b = 0; b < p->batch; ++b) {
         const int64_t s2 = p->cu_kv[b + 1] - p->cu_kv[b];
-        for (int64_t t = q0(p, b); t < q0(p, b) + (p->cu_q[b + 1] - p->cu_q[b]); ++t)
+        for (int64_t t = q0(p, b); t < q0(p, b) + (p->cu_q[b + 1] - p->cu_q[b]); ++t) {
+            if (t < t_lo || t >= t_hi) continue;
             for (int n2 = 0; n2 < p->n2; ++n2)
                 for (int j = 0; j < p->topk; ++j) {
                     const int64_t sel = ((int64_t)t * p->n2 + n2) * p->topk + j;
@@ -133,8 +136,15 @@ int lio_backward(const lio_problem *p, double *dq, double *dk, double *dw)
                         }
                     }
                 }
+        }
     }
     return LIO_OK;
+}
+
+/* The whole backward (every query row). */
+int lio_backward(const lio_problem *p, double *dq, double *dk, double *dw)
+{
+    return lio_backward_range(p, 0, INT64_MAX, dq, dk, dw);
 }
 
 /*

@@ -30,7 +30,8 @@ SAG_LAYOUT_TND, SAG_LAYOUT_BSND = 0, 1
 
 EXPORTED = ("sel_attn_grad_workspace_size", "sel_attn_grad", "sel_attn_grad_timed", "sel_attn_grad_ex",
             "sel_attn_grad_plan_info", "sel_attn_grad_query_error", "sel_attn_grad_status_string",
-            "sel_attn_fwd_workspace_size", "sel_attn_fwd", "sel_attn_fwd_timed", "sel_attn_fwd_ex")
+            "sel_attn_fwd_workspace_size", "sel_attn_fwd", "sel_attn_fwd_timed", "sel_attn_fwd_ex",
+            "lightning_indexer_grad_workspace_size", "lightning_indexer_grad")
 
 
 class SagDesc(ctypes.Structure):
@@ -319,3 +320,93 @@ def forward(q, k, v, topk, cu_seqlens_q, cu_seqlens_kv, scale, block_size, block
         if st != SAG_OK:
             raise SagError(st, "device")
     return o, smax, ssum
+
+
+# ------------------------------------------------------------ lightning indexer
+class SliDesc(ctypes.Structure):
+    """Mirror of ``sli_desc`` in include/selattn.h."""
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("n1", ctypes.c_int32), ("n2", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("topk", ctypes.c_int32), ("dtype", ctypes.c_int32), ("deterministic", ctypes.c_int32),
+        ("layout", ctypes.c_int32),
+        ("cu_seqlens_q", ctypes.POINTER(ctypes.c_int32)), ("cu_seqlens_kv", ctypes.POINTER(ctypes.c_int32)),
+        ("s1_max", ctypes.c_int32), ("s2_max", ctypes.c_int32),
+    ]
+
+
+class SliIo(ctypes.Structure):
+    """Mirror of ``sli_io`` in include/selattn.h (device pointers as ints)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("query", "key", "weights", "dy", "indices", "dq", "dk", "dweights")]
+
+
+def _lib_indexer():
+    lib = load()
+    if not getattr(lib, "_sli_ready", False):
+        D, IO, vp, sz = ctypes.POINTER(SliDesc), ctypes.POINTER(SliIo), ctypes.c_void_p, ctypes.c_size_t
+        lib.lightning_indexer_grad_workspace_size.argtypes = [D, ctypes.POINTER(sz)]
+        lib.lightning_indexer_grad_workspace_size.restype = ctypes.c_int
+        lib.lightning_indexer_grad.argtypes = [D, IO, vp, sz, vp]
+        lib.lightning_indexer_grad.restype = ctypes.c_int
+        lib._sli_ready = True
+    return lib
+
+
+def make_indexer_desc(cu_seqlens_q, cu_seqlens_kv, n1, n2, d, topk, dtype=SAG_BF16, deterministic=False,
+                      layout=SAG_LAYOUT_TND, s1_max=0, s2_max=0) -> SliDesc:
+    cq = (ctypes.c_int32 * len(cu_seqlens_q))(*[int(x) for x in cu_seqlens_q])
+    ck = (ctypes.c_int32 * len(cu_seqlens_kv))(*[int(x) for x in cu_seqlens_kv])
+    desc = SliDesc(batch=len(cu_seqlens_q) - 1, n1=n1, n2=n2, d=d, topk=topk, dtype=dtype,
+                   deterministic=1 if deterministic else 0, layout=int(layout),
+                   cu_seqlens_q=ctypes.cast(cq, ctypes.POINTER(ctypes.c_int32)),
+                   cu_seqlens_kv=ctypes.cast(ck, ctypes.POINTER(ctypes.c_int32)), s1_max=int(s1_max),
+                   s2_max=int(s2_max))
+    desc._keep = (cq, ck)
+    return desc
+
+
+def indexer_workspace_size(desc: SliDesc) -> int:
+    n = ctypes.c_size_t(0)
+    st = _lib_indexer().lightning_indexer_grad_workspace_size(ctypes.byref(desc), ctypes.byref(n))
+    if st != SAG_OK:
+        raise SagError(st, "lightning_indexer_grad_workspace_size")
+    return n.value
+
+
+def lightning_indexer_grad(desc: SliDesc, io: SliIo, workspace, workspace_bytes: int, stream) -> None:
+    """Phase 2 on raw device pointers (ints); raises on a non-OK status."""
+    st = _lib_indexer().lightning_indexer_grad(ctypes.byref(desc), ctypes.byref(io), workspace, workspace_bytes,
+                                               stream)
+    if st != SAG_OK:
+        raise SagError(st, "lightning_indexer_grad")
+
+
+def indexer_backward(q, k, weights, dy, indices, cu_seqlens_q, cu_seqlens_kv, deterministic=False, out=None,
+                     workspace=None, stream=None, check=False):
+    """torch-tensor convenience for the lightning-indexer backward: returns
+    (dq, dk, dweights).  TND tensors ([T, N, D]) or BSND (4-D, padded)."""
+    import torch
+    if not q.is_cuda:
+        raise ValueError("inputs must be CUDA tensors (there is no CPU path)")
+    dtype = SAG_FP16 if q.dtype == torch.float16 else SAG_BF16
+    bsnd = q.dim() == 4
+    layout = SAG_LAYOUT_BSND if bsnd else SAG_LAYOUT_TND
+    desc = make_indexer_desc(cu_seqlens_q, cu_seqlens_kv, q.shape[-2], k.shape[-2], q.shape[-1], indices.shape[-1],
+                             dtype, deterministic, layout, q.shape[1] if bsnd else 0, k.shape[1] if bsnd else 0)
+    need = indexer_workspace_size(desc)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(weights))
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    named = dict(query=q, key=k, weights=weights, dy=dy, indices=indices, dq=out[0], dk=out[1], dweights=out[2])
+    for t in named.values():
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    io = SliIo(**{k_: t.data_ptr() for k_, t in named.items()})
+    lightning_indexer_grad(desc, io, workspace.data_ptr(), need, stream.cuda_stream)
+    if check:
+        st = query_error(workspace.data_ptr(), stream.cuda_stream)
+        if st != SAG_OK:
+            raise SagError(st, "device")
+    return out

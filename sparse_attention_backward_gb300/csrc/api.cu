@@ -539,6 +539,139 @@ extern "C" sag_status sel_attn_fwd_ex(const sag_desc *desc, const sag_io *io, vo
     return SAG_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Lightning-indexer backward: validation, workspace carve, launch sequence.
+namespace {
+
+struct LiPlan {
+    Geometry g;
+    bool fp16, bsnd;
+    std::vector<int32_t> row_q, row_kv, q_end, kv_len;
+    size_t o_hdr, o_cu_q, o_cu_kv, o_q_end, o_kv_len, o_dk, o_dw, total;
+};
+
+sag_status li_plan(const sli_desc *d, LiPlan *p) {
+    if (!d || !d->cu_seqlens_q || !d->cu_seqlens_kv) return SAG_ERR_NULL;
+    if (d->dtype != SAG_BF16 && d->dtype != SAG_FP16) return SAG_ERR_DTYPE;
+    if (d->deterministic != 0 && d->deterministic != 1) return SAG_ERR_SHAPE;
+    if (d->layout != SAG_LAYOUT_TND && d->layout != SAG_LAYOUT_BSND) return SAG_ERR_SHAPE;
+    if (d->batch < 1 || d->batch > kMaxTokens) return SAG_ERR_SHAPE;
+    if (d->n1 < 1 || d->n2 < 1 || d->n1 % d->n2 != 0 || d->d < 1 || d->topk < 1 || d->topk > kMaxSeq)
+        return SAG_ERR_SHAPE;
+    const bool bsnd = d->layout == SAG_LAYOUT_BSND;
+    if (bsnd) {
+        if (d->s1_max < 1 || d->s1_max > kMaxSeq || d->s2_max < 1 || d->s2_max > kMaxSeq) return SAG_ERR_SHAPE;
+        if ((int64_t)d->batch * d->s1_max > kMaxTokens || (int64_t)d->batch * d->s2_max > kMaxTokens)
+            return SAG_ERR_SHAPE;
+    } else if (d->s1_max != 0 || d->s2_max != 0) {
+        return SAG_ERR_SHAPE;
+    }
+    const int32_t *cq = d->cu_seqlens_q, *ck = d->cu_seqlens_kv;
+    if (cq[0] != 0 || ck[0] != 0) return SAG_ERR_SHAPE;
+    for (int b = 0; b < d->batch; ++b) {
+        const int64_t s1 = (int64_t)cq[b + 1] - cq[b], s2 = (int64_t)ck[b + 1] - ck[b];
+        if (s1 < 0 || s1 > (bsnd ? d->s1_max : kMaxSeq)) return SAG_ERR_SHAPE;
+        if (s2 < d->topk || s2 > (bsnd ? d->s2_max : kMaxSeq)) return SAG_ERR_SHAPE;
+    }
+    if ((int64_t)cq[d->batch] > kMaxTokens || (int64_t)ck[d->batch] > kMaxTokens || ck[d->batch] < 1)
+        return SAG_ERR_SHAPE;
+    if (d->deterministic) return SAG_ERR_UNSUPPORTED;
+    Geometry &g = p->g;
+    g = Geometry{};
+    g.batch = d->batch;
+    g.n1 = d->n1;
+    g.n2 = d->n2;
+    g.group = d->n1 / d->n2;
+    g.d_qk = d->d;
+    g.block_count = d->topk;
+    if (!lig_tc_supported(g)) return SAG_ERR_UNSUPPORTED;
+    p->fp16 = d->dtype == SAG_FP16;
+    p->bsnd = bsnd;
+    p->row_q.assign(d->batch + 1, 0);
+    p->row_kv.assign(d->batch + 1, 0);
+    p->q_end.assign(d->batch, 0);
+    p->kv_len.assign(d->batch, 0);
+    for (int b = 0; b <= d->batch; ++b) {
+        p->row_q[b] = bsnd ? b * d->s1_max : cq[b];
+        p->row_kv[b] = bsnd ? b * d->s2_max : ck[b];
+    }
+    for (int b = 0; b < d->batch; ++b) {
+        p->q_end[b] = p->row_q[b] + (cq[b + 1] - cq[b]);
+        p->kv_len[b] = ck[b + 1] - ck[b];
+    }
+    g.t1 = p->row_q[d->batch];
+    g.t2 = p->row_kv[d->batch];
+    g.tok_hi = g.t1;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
+    p->o_hdr = take(sizeof(WsHeader));
+    p->o_cu_q = take(sizeof(int32_t) * (g.batch + 1));
+    p->o_cu_kv = take(sizeof(int32_t) * (g.batch + 1));
+    p->o_q_end = take(sizeof(int32_t) * g.batch);
+    p->o_kv_len = take(sizeof(int32_t) * g.batch);
+    p->o_dk = take(sizeof(float) * (size_t)g.t2 * g.n2 * g.d_qk);
+    p->o_dw = take(sizeof(float) * (size_t)g.t1 * g.n1);
+    p->total = o;
+    return SAG_OK;
+}
+
+}  // namespace
+
+extern "C" sag_status lightning_indexer_grad_workspace_size(const sli_desc *desc, size_t *workspace_bytes) {
+    if (!workspace_bytes) return SAG_ERR_NULL;
+    LiPlan p;
+    sag_status st = li_plan(desc, &p);
+    if (st != SAG_OK) return st;
+    *workspace_bytes = p.total;
+    return SAG_OK;
+}
+
+extern "C" sag_status lightning_indexer_grad(const sli_desc *desc, const sli_io *io, void *workspace,
+                                             size_t workspace_bytes, void *stream) {
+    LiPlan p;
+    sag_status st = li_plan(desc, &p);
+    if (st != SAG_OK) return st;
+    if (!io) return SAG_ERR_NULL;
+    const void *ptrs[] = {io->query, io->key, io->weights, io->dy, io->indices, io->dq, io->dk, io->dweights};
+    for (const void *x : ptrs)
+        if (!x) return SAG_ERR_NULL;
+    if (!workspace) return SAG_ERR_WORKSPACE;
+    for (const void *x : ptrs)
+        if (!aligned16(x)) return SAG_ERR_ALIGN;
+    if (!aligned16(workspace)) return SAG_ERR_ALIGN;
+    if (workspace_bytes < p.total) return SAG_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DeviceGuard dg;
+    if (!dg.bind(s)) return SAG_ERR_CUDA;
+    const Geometry &g = p.g;
+    char *base = static_cast<char *>(workspace);
+    Workspace ws{};
+    ws.hdr = reinterpret_cast<WsHeader *>(base + p.o_hdr);
+    ws.cu_q = reinterpret_cast<int32_t *>(base + p.o_cu_q);
+    ws.cu_kv = reinterpret_cast<int32_t *>(base + p.o_cu_kv);
+    ws.q_end = reinterpret_cast<int32_t *>(base + p.o_q_end);
+    ws.kv_blocks = reinterpret_cast<int32_t *>(base + p.o_kv_len);
+    ws.dq_acc = reinterpret_cast<float *>(base + p.o_dk);
+    ws.dkv_acc = reinterpret_cast<float *>(base + p.o_dw);
+    std::vector<char> meta(p.o_dk - p.o_cu_q, 0);
+    auto put = [&](size_t off, const void *src, size_t bytes) { memcpy(meta.data() + (off - p.o_cu_q), src, bytes); };
+    put(p.o_cu_q, p.row_q.data(), sizeof(int32_t) * (g.batch + 1));
+    put(p.o_cu_kv, p.row_kv.data(), sizeof(int32_t) * (g.batch + 1));
+    put(p.o_q_end, p.q_end.data(), sizeof(int32_t) * g.batch);
+    put(p.o_kv_len, p.kv_len.data(), sizeof(int32_t) * g.batch);
+    if (cudaMemsetAsync(base + p.o_hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return SAG_ERR_CUDA;
+    if (cudaMemcpyAsync(base + p.o_cu_q, meta.data(), meta.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return SAG_ERR_CUDA;
+    // both fp32 accumulators are adjacent: one memset
+    if (cudaMemsetAsync(base + p.o_dk, 0, p.total - p.o_dk, s) != cudaSuccess) return SAG_ERR_CUDA;
+    // padding rows (BSND) of dq get no unit: zero them with the rest
+    const int es = 2;
+    if (p.bsnd && cudaMemsetAsync(io->dq, 0, (size_t)g.t1 * g.n1 * g.d_qk * es, s) != cudaSuccess)
+        return SAG_ERR_CUDA;
+    if (launch_lig(g, ws, *io, p.fp16, s, device_sms()) != cudaSuccess) return SAG_ERR_CUDA;
+    return SAG_OK;
+}
+
 extern "C" sag_status sel_attn_grad_query_error(const void *workspace, void *stream) {
     if (!workspace) return SAG_ERR_NULL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -64,6 +64,14 @@ cudaError_t launch_fwd_finalize(const Geometry &g, const Workspace &ws, void *o,
 cudaError_t launch_dq_from_ds(const Geometry &g, const Workspace &ws, const sag_io &io, bool fp16, cudaStream_t s,
                               int num_sms);
 
+// Lightning-indexer backward (tensor cores): head dim 128, G = n1 / n2 <= 64.
+// Geometry: t1 / t2 rows, n1, n2, group, block_count = topk; Workspace: hdr,
+// cu_q / cu_kv row starts, q_end, kv_blocks = valid key rows of each batch,
+// dq_acc = fp32 dK accumulator [t2 * n2, 128], dkv_acc = fp32 dW accumulator.
+bool lig_tc_supported(const Geometry &g);
+cudaError_t launch_lig(const Geometry &g, const Workspace &ws, const sli_io &io, bool fp16, cudaStream_t s,
+                       int num_sms);
+
 // Element (row, col) of a [rows, d_qk] gradient whose columns from d_qk -
 // d_rope on live in a separate [rows, d_rope] tensor (the rope split).
 __device__ __forceinline__ uint16_t *split_col(uint16_t *main, uint16_t *rope, int64_t row, int col, int d_qk,

@@ -1,0 +1,488 @@
+// Lightning-indexer backward on tensor cores ("aclnnLightningIndexerGrad",
+// formula section):
+//     S  = Relu(Matmul(Query, Gather(Key, Indices)))
+//     Y  = Dy * Weights,  R = ReluGrad(Y, S) = Y where S > 0, else 0
+//     dW = Reduce(S * dy),  dQ = Matmul(R, Gather(Key, Indices)),
+//     dK = ScatterAdd(Matmul(R^T, Q), Indices)
+// for query head h of key head n2 = h / G:  S[t,h,j] = relu(<q[t,h], k[idx[t,n2,j]]>),
+// R[t,h,j] = dy[t,n2,j] * w[t,h] * [S > 0].
+//
+// Work unit: one (query token t, key head n2) and its topk selections, taken
+// in chunks of 128 gathered key rows.  Per chunk (heads padded to 64):
+//     S^T  = Kc Q^T       (M = 128 keys, N = 64 heads, K = d)     -> TMEM
+//     R    from S^T, dy, w  (CUDA cores, thread = key = TMEM lane) -> shared
+//     dQ^T += Kc^T R      (M = d dims, N = 64 heads, K = 128 keys) TMEM, per unit
+//     dKc  = R Q          (M = 128 keys, N = d dims, K = 64 heads)   -> TMEM
+// dKc is scatter-added (fp32 reductions) into a workspace accumulator at the
+// gathered key rows; dQ is stored once per unit (a unit owns its rows); dW is
+// reduced over the chunk's keys with warp butterflies.
+//
+// Warp roles (320 threads): 0 TMA producer (query rows, key rows by
+// tile::gather4, the unit's weights), 1 MMA issuer and TMEM owner, 2-5 relu /
+// dW (thread = key; dW partials added into an fp32 row with atomics),
+// 6-9 epilogue (dK reductions, dQ stores).  Every wait is bounded and there
+// is no block-level barrier between the roles.
+#include "kernels.cuh"
+#include "tc.cuh"
+#include "tile.cuh"
+#include "tmap.cuh"
+
+namespace sag {
+namespace {
+
+constexpr int kLiD = 128;            // head dim
+constexpr int kLiChunk = 128;        // gathered keys per chunk (MMA M)
+constexpr int kLiHeads = 64;         // heads per unit, padded (MMA N)
+constexpr int kLiThreads = 320;
+
+// TMEM columns: S^T stages, dK stages, dQ^T buffers (512 allocated)
+constexpr uint32_t kLiColS = 0, kLiColDK = 128, kLiColDQ = 384;
+
+struct LiSmem {
+    static constexpr int K_STAGE = 2 * kLiChunk * 128;     // 2 chunks of 64 dims x 128 rows
+    static constexpr int Q_STAGE = 2 * kLiHeads * 128;     // 2 chunks of 64 dims x 64 head rows
+    static constexpr int R_STAGE = kLiChunk * 128;         // 128 key rows x 64 heads (bf16)
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_Q = OFF_K + 2 * K_STAGE;
+    static constexpr int OFF_R = OFF_Q + 2 * Q_STAGE;
+    static constexpr int OFF_STG = OFF_R + 2 * R_STAGE;      // 4 epilogue warps x 4 KB
+    static constexpr int OFF_W = OFF_STG + 16384;            // 2 x 64 weights (fp32), by query stage
+    static constexpr int OFF_BAR = OFF_W + 2 * kLiHeads * 4;
+    static constexpr int TOTAL = OFF_BAR + 256 + 1024;
+};
+
+enum LiBar {
+    L_Q_FULL0 = 0, L_Q_FULL1, L_Q_EMPTY0, L_Q_EMPTY1, L_K_FULL0, L_K_FULL1, L_K_EMPTY0, L_K_EMPTY1,
+    L_S_FULL0, L_S_FULL1, L_R_FULL0, L_R_FULL1, L_DK_FULL0, L_DK_FULL1, L_DK_FREE0, L_DK_FREE1,
+    L_DQ_FULL0, L_DQ_FULL1, L_DQ_FREE0, L_DQ_FREE1, L_DRAIN, L_COUNT
+};
+
+struct LiArgs {
+    Geometry g;            // batch, t1, t2, n1, n2, group; block_count = topk
+    Workspace ws;          // hdr, cu_q / cu_kv (row starts), q_end, kv_blocks = valid key rows,
+                           // dq_acc = fp32 dK accumulator, dkv_acc = fp32 dW accumulator
+    const int32_t *idx;    // [T1, n2, topk]
+    const float *dy;       // [T1, n2, topk]
+    const uint16_t *w;     // [T1, n1]
+    uint16_t *dq;          // [T1, n1, d]
+    int64_t n_units;       // T1 * n2
+    int nchunks;           // ceil(topk / 128)
+};
+
+// Key row (of the [T2 * n2] rows of the key map) of selection j of unit
+// (t, n2), or -1 for an empty slot, a slot past topk, or an id out of range
+// (reported).
+__device__ __forceinline__ int64_t li_key_row(const LiArgs &A, int t, int n2, int b, int j, bool report) {
+    if (j >= A.g.block_count) return -1;
+    const int id = __ldg(A.idx + ((int64_t)t * A.g.n2 + n2) * A.g.block_count + j);
+    if (id == -1) return -1;
+    const int s2 = A.ws.kv_blocks[b];                 // valid key rows of the batch
+    if (id < 0 || id >= s2) {
+        if (report) raise_error(&A.ws.hdr->error, SAG_ERR_INDEX);
+        return -1;
+    }
+    return ((int64_t)A.ws.cu_kv[b] + id) * A.g.n2 + n2;
+}
+
+template <bool kFp16>
+__global__ void __launch_bounds__(kLiThreads, 1)
+    k_lig_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, LiArgs A) {
+    using L = LiSmem;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_BAR + 8 * L_COUNT);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_BAR + 8 * L_COUNT + 4);
+    float *wbuf = reinterpret_cast<float *>(smem + L::OFF_W);
+    const Geometry &g = A.g;
+    const Workspace &ws = A.ws;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = g.group;
+    const uint32_t sbase = tc::smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int i = 0; i < L_COUNT; ++i) {
+            const bool from_threads = i == L_R_FULL0 || i == L_R_FULL1 || i == L_DK_FREE0 || i == L_DK_FREE1 ||
+                                      i == L_DQ_FREE0 || i == L_DQ_FREE1;
+            tc::mbar_init(&bars[i], from_threads ? 128 : 1);
+        }
+        tc::fence_mbar_init();
+    }
+    // head rows G..63 of the query stages are never loaded: they stay zero, so
+    // the padded heads give S = 0 and R = 0
+    if (G < kLiHeads) {
+        for (int i = threadIdx.x; i < 2 * L::Q_STAGE / 16; i += kLiThreads)
+            reinterpret_cast<uint4 *>(smem + L::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
+        tc::fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        raise_error(&ws.hdr->error, SAG_ERR_TIMEOUT);
+    };
+    // unit -> (token, key head, batch); padding tokens (BSND) are skipped by every role
+    auto unit = [&](int64_t u, int &t, int &n2, int &b) {
+        t = (int)(u / g.n2);
+        n2 = (int)(u % g.n2);
+        b = batch_of(ws.cu_q, g.batch, t);
+        return t < ws.q_end[b];
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tc::prefetch_tmap(&map_q);
+            tc::prefetch_tmap(&map_k);
+        }
+        int uu = 0, kc = 0;
+        uint32_t armed_q[2] = {0, 0}, armed_k[2] = {0, 0};
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < A.n_units && ok; u += gridDim.x) {
+            int t, n2, b;
+            if (!unit(u, t, n2, b)) continue;
+            const int qs = uu & 1;
+            if (uu >= 2 && !tc::mbar_wait(&bars[L_Q_EMPTY0 + qs], ((uu >> 1) - 1) & 1, abort_flag, kWaitNs)) {
+                ok = false;
+                break;
+            }
+            // the unit's weights (0 past G) for the relu warps; the arrive below
+            // publishes them with the query tile
+            for (int h = lane; h < kLiHeads; h += 32)
+                wbuf[qs * kLiHeads + h] = h < G ? u16_to_f<kFp16>(A.w[(int64_t)t * g.n1 + n2 * G + h]) : 0.f;
+            __syncwarp();
+            ++armed_q[qs];
+            if (lane == 0) {
+                tc::mbar_arrive_expect_tx(&bars[L_Q_FULL0 + qs], (uint32_t)G * kLiD * 2);
+                for (int c = 0; c < 2; ++c)
+                    tc::tma_load_2d(smem + L::OFF_Q + qs * L::Q_STAGE + c * (L::Q_STAGE / 2), &map_q, c * 64,
+                                    t * g.n1 + n2 * G, &bars[L_Q_FULL0 + qs]);
+            }
+            // an empty or bad slot fetches the batch's first key row (its R is 0)
+            const int64_t row0 = (int64_t)ws.cu_kv[b] * g.n2 + n2;
+            for (int c = 0; c < A.nchunks; ++c, ++kc) {
+                const int ks = kc & 1;
+                if (kc >= 2 && !tc::mbar_wait(&bars[L_K_EMPTY0 + ks], ((kc >> 1) - 1) & 1, abort_flag, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                int y[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int64_t r = li_key_row(A, t, n2, b, c * kLiChunk + 4 * lane + e, false);
+                    y[e] = (int)(r >= 0 ? r : row0);
+                }
+                ++armed_k[ks];
+                if (lane == 0) tc::mbar_arrive_expect_tx(&bars[L_K_FULL0 + ks], (uint32_t)kLiChunk * kLiD * 2);
+                __syncwarp();
+                uint8_t *kdst = smem + L::OFF_K + ks * L::K_STAGE;
+                for (int h = 0; h < 2; ++h)
+                    tc::tma_gather4(kdst + h * (L::K_STAGE / 2) + lane * 512, &map_k, h * 64, y[0], y[1], y[2], y[3],
+                                    &bars[L_K_FULL0 + ks]);
+            }
+            ++uu;
+        }
+        if (!ok) fail();
+        bool drained = true;
+        for (int i = 0; i < 2; ++i)
+            drained = tc::drain_armed(&bars[L_Q_FULL0 + i], armed_q[i], kWaitNs) &&
+                      tc::drain_armed(&bars[L_K_FULL0 + i], armed_k[i], kWaitNs) && drained;
+        if (!drained) fail();
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const bool bf16 = !kFp16;
+            const uint32_t id_s = tc::idesc_f16(kLiChunk, kLiHeads, bf16, false, false);   // S^T = Kc Q^T
+            const uint32_t id_q = tc::idesc_f16(kLiD, kLiHeads, bf16, true, true);         // dQ^T += Kc^T R
+            const uint32_t id_k = tc::idesc_f16(kLiChunk, kLiD, bf16, false, true);        // dKc = R Q
+            struct Prev { int kc, qs, dqb, uu; bool first, last; };
+            Prev pv{};
+            bool have = false, ok = true;
+            int uu = 0, kc = 0;
+            // the dQ / dK MMAs of chunk p once its R is in shared memory
+            auto back = [&](const Prev &p) -> bool {
+                const int rs = p.kc & 1;
+                if (!tc::mbar_wait(&bars[L_R_FULL0 + rs], (p.kc >> 1) & 1, abort_flag, kWaitNs)) return false;
+                if (p.first && p.uu >= 2 &&
+                    !tc::mbar_wait(&bars[L_DQ_FREE0 + p.dqb], ((p.uu >> 1) - 1) & 1, abort_flag, kWaitNs))
+                    return false;
+                if (p.kc >= 2 && !tc::mbar_wait(&bars[L_DK_FREE0 + rs], ((p.kc >> 1) - 1) & 1, abort_flag, kWaitNs))
+                    return false;
+                tc::tc_fence_after();
+                const uint32_t ks = sbase + L::OFF_K + rs * L::K_STAGE;
+                const uint32_t qs = sbase + L::OFF_Q + p.qs * L::Q_STAGE;
+                const uint32_t rr = sbase + L::OFF_R + rs * L::R_STAGE;
+                // dQ^T += Kc^T R: A = key tile MN-major (dims x keys), B = R MN-major (heads x keys)
+                for (int kk = 0; kk < kLiChunk / 16; ++kk)
+                    tc::mma_f16_ss(tmem + kLiColDQ + p.dqb * kLiHeads, tc::sw128_desc(ks + kk * 2048, L::K_STAGE / 2, 1024),
+                                   tc::sw128_desc(rr + kk * 2048, L::R_STAGE, 1024), id_q, (!p.first) || (kk > 0));
+                // dKc = R Q: A = R K-major (keys x heads), B = query tile MN-major (dims x heads)
+                for (int kk = 0; kk < kLiHeads / 16; ++kk)
+                    tc::mma_f16_ss(tmem + kLiColDK + rs * kLiD, tc::sw128_desc(rr + kk * 32, 16, 1024),
+                                   tc::sw128_desc(qs + kk * 2048, L::Q_STAGE / 2, 1024), id_k, kk > 0);
+                tc::mma_commit(&bars[L_DK_FULL0 + rs]);
+                tc::mma_commit(&bars[L_K_EMPTY0 + rs]);      // key tile and R stage free
+                if (p.last) {
+                    tc::mma_commit(&bars[L_DQ_FULL0 + p.dqb]);
+                    tc::mma_commit(&bars[L_Q_EMPTY0 + p.qs]);
+                }
+                return true;
+            };
+            for (int64_t u = blockIdx.x; u < A.n_units && ok; u += gridDim.x) {
+                int t, n2, b;
+                if (!unit(u, t, n2, b)) continue;
+                const int qs = uu & 1;
+                if (!tc::mbar_wait(&bars[L_Q_FULL0 + qs], (uu >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                for (int c = 0; c < A.nchunks; ++c, ++kc) {
+                    const int ks = kc & 1;
+                    if (!tc::mbar_wait(&bars[L_K_FULL0 + ks], (kc >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t kt = sbase + L::OFF_K + ks * L::K_STAGE;
+                    const uint32_t qt = sbase + L::OFF_Q + qs * L::Q_STAGE;
+                    // S^T = Kc Q^T (both operands K-major)
+                    for (int kk = 0; kk < kLiD / 16; ++kk)
+                        tc::mma_f16_ss(tmem + kLiColS + ks * kLiHeads,
+                                       tc::sw128_desc(kt + (kk >> 2) * (L::K_STAGE / 2) + (kk & 3) * 32, 16, 1024),
+                                       tc::sw128_desc(qt + (kk >> 2) * (L::Q_STAGE / 2) + (kk & 3) * 32, 16, 1024), id_s,
+                                       kk > 0);
+                    tc::mma_commit(&bars[L_S_FULL0 + ks]);
+                    if (have && !back(pv)) { ok = false; break; }
+                    pv = Prev{kc, qs, uu & 1, uu, c == 0, c == A.nchunks - 1};
+                    have = true;
+                }
+                ++uu;
+            }
+            if (ok && have && !back(pv)) ok = false;
+            if (!ok) fail();
+            tc::mma_commit(&bars[L_DRAIN]);
+            if (!tc::mbar_wait_drain(&bars[L_DRAIN], 0, kWaitNs)) fail();
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------ relu / dW
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;                        // key of the chunk = TMEM lane
+        const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+        int uu = 0, kc = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < A.n_units && ok; u += gridDim.x) {
+            int t, n2, b;
+            if (!unit(u, t, n2, b)) continue;
+            // the weights come with the query tile (stage = unit parity)
+            ok = tc::mbar_wait(&bars[L_Q_FULL0 + (uu & 1)], (uu >> 1) & 1, abort_flag, kWaitNs);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            const float *wv = wbuf + (uu & 1) * kLiHeads;
+            float dw0 = 0.f, dw1 = 0.f;                      // this lane's two heads (see below)
+            for (int c = 0; c < A.nchunks; ++c, ++kc) {
+                const int ks = kc & 1;
+                const int j = c * kLiChunk + r;
+                const bool valid = li_key_row(A, t, n2, b, j, true) >= 0;
+                const float dyv = valid ? A.dy[((int64_t)t * g.n2 + n2) * g.block_count + j] : 0.f;
+                ok = tc::mbar_wait(&bars[L_S_FULL0 + ks], (kc >> 1) & 1, abort_flag, kWaitNs);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc::tc_fence_after();
+                float v[kLiHeads];                           // relu(S) * dy, reduced below
+                uint32_t pk[kLiHeads / 2];
+#pragma unroll
+                for (int h0 = 0; h0 < kLiHeads; h0 += 32) {
+                    uint32_t sv[4][8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) tc::tmem_ld8(trow + kLiColS + ks * kLiHeads + h0 + 8 * i, sv[i]);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            const int h = h0 + 8 * i + e;
+                            const float x0 = __uint_as_float(sv[i][e]), x1 = __uint_as_float(sv[i][e + 1]);
+                            v[h] = fmaxf(x0, 0.f) * dyv;
+                            v[h + 1] = fmaxf(x1, 0.f) * dyv;
+                            const float r0 = x0 > 0.f ? dyv * wv[h] : 0.f;
+                            const float r1 = x1 > 0.f ? dyv * wv[h + 1] : 0.f;
+                            pk[h / 2] = pack2<kFp16>(r0, r1);
+                        }
+                }
+                // R row of this key into the chunk's R stage (128-byte swizzled rows)
+                uint8_t *rrow = smem + L::OFF_R + ks * L::R_STAGE;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc)
+                    *reinterpret_cast<uint4 *>(rrow + sw_off(r, cc)) =
+                        make_uint4(pk[cc * 4], pk[cc * 4 + 1], pk[cc * 4 + 2], pk[cc * 4 + 3]);
+                tc::fence_proxy_async_smem();
+                tc::tc_fence_before();
+                tc::mbar_arrive(&bars[L_R_FULL0 + ks]);
+                // dW over the warp's 32 keys: each step trades half of the
+                // values with the partner lane (the upper half of the heads goes
+                // to the lane with the step's bit set) and adds; after 5 steps
+                // lane l holds heads 2 l and 2 l + 1 summed over all 32 lanes
+#pragma unroll
+                for (int step = 0; step < 5; ++step) {
+                    const int off = 16 >> step, half = 32 >> step;
+                    const bool upper = (lane & off) != 0;
+#pragma unroll
+                    for (int i = 0; i < half; ++i) {
+                        const float send = upper ? v[i] : v[i + half];
+                        const float keep = upper ? v[i + half] : v[i];
+                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    }
+                }
+                dw0 += v[0];
+                dw1 += v[1];
+            }
+            if (!ok) break;
+            // lane l holds heads 2 l and 2 l + 1 summed over its warp's keys
+            float *dwa = ws.dkv_acc + (int64_t)t * g.n1 + n2 * G;
+            if (2 * lane < G) atomicAdd(dwa + 2 * lane, dw0);
+            if (2 * lane + 1 < G) atomicAdd(dwa + 2 * lane + 1, dw1);
+            ++uu;
+        }
+        if (!ok) fail();
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;                        // key of the chunk / head dim = TMEM lane
+        const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+        uint8_t *stg = smem + L::OFF_STG + (warp - 6) * 4096;
+        float *acc = ws.dq_acc;                              // fp32 dK [T2 * n2, d]
+        int uu = 0, kc = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < A.n_units && ok; u += gridDim.x) {
+            int t, n2, b;
+            if (!unit(u, t, n2, b)) continue;
+            for (int c = 0; c < A.nchunks; ++c, ++kc) {
+                const int ks = kc & 1;
+                const int64_t krow = li_key_row(A, t, n2, b, c * kLiChunk + r, false);
+                ok = tc::mbar_wait(&bars[L_DK_FULL0 + ks], (kc >> 1) & 1, abort_flag, kWaitNs);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc::tc_fence_after();
+                for (int c32 = 0; c32 < kLiD / 32; ++c32) {
+                    uint32_t v0[16], v1[16];
+                    tc::tmem_ld16(trow + kLiColDK + ks * kLiD + c32 * 32, v0);
+                    tc::tmem_ld16(trow + kLiColDK + ks * kLiD + c32 * 32 + 16, v1);
+                    tc::tmem_wait_ld();
+                    // stage the warp's 32 keys x 32 dims, then reduce whole 128-byte row segments
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4)
+                        *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j4 ^ (lane & 7)) << 4)) =
+                            make_uint4(v0[4 * j4], v0[4 * j4 + 1], v0[4 * j4 + 2], v0[4 * j4 + 3]);
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4)
+                        *reinterpret_cast<uint4 *>(stg + lane * 128 + (((j4 + 4) ^ (lane & 7)) << 4)) =
+                            make_uint4(v1[4 * j4], v1[4 * j4 + 1], v1[4 * j4 + 2], v1[4 * j4 + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int kq = 0; kq < 8; ++kq) {
+                        const int rr = kq * 4 + (lane >> 3), j4 = lane & 7;
+                        const int64_t kr = __shfl_sync(0xffffffffu, krow, rr);
+                        const float4 x = *reinterpret_cast<const float4 *>(stg + rr * 128 + ((j4 ^ (rr & 7)) << 4));
+                        if (kr >= 0) tc::red_add_v4(acc + kr * kLiD + c32 * 32 + j4 * 4, x.x, x.y, x.z, x.w);
+                    }
+                    __syncwarp();
+                }
+                tc::tc_fence_before();
+                tc::mbar_arrive(&bars[L_DK_FREE0 + ks]);
+            }
+            if (!ok) break;
+            // dQ of the unit: lane = head dim, columns = heads
+            const int dqb = uu & 1;
+            ok = tc::mbar_wait(&bars[L_DQ_FULL0 + dqb], (uu >> 1) & 1, abort_flag, kWaitNs);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc::tc_fence_after();
+            for (int h0 = 0; h0 < kLiHeads; h0 += 16) {
+                if (h0 >= G) break;
+                uint32_t v[16];
+                tc::tmem_ld16(trow + kLiColDQ + dqb * kLiHeads + h0, v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (h0 + i < G)
+                        A.dq[((int64_t)t * g.n1 + n2 * G + h0 + i) * kLiD + r] = f_to_u16<kFp16>(__uint_as_float(v[i]));
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&bars[L_DQ_FREE0 + dqb]);
+            ++uu;
+        }
+        if (!ok) fail();
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// fp32 dK accumulator -> 16-bit dk
+template <bool kFp16>
+__global__ void __launch_bounds__(256) k_lig_cast(const float *__restrict__ in, uint16_t *__restrict__ out, int64_t n4) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 v = reinterpret_cast<const float4 *>(in)[i];
+        ushort4 o;
+        o.x = f_to_u16<kFp16>(v.x);
+        o.y = f_to_u16<kFp16>(v.y);
+        o.z = f_to_u16<kFp16>(v.z);
+        o.w = f_to_u16<kFp16>(v.w);
+        reinterpret_cast<ushort4 *>(out)[i] = o;
+    }
+}
+
+template <bool kFp16>
+__global__ void __launch_bounds__(256) k_lig_cast1(const float *__restrict__ in, uint16_t *__restrict__ out, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = f_to_u16<kFp16>(in[i]);
+}
+
+template <bool kFp16>
+cudaError_t launch_lig_t(const Geometry &g, const Workspace &ws, const sli_io &io, cudaStream_t s, int num_sms) {
+    LiArgs a;
+    a.g = g;
+    a.ws = ws;
+    a.idx = io.indices;
+    a.dy = io.dy;
+    a.w = (const uint16_t *)io.weights;
+    a.dq = (uint16_t *)io.dq;
+    a.n_units = (int64_t)g.t1 * g.n2;
+    a.nchunks = (g.block_count + kLiChunk - 1) / kLiChunk;
+    CUtensorMap mq, mk;
+    if (!tmap_2d(&mq, io.query, kFp16, kLiD, (uint64_t)g.t1 * g.n1, g.group) ||
+        !tmap_2d(&mk, io.key, kFp16, kLiD, (uint64_t)g.t2 * g.n2, 1))
+        return cudaErrorInvalidValue;
+    auto fn = k_lig_tc<kFp16>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, LiSmem::TOTAL);
+    if (e != cudaSuccess) return e;
+    int64_t grid = a.n_units < num_sms ? a.n_units : num_sms;
+    if (grid < 1) grid = 1;
+    fn<<<(int)grid, kLiThreads, LiSmem::TOTAL, s>>>(mq, mk, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    auto cast = [&](const float *in, void *out, int64_t n) {
+        const int64_t n4 = n / 4;
+        int64_t cg = (n4 + 255) / 256;
+        if (cg > (int64_t)num_sms * 8) cg = (int64_t)num_sms * 8;
+        if (cg > 0) k_lig_cast<kFp16><<<(int)cg, 256, 0, s>>>(in, (uint16_t *)out, n4);
+    };
+    cast(ws.dq_acc, io.dk, (int64_t)g.t2 * g.n2 * kLiD);
+    const int64_t nw = (int64_t)g.t1 * g.n1;
+    int64_t cw = (nw + 255) / 256;
+    if (cw > (int64_t)num_sms * 8) cw = (int64_t)num_sms * 8;
+    if (cw > 0) k_lig_cast1<kFp16><<<(int)cw, 256, 0, s>>>(ws.dkv_acc, (uint16_t *)io.dweights, nw);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool lig_tc_supported(const Geometry &g) { return g.d_qk == kLiD && g.group >= 1 && g.group <= kLiHeads; }
+
+cudaError_t launch_lig(const Geometry &g, const Workspace &ws, const sli_io &io, bool fp16, cudaStream_t s,
+                       int num_sms) {
+    if (!lig_tc_supported(g)) return cudaErrorInvalidValue;
+    return fp16 ? launch_lig_t<true>(g, ws, io, s, num_sms) : launch_lig_t<false>(g, ws, io, s, num_sms);
+}
+
+}  // namespace sag

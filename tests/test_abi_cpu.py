@@ -26,7 +26,7 @@ def _declared():
     names = set()
     for h in hdrs:
         txt = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        names |= set(re.findall(r"\b(sel_attn_\w*)\s*\(", txt))
+        names |= set(re.findall(r"\b((?:sel_attn|lightning_indexer)_\w*)\s*\(", txt))
     return names
 
 
@@ -236,3 +236,27 @@ def test_dq_path_of_the_plan(lib, monkeypatch):
     d = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale)
     info = sab.plan_info(d)
     assert info.dq_path == 1 and info.token_chunks == 1 and info.launches == 9
+
+
+
+def _li_status(**kw):
+    import ctypes
+    a = dict(cu_seqlens_q=[0, 300, 1000], cu_seqlens_kv=[0, 300, 1000], n1=32, n2=1, d=128, topk=128)
+    a.update(kw)
+    d = sab.make_indexer_desc(**a)
+    n = ctypes.c_size_t(0)
+    return sab._lib_indexer().lightning_indexer_grad_workspace_size(ctypes.byref(d), ctypes.byref(n)), n.value
+
+
+def test_indexer_descriptor_validation(lib):
+    st, n = _li_status()
+    # header + row starts / ends + fp32 dK [1000, 1, 128] + fp32 dW [1000, 32], 256-byte aligned
+    assert st == sab.SAG_OK and n >= 1000 * 128 * 4 + 1000 * 32 * 4
+    assert _li_status(topk=301)[0] == G                                # a batch shorter than topk
+    assert _li_status(n1=30, n2=4)[0] == G                             # n1 not a multiple of n2
+    assert _li_status(n1=128)[0] == sab.SAG_ERR_UNSUPPORTED            # G = 128 > 64
+    assert _li_status(d=64)[0] == sab.SAG_ERR_UNSUPPORTED
+    assert _li_status(deterministic=True)[0] == sab.SAG_ERR_UNSUPPORTED
+    assert _li_status(layout=sab.SAG_LAYOUT_BSND, s1_max=700, s2_max=700)[0] == sab.SAG_OK
+    assert _li_status(layout=sab.SAG_LAYOUT_BSND, s1_max=699, s2_max=700)[0] == G
+    assert _li_status(s1_max=700)[0] == G

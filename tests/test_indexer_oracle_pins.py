@@ -112,6 +112,15 @@ def test_row_entry_points_match_the_full_backward():
     np.testing.assert_array_equal(li.k_rows(p, rows, heads), dk[rows, heads])
 
 
+def test_token_ranges_sum_to_the_full_backward():
+    rng = np.random.default_rng(6)
+    p = _problem(rng, dup=True, empty=True)
+    full = li.backward(p)
+    parts = [li.backward_range(p, a, b) for a, b in ((0, 3), (3, 7), (7, p.t1))]
+    for i in range(3):
+        np.testing.assert_allclose(sum(x[i] for x in parts), full[i], rtol=1e-13, atol=1e-13)
+
+
 def test_bsnd_is_the_packed_problem_and_bad_ids_fail():
     rng = np.random.default_rng(5)
     p = _problem(rng, lens_q=(5, 0, 4), lens_kv=(20, 8, 12))
