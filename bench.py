@@ -55,6 +55,10 @@ def parse():
                     help="time the selected-attention forward (O and the softmax stats) instead")
     ap.add_argument("--seq", type=int, default=0,
                     help="override every batch's query and key length (smaller profiling captures)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload timings added to the line (long context, max selection, small group)")
+    ap.add_argument("--op", choices=["backward", "indexer"], default="backward",
+                    help="indexer: the lightning-indexer backward on its long workload instead")
     return ap.parse_args()
 
 
@@ -287,6 +291,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.op == "indexer":
+        run_indexer(args, world, rank, local)
+        return
     w = synth.WORKLOADS[args.config]
     if args.seq:
         cu = tuple(args.seq * i for i in range(w.batch + 1))
@@ -403,6 +410,13 @@ def main():
                "sample": f"{n} query tokens x {w.group} heads (KV head 0, batch 0), full backward of those "
                          f"rows, {dt:.1f} s on one core of {host_cpu()} ({os.cpu_count()} cores)"}
 
+    # the other large workloads, both modes, after this run's tensors are freed
+    workloads = None
+    if rank == 0 and world == 1 and not args.no_workloads and not args.seq and args.config == 2:
+        del x, ins, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+        workloads = time_workloads(dev, stream, peak)
+
     if rank == 0:
         traffic = profiled_traffic(w.name, args.deterministic)
         line = {
@@ -420,10 +434,64 @@ def main():
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(info.launches) * K,
             "clocks": clk,
+            "workloads": workloads,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def time_workloads(dev, stream, peak):
+    """ms per call (CUDA events, after warm-up; inputs beyond L2) of the
+    long-context, max-selection and small-group workloads in both modes, with
+    TFLOP/s and the fraction of the bf16 burst peak; the main kernel alone in
+    parentheses (`main_ms`).  Attention outputs and stats from the library's
+    forward."""
+    import sparse_attention_backward_gb300 as sab
+    out = {}
+    for idx, reps in ((2, 10), (3, 2), (4, 10)):
+        w = synth.WORKLOADS[idx]
+        x = synth.make_inputs(w, device=dev)
+        o, m, l = sab.forward(x["q"], x["k"], x["v"], x["topk"], w.cu_q, w.cu_kv, w.scale, w.block_size,
+                              w.block_count, check=True)
+        ins = [x["q"], x["k"], x["v"], o, x["dy"], m, l, x["topk"]]
+        outs = [torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])]
+        for det in (False, True):
+            desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
+                                 sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, det)
+            need = sab.workspace_size(desc)
+            ws = torch.empty(need, dtype=torch.uint8, device=dev)
+            e0 = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+            e1 = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+            for e in e0 + e1:
+                e.record(stream)
+
+            def call(a=None, b=None):
+                sab.sel_attn_grad(desc, *[t.data_ptr() for t in ins], *[t.data_ptr() for t in outs], ws.data_ptr(),
+                                  need, stream.cuda_stream, a.cuda_event if a is not None else None,
+                                  b.cuda_event if b is not None else None)
+            call()
+            call()
+            st = sab.query_error(ws.data_ptr(), stream.cuda_stream)
+            if st != sab.SAG_OK:
+                raise sab.SagError(st, "device")
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            t0.record(stream)
+            for i in range(reps):
+                call(e0[i], e1[i])
+            t1.record(stream)
+            torch.cuda.synchronize()
+            ms = t0.elapsed_time(t1) / reps
+            main_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(e0, e1))
+            tf = w.flops() / (ms * 1e-3) / 1e12
+            out[f"{w.name}:{'deterministic' if det else 'default'}"] = {
+                "ms": ms, "main_ms": main_ms, "tflops": tf, "frac": tf / peak,
+                "main_frac": w.flops() / (main_ms * 1e-3) / 1e12 / peak, "calls": reps}
+            del ws
+        del x, o, m, l, ins, outs
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_forward(args, w, x, dev, stream, world, rank, local):
@@ -520,6 +588,153 @@ def run_forward(args, w, x, dev, stream, world, rank, local):
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 10 * K, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_indexer(args, world, rank, local):
+    """The lightning-indexer backward on its long workload (8192 tokens, 64
+    query heads on one key head, head dim 128, 2048 selections per token):
+    one call per step (row starts staged, accumulators zeroed, the tensor-core
+    kernel, two casts); flops = 3 contractions x 2 * d per (query head,
+    selection)."""
+    import oracle.indexer as li
+    import sparse_attention_backward_gb300 as sab
+    w = synth.INDEXER_WORKLOADS[2 if args.config == 2 else args.config]
+    if args.seq:
+        cu = tuple(args.seq * i for i in range(w.batch + 1))
+        w = w.with_(name=f"{w.name}_seq{args.seq}", cu_q=cu, cu_kv=cu)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        x = synth.make_indexer_inputs(w, device="cpu")
+    else:
+        sab.load()
+        torch.cuda.set_device(local)
+        dev = torch.device("cuda", local)
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl", device_id=dev)
+        x = synth.make_indexer_inputs(w, device=dev, seed=w.seed + rank)
+    flops = w.flops()
+
+    def oracle_rate(budget_s, seed=0):
+        rng = np.random.default_rng(seed)
+        xs = {k: v.cpu() for k, v in x.items()}
+        p = li.Problem(cu_q=np.asarray(w.cu_q, np.int32), cu_kv=np.asarray(w.cu_kv, np.int32), n1=w.n1, n2=w.n2,
+                       d=w.d, topk=w.topk, idx=xs["idx"].numpy(), q=_np16(xs["q"]), k=_np16(xs["k"]),
+                       w=_np16(xs["w"]), dy=xs["dy"].numpy(), kind=w.dtype)
+        t0 = time.perf_counter()
+        li.q_rows(p, [0])
+        per = max(1e-4, time.perf_counter() - t0)
+        n = max(1, int(budget_s / (2 * per)))    # dK of the same rows costs about as much again
+        toks = np.sort(rng.choice(w.t1, min(n, w.t1), replace=False))
+        t0 = time.perf_counter()
+        li.backward_range(p, int(toks[0]), int(toks[0]) + len(toks))
+        dt = time.perf_counter() - t0
+        return 3 * 2.0 * w.d * w.topk * len(toks) * w.n1 / dt / 1e12, dt, len(toks)
+
+    cfg = {"workload": w.name, "batch": w.batch, "seq_len_q": [int(v) for v in np.diff(w.cu_q)], "n1": w.n1,
+           "n2": w.n2, "d": w.d, "topk": w.topk, "dtype": w.dtype, "mode": "default",
+           "l2": "inputs larger than L2 (129 MB): no flush between steps"}
+    metric = "lightning-indexer backward TFLOP/s and % of GB300 bf16 roofline; ms per call"
+    if args.impl == "reference":
+        per_step = min(5.0, 150.0 / max(1, args.steps + args.warmup))
+        vals, times = [], []
+        for s_ in range(args.warmup + args.steps):
+            v, dt, n = oracle_rate(per_step, s_)
+            if s_ >= args.warmup:
+                vals.append(v)
+                times.append(dt)
+        value = statistics.median(vals)
+        print(json.dumps({"impl": "reference", "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": cfg,
+                          "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                                           "sample": f"{n} consecutive query tokens (all heads) per step, one core "
+                                                     f"of {host_cpu()}"},
+                          "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    dev = x["q"].device
+    stream = torch.cuda.current_stream(dev)
+    desc = sab.make_indexer_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d, w.topk,
+                                 sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16)
+    need = sab.indexer_workspace_size(desc)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    outs = (torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["w"]))
+    io = sab.SliIo(query=x["q"].data_ptr(), key=x["k"].data_ptr(), weights=x["w"].data_ptr(), dy=x["dy"].data_ptr(),
+                   indices=x["idx"].data_ptr(), dq=outs[0].data_ptr(), dk=outs[1].data_ptr(),
+                   dweights=outs[2].data_ptr())
+
+    def call():
+        sab.lightning_indexer_grad(desc, io, ws.data_ptr(), need, stream.cuda_stream)
+
+    for _ in range(args.warmup):
+        call()
+    st = sab.query_error(ws.data_ptr(), stream.cuda_stream)
+    if st != sab.SAG_OK:
+        raise sab.SagError(st, "device")
+    K = args.steps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    t0.record(stream)
+    for _ in range(K):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1) / K, dev)
+    pk, pk_src = peaks()
+    peak = float(pk["bf16_tflops"])
+    achieved = flops / (ms * 1e-3) / 1e12
+    e2e = None
+    if not args.no_e2e:
+        names = ("q", "k", "w", "dy", "idx")
+        host_in = [x[k].cpu().pin_memory() for k in names]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def e2e_step():
+            for k_, h in zip(names, host_in):
+                x[k_].copy_(h, non_blocking=True)
+            call()
+            for h, d in zip(host_out, outs):
+                h.copy_(d, non_blocking=True)
+        e2e_step()
+        torch.cuda.synchronize()
+        ke = max(3, min(K, 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(a.elapsed_time(b) / ke, dev)
+        e2e = {"value": job_throughput(flops, world, ems), "unit": "TFLOP/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, n = oracle_rate(args.cpu_seconds)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} consecutive query tokens (all heads), full backward of those rows, {dt:.1f} s on "
+                         f"one core of {host_cpu()} ({os.cpu_count()} cores)"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": metric, "value": job_throughput(flops, world, ms), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": cfg,
+            "roofline": {"bound": "tensor", "kernel": "indexer backward (whole call)", "achieved": achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{pk_src} bf16 burst", "kernel_ms": ms, "traffic": None},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clk}), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 

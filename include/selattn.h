@@ -421,6 +421,19 @@ sag_status lightning_indexer_grad_workspace_size(const sli_desc *desc, size_t *w
 sag_status lightning_indexer_grad(const sli_desc *desc, const sli_io *io, void *workspace, size_t workspace_bytes,
                                   void *stream);
 
+/*
+ * Self-test of the device failure path (not part of the operator; the pages
+ * have no counterpart).  Enqueues one small kernel that runs the library's
+ * bounded mbarrier wait on a barrier nothing ever arrives on: after limit_ns
+ * (1 us .. 4 s) the wait gives up, SAG_ERR_TIMEOUT is recorded in the first
+ * 256 bytes of `workspace` (device memory, 16-byte aligned, at least 256
+ * bytes) and the kernel returns, so the context stays usable.  Read the
+ * status back with sel_attn_grad_query_error(workspace, stream).  Returns
+ * SAG_OK once enqueued, SAG_ERR_NULL / SAG_ERR_ALIGN / SAG_ERR_SHAPE for bad
+ * arguments, SAG_ERR_CUDA if the launch failed.
+ */
+sag_status sel_attn_selftest_wait_timeout(void *workspace, uint64_t limit_ns, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *sel_attn_grad_status_string(int status);
 

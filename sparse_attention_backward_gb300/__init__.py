@@ -31,7 +31,7 @@ SAG_LAYOUT_TND, SAG_LAYOUT_BSND = 0, 1
 EXPORTED = ("sel_attn_grad_workspace_size", "sel_attn_grad", "sel_attn_grad_timed", "sel_attn_grad_ex",
             "sel_attn_grad_plan_info", "sel_attn_grad_query_error", "sel_attn_grad_status_string",
             "sel_attn_fwd_workspace_size", "sel_attn_fwd", "sel_attn_fwd_timed", "sel_attn_fwd_ex",
-            "lightning_indexer_grad_workspace_size", "lightning_indexer_grad")
+            "lightning_indexer_grad_workspace_size", "lightning_indexer_grad", "sel_attn_selftest_wait_timeout")
 
 
 class SagDesc(ctypes.Structure):
@@ -208,6 +208,18 @@ def sel_attn_grad(desc: SagDesc, query, key, value, attention_out, attention_out
                                      main_stop)
     if st != SAG_OK:
         raise SagError(st, "sel_attn_grad")
+
+
+def selftest_wait_timeout(workspace, limit_ns: int, stream) -> None:
+    """Enqueue the bounded-wait self-test (see include/selattn.h); read its
+    status with ``query_error``."""
+    lib = load()
+    f = lib.sel_attn_selftest_wait_timeout
+    f.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    st = f(workspace, int(limit_ns), stream)
+    if st != SAG_OK:
+        raise SagError(st, "sel_attn_selftest_wait_timeout")
 
 
 def query_error(workspace, stream) -> int:

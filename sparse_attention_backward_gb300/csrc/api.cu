@@ -244,6 +244,10 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     return SAG_OK;
 }
 
+// Buckets are sorted by token where their order matters: the fixed-order dQ
+// path (deterministic accumulation, token chunks) and token windows.
+bool buckets_sorted(const Plan &p) { return p.ds_path || p.g.windowed; }
+
 Workspace carve(const Plan &p, void *base) {
     char *c = static_cast<char *>(base);
     Workspace w;
@@ -311,8 +315,8 @@ extern "C" sag_status sel_attn_grad_workspace_size(const sag_desc *desc, size_t 
 
 namespace {
 int launches_of(const Plan &p) {
-    // preprocess, histogram, 3 scan passes, fill, sort
-    int n = 7;
+    // preprocess, histogram, 3 scan passes, fill (, sort)
+    int n = 6 + (buckets_sorted(p) ? 1 : 0);
     if (!p.ds_path) return n + 2 + (p.g.windowed ? 1 : 0);   // main, cast dQ (, cast dK/dV)
     return n + 2 * p.n_chunks + (p.n_chunks > 1);    // (main, dQ) per chunk, cast dK/dV
 }
@@ -441,7 +445,7 @@ extern "C" sag_status sel_attn_grad_ex(const sag_desc *desc, const sag_io *io, v
     if ((launch_preprocess(g, ws, io->attention_out, io->attention_out_grad, io->softmax_max, io->softmax_sum,
                            p.fp16, !p.ds_path, s, sms)) != cudaSuccess)
         return SAG_ERR_CUDA;
-    if ((launch_inversion(g, ws, io->topk_indices, s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
+    if ((launch_inversion(g, ws, io->topk_indices, buckets_sorted(p), s, sms)) != cudaSuccess) return SAG_ERR_CUDA;
     if (!p.ds_path) {
         if (g.windowed &&
             cudaMemsetAsync(ws.dkv_acc, 0, sizeof(float) * (size_t)g.t2 * g.n2 * (g.d_qk + g.d_v), s) != cudaSuccess)
@@ -528,7 +532,7 @@ extern "C" sag_status sel_attn_fwd_ex(const sag_desc *desc, const sag_io *io, vo
     st = stage_metadata(p, workspace, s);
     if (st != SAG_OK) return st;
     if (launch_fwd_init(g, ws, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
-    if (launch_inversion(g, ws, io->topk_indices, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
+    if (launch_inversion(g, ws, io->topk_indices, g.windowed, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
     if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return SAG_ERR_CUDA;
     for (int pass = 1; pass <= 2; ++pass)
         if (launch_fwd_tc(g, ws, *io, pass, p.fp16, s, sms) != cudaSuccess) return SAG_ERR_CUDA;

@@ -181,13 +181,12 @@ __global__ void __launch_bounds__(512) k_bwd_simt(Geometry g, Workspace ws,
 // shapes the tensor-core pass does not take):
 //     dQ[t, h] = scale * sum over slots in list order, keys in block order, of
 //                dS[t, h, slot, key] * K[key row]
-// One warp per (token, KV head) and group of up to kHeadsPerWarp query heads;
-// lane l owns head dims [l * DQK/32, (l + 1) * DQK/32) of those heads.  No
-// shared memory and no block barrier: a key row is one coalesced warp load,
-// the dS value of a head a broadcast load.
-constexpr int kHeadsPerWarp = 8;
-
-template <bool kFp16, int DQK>
+// One warp per (token, KV head) and group of up to HPW query heads (HPW = 1,
+// 2, 4 or 8, the smallest that covers G up to 8: fewer accumulators, more
+// warps and loads in flight); lane l owns head dims [l * DQK/32,
+// (l + 1) * DQK/32) of those heads.  No shared memory and no block barrier: a
+// key row is one coalesced warp load, the dS value of a head a broadcast load.
+template <bool kFp16, int DQK, int kHeadsPerWarp>
 __global__ void __launch_bounds__(256) k_dq_from_ds(Geometry g, Workspace ws,
                                                     const uint16_t *__restrict__ k,
                                                     const uint16_t *__restrict__ k_rope,
@@ -218,14 +217,20 @@ __global__ void __launch_bounds__(256) k_dq_from_ds(Geometry g, Workspace ws,
             if (id < 0 || id >= nblk) continue;       // reported by the histogram
             const int64_t key0 = ws.cu_kv[b] + (int64_t)id * bs;
             const uint16_t *dsrow = ws.ds + ((cp * g.block_count + slot) * (int64_t)G + h0) * bs;
+#pragma unroll 4
             for (int r = 0; r < bs; ++r) {
                 const int64_t krow = (key0 + r) * g.n2 + n2;
+                // the lane's DPL dims in pairs (4-byte loads; a pair never
+                // straddles the rope boundary: both offsets are even)
                 float kv[DPL];
 #pragma unroll
-                for (int e = 0; e < DPL; ++e) {
+                for (int e = 0; e < DPL; e += 2) {
                     const int d = lane * DPL + e;
-                    kv[e] = u16_to_f<kFp16>(d < d_main ? __ldg(k + krow * d_main + d)
-                                                       : __ldg(k_rope + krow * g.d_rope + d - d_main));
+                    const uint32_t two = d < d_main ? __ldg(reinterpret_cast<const uint32_t *>(k + krow * d_main + d))
+                                                    : __ldg(reinterpret_cast<const uint32_t *>(
+                                                          k_rope + krow * g.d_rope + d - d_main));
+                    kv[e] = u16_to_f<kFp16>((uint16_t)(two & 0xffffu));
+                    kv[e + 1] = u16_to_f<kFp16>((uint16_t)(two >> 16));
                 }
 #pragma unroll
                 for (int h = 0; h < kHeadsPerWarp; ++h) {
@@ -304,17 +309,27 @@ cudaError_t launch_bwd_simt(const Geometry &g, const Workspace &ws, const sag_io
     return cudaErrorInvalidValue;
 }
 
+template <bool kFp16, int DQK, int HPW>
+static cudaError_t launch_dq_h(const Geometry &g, const Workspace &ws, const sag_io &io, cudaStream_t s,
+                               int num_sms) {
+    const int hgroups = (g.group + HPW - 1) / HPW;
+    const int64_t warps = (int64_t)(g.tok_hi - g.tok_lo) * g.n2 * hgroups;
+    int64_t grid = (warps + 7) / 8;
+    if (grid > (int64_t)num_sms * 32) grid = (int64_t)num_sms * 32;
+    if (grid == 0) return cudaSuccess;
+    k_dq_from_ds<kFp16, DQK, HPW><<<(int)grid, 256, 0, s>>>(g, ws, (const uint16_t *)io.key,
+                                                            (const uint16_t *)io.key_rope, io.topk_indices,
+                                                            (uint16_t *)io.dq, (uint16_t *)io.dq_rope);
+    return cudaGetLastError();
+}
+
 template <bool kFp16, int DQK>
 static cudaError_t launch_dq_t(const Geometry &g, const Workspace &ws, const sag_io &io, cudaStream_t s,
                                int num_sms) {
-    const int hgroups = (g.group + kHeadsPerWarp - 1) / kHeadsPerWarp;
-    const int64_t warps = (int64_t)(g.tok_hi - g.tok_lo) * g.n2 * hgroups;
-    int64_t grid = (warps + 7) / 8;
-    if (grid > (int64_t)num_sms * 16) grid = (int64_t)num_sms * 16;
-    if (grid == 0) return cudaSuccess;
-    k_dq_from_ds<kFp16, DQK><<<(int)grid, 256, 0, s>>>(g, ws, (const uint16_t *)io.key, (const uint16_t *)io.key_rope,
-                                                       io.topk_indices, (uint16_t *)io.dq, (uint16_t *)io.dq_rope);
-    return cudaGetLastError();
+    if (g.group == 1) return launch_dq_h<kFp16, DQK, 1>(g, ws, io, s, num_sms);
+    if (g.group == 2) return launch_dq_h<kFp16, DQK, 2>(g, ws, io, s, num_sms);
+    if (g.group <= 4) return launch_dq_h<kFp16, DQK, 4>(g, ws, io, s, num_sms);
+    return launch_dq_h<kFp16, DQK, 8>(g, ws, io, s, num_sms);
 }
 
 cudaError_t launch_dq_from_ds(const Geometry &g, const Workspace &ws, const sag_io &io, bool fp16, cudaStream_t s,

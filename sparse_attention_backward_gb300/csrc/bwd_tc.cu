@@ -69,6 +69,7 @@ struct TcArgs {
     Workspace ws;
     uint16_t *dk, *dv, *dk_rope;
     int nk, halves, tpt, deterministic;
+    int early_s;            // issue S = Q K^T before dY has landed
     int64_t n_titems;
 };
 
@@ -258,7 +259,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (ne > 0 && !tc::mbar_wait(&bars[B_ACC_FREE], (ne - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
                     const int s = tc_i & 1, d = tc_i % DOS;
-                    if (!tc::mbar_wait(&bars[B_Q_FULL0 + s], (tc_i >> 1) & 1, abort_flag, kWaitNs)) {
+                    if (!tc::mbar_wait(&bars[B_Q_FULL0 + s], (tc_i >> 1) & 1, abort_flag, kWaitNs) ||
+                        (!A.early_s && !tc::mbar_wait(&bars[B_DO_FULL0 + d], (tc_i / DOS) & 1, abort_flag, kWaitNs))) {
                         ok = false;
                         break;
                     }
@@ -266,12 +268,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const uint32_t qs = sbase + L::OFF_Q + s * L::Q_STAGE;
                     const uint32_t ds_ = sbase + L::OFF_DO + d * L::DO_STAGE;
                     const uint32_t ks = sbase + L::OFF_K, vs = sbase + L::OFF_V;
-                    // S = Q K^T, dP = dY V^T (both operands K-major); S is issued
-                    // before dY has landed
+                    // S = Q K^T, dP = dY V^T (both operands K-major); with early_s
+                    // S is issued before dY has landed
                     for (int kk = 0; kk < DQK / 16; ++kk)
                         tc::mma_f16_ss(tmem + kColS, tc::sw128_desc(qs + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                                        tc::sw128_desc(ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
-                    if (!tc::mbar_wait(&bars[B_DO_FULL0 + d], (tc_i / DOS) & 1, abort_flag, kWaitNs)) {
+                    if (A.early_s && !tc::mbar_wait(&bars[B_DO_FULL0 + d], (tc_i / DOS) & 1, abort_flag, kWaitNs)) {
                         ok = false;
                         break;
                     }
@@ -539,6 +541,11 @@ static cudaError_t launch_tc_t(const Geometry &g, const Workspace &ws, const sag
     a.halves = g.block_size / nk;
     a.tpt = kRows / g.group;
     a.deterministic = det ? 1 : 0;
+    // S ahead of dY: measured on GB300 faster in the deterministic mode and for
+    // G >= 32 (max selection 1001 -> 961 ms, long context deterministic
+    // 16.0 -> 15.2 ms), slower for the default mode at G = 16 (long context
+    // 10.45 -> 10.87 ms)
+    a.early_s = (det || g.group >= 32) ? 1 : 0;
     a.n_titems = g.n_units;
     // G in {1, 2, 4}: one-row boxes for tile::gather4; otherwise one box per token (G rows)
     const uint32_t box_rows = (g.group <= 4 && 4 % g.group == 0) ? 1 : g.group;

@@ -23,7 +23,9 @@ private:
 cudaError_t launch_preprocess(const Geometry &g, const Workspace &ws, const void *o, const void *dy,
                               const float *smax, const float *ssum, bool fp16, bool zero_dq,
                               cudaStream_t s, int num_sms);
-cudaError_t launch_inversion(const Geometry &g, const Workspace &ws, const int32_t *topk, cudaStream_t s,
+// topkIndices -> per key block the (token, slot) pairs naming it; `sorted`
+// orders each bucket by token (the fill's own order depends on atomic timing)
+cudaError_t launch_inversion(const Geometry &g, const Workspace &ws, const int32_t *topk, bool sorted, cudaStream_t s,
                              int num_sms);
 // scale * dq_acc -> dq (and dq_rope: columns d_qk - d_rope .. d_qk - 1)
 cudaError_t launch_cast_dq(const Geometry &g, const float *dq_acc, void *dq, void *dq_rope, bool fp16,

@@ -198,7 +198,10 @@ __global__ void __launch_bounds__(256) k_fill(Geometry g, Workspace ws,
 }
 
 // Sort each bucket ascending (token-major order), so that the order of the
-// entries does not depend on the timing of the fill's atomics.  The network
+// entries does not depend on the timing of the fill's atomics.  Needed where
+// the order matters: the deterministic mode (fixed accumulation order), token
+// chunks and token windows (binary searches by token); the default mode takes
+// the buckets as filled.  The network
 // is bitonic in its all-ascending form (the first step of every merge pairs
 // i with its mirror i ^ (k - 1), the later ones pair i with i ^ j), which
 // lets a bucket of n entries be padded virtually to the next power of two
@@ -376,7 +379,7 @@ cudaError_t launch_preprocess(const Geometry &g, const Workspace &ws, const void
 int scan_parts(int64_t n_items) { return (int)((n_items + kScanTile - 1) / kScanTile); }
 int64_t max_scannable_items() { return (int64_t)kScanTile * kScanTile; }
 
-cudaError_t launch_inversion(const Geometry &g, const Workspace &ws, const int32_t *topk, cudaStream_t s,
+cudaError_t launch_inversion(const Geometry &g, const Workspace &ws, const int32_t *topk, bool sorted, cudaStream_t s,
                              int num_sms) {
     const int64_t sel = (int64_t)g.t1 * g.n2 * g.block_count;
     if (sel > 0) {
@@ -388,9 +391,11 @@ cudaError_t launch_inversion(const Geometry &g, const Workspace &ws, const int32
     k_scan_apply<<<parts, kScanBlock, 0, s>>>(ws.count, g.n_items, ws.scan_part, ws.offset);
     if (sel > 0) {
         k_fill<<<grid_for(sel, 256, num_sms * 8), 256, 0, s>>>(g, ws, topk);
-        cudaFuncSetAttribute(k_sort_buckets, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(kSortCap * sizeof(int32_t)));
-        k_sort_buckets<<<grid_for(g.n_items, 1, num_sms * 4), 512, kSortCap * sizeof(int32_t), s>>>(g, ws);
+        if (sorted) {
+            cudaFuncSetAttribute(k_sort_buckets, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(kSortCap * sizeof(int32_t)));
+            k_sort_buckets<<<grid_for(g.n_items, 1, num_sms * 4), 512, kSortCap * sizeof(int32_t), s>>>(g, ws);
+        }
     }
     return cudaGetLastError();
 }

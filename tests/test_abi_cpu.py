@@ -139,11 +139,12 @@ def test_forward_phase1(lib):
 def test_plan_default_and_deterministic(lib):
     d = _desc()
     info = sab.plan_info(d)
-    # preprocess, histogram, 3 scan passes, fill, sort, main kernel, dQ cast
-    assert info.launches == 9 and info.token_chunks == 1 and info.main_kernel == 1
+    # preprocess, histogram, 3 scan passes, fill, main kernel, dQ cast (the
+    # default mode takes the buckets unsorted)
+    assert info.launches == 8 and info.token_chunks == 1 and info.main_kernel == 1
     assert info.workspace_bytes == sab.workspace_size(d)
     det = sab.plan_info(_desc(deterministic=True))
-    # one chunk: main kernel (stores dS) and the fixed-order dQ pass
+    # the bucket sort, then one chunk: main kernel (stores dS) and the fixed-order dQ pass
     assert det.token_chunks == 1 and det.launches == 7 + 2
     # items: key blocks (batch, KV head, block id)
     assert info.items == 256 // 16
@@ -165,10 +166,11 @@ def test_plan_kernel_choice(lib, monkeypatch):
 def test_plan_token_windows(lib, monkeypatch):
     monkeypatch.setenv("SELATTN_WINDOW_TOKENS", "64")
     w = sab.plan_info(_desc())
-    # windowed: dK / dV reduced as partials, so their cast runs too
+    # windowed: buckets sorted (window starts are found by token), dK / dV
+    # reduced as partials, so their cast runs too
     assert w.launches == 10
     monkeypatch.delenv("SELATTN_WINDOW_TOKENS")
-    assert sab.plan_info(_desc()).launches == 9
+    assert sab.plan_info(_desc()).launches == 8
 
 
 def test_deterministic_workspace_holds_ds_not_dq(lib):

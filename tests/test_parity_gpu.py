@@ -224,3 +224,21 @@ def test_default_mode_with_the_dq_pass(small_data, name, monkeypatch):
     S.assert_close(f"{name} dq pass dq", S.f64(dq), rdq)
     S.assert_close(f"{name} dq pass dk", S.f64(dk), rdk)
     S.assert_close(f"{name} dq pass dv", S.f64(dv), rdv)
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable(small_data):
+    """A wait that nothing completes gives up after its limit, the device
+    reports SAG_ERR_TIMEOUT through the workspace, and the next backward on the
+    same context is still correct."""
+    import time
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    t0 = time.perf_counter()
+    sab.selftest_wait_timeout(ws.data_ptr(), 50_000_000, stream.cuda_stream)    # 50 ms
+    assert sab.query_error(ws.data_ptr(), stream.cuda_stream) == sab.SAG_ERR_TIMEOUT
+    assert time.perf_counter() - t0 >= 0.05
+    w, x, (rdq, rdk, rdv) = small_data("tiny")
+    dq, dk, dv = _run(w, x, False)
+    S.assert_close("after timeout dq", S.f64(dq), rdq)
+    S.assert_close("after timeout dk", S.f64(dk), rdk)
+    S.assert_close("after timeout dv", S.f64(dv), rdv)
