@@ -174,13 +174,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
                 const int s = tc_i & 1;
+                const int nt = min(tpt, kt.ntok - i * tpt);
+                // the tile's bucket entries (up to 128 tokens: 4 per lane), loaded
+                // before waiting for the stage
+                int ent[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int tt = lane + 32 * q;
+                    ent[q] = tt < nt ? ws.entries[kt.e0 + i * tpt + tt] : -1;
+                }
                 if (tc_i >= 2 && !tc::mbar_wait(&bars[B_Q_EMPTY0 + s], ((tc_i >> 1) - 1) & 1, abort_flag, kWaitNs)) {
                     ok = false;
                     break;
                 }
-                const int nt = min(tpt, kt.ntok - i * tpt);
                 int *m = meta + (tc_i % kMeta) * kRows;
-                for (int tt = lane; tt < tpt; tt += 32) m[tt] = tt < nt ? ws.entries[kt.e0 + i * tpt + tt] : -1;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (lane + 32 * q < tpt) m[lane + 32 * q] = ent[q];
                 __syncwarp();
                 ++armed_q[s];
                 if (lane == 0) tc::mbar_arrive_expect_tx(&bars[B_Q_FULL0 + s], (uint32_t)tpt * G * DQK * 2);
@@ -199,10 +209,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tc::tma_gather4(qdst + c * 16384 + lane * 512, qmap(c), cx(c), y[0], y[1], y[2], y[3],
                                         &bars[B_Q_FULL0 + s]);
                 } else {
-                    for (int tt = lane; tt < tpt; tt += 32) {
+                    // one (token, chunk) box per lane: the issue is spread over the warp
+                    for (int j = lane; j < tpt * KC; j += 32) {
+                        const int tt = j / KC, c = j % KC;
                         const int y = tt < nt ? (m[tt] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
-                        for (int c = 0; c < KC; ++c)
-                            tc::tma_load_2d(qdst + c * 16384 + tt * G * 128, qmap(c), cx(c), y, &bars[B_Q_FULL0 + s]);
+                        tc::tma_load_2d(qdst + c * 16384 + tt * G * 128, qmap(c), cx(c), y, &bars[B_Q_FULL0 + s]);
                     }
                 }
                 const int d = tc_i % DOS;
@@ -227,10 +238,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tc::tma_gather4(ddst + c * 16384 + lane * 512, &map_do, c * 64, y[0], y[1], y[2], y[3],
                                         &bars[B_DO_FULL0 + d]);
                 } else {
-                    for (int tt = lane; tt < tpt; tt += 32) {
+                    for (int j = lane; j < tpt * 2; j += 32) {
+                        const int tt = j / 2, c = j % 2;
                         const int y = tt < nt ? (m[tt] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
-                        for (int c = 0; c < 2; ++c)
-                            tc::tma_load_2d(ddst + c * 16384 + tt * G * 128, &map_do, c * 64, y, &bars[B_DO_FULL0 + d]);
+                        tc::tma_load_2d(ddst + c * 16384 + tt * G * 128, &map_do, c * 64, y, &bars[B_DO_FULL0 + d]);
                     }
                 }
             }

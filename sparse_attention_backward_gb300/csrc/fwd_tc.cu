@@ -186,10 +186,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::tma_gather4(qdst + c * 16384 + lane * 512, qmap(c), cx(c), y[0], y[1], y[2], y[3],
                                         &bars[F_Q_FULL + s]);
                 } else {
-                    for (int tt = lane; tt < tpt; tt += 32) {
+                    // one (token, chunk) box per lane: the issue is spread over the warp
+                    for (int j = lane; j < tpt * KC; j += 32) {
+                        const int tt = j / KC, c = j % KC;
                         const int y = tt < nt ? (m[tt] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
-                        for (int c = 0; c < KC; ++c)
-                            tc::tma_load_2d(qdst + c * 16384 + tt * G * 128, qmap(c), cx(c), y, &bars[F_Q_FULL + s]);
+                        tc::tma_load_2d(qdst + c * 16384 + tt * G * 128, qmap(c), cx(c), y, &bars[F_Q_FULL + s]);
                     }
                 }
             }
