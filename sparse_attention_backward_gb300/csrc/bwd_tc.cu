@@ -73,7 +73,7 @@ struct TcArgs {
     int64_t n_titems;
 };
 
-template <bool kFp16, int DQK>
+template <bool kFp16, int DQK, bool kWarpIssue>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     k_bwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
              const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -256,82 +256,94 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!drained) fail();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const bool bf16 = !kFp16;
-            const uint32_t id_s = tc::idesc_f16(kRows, nk, bf16, false, false);
-            const uint32_t id_t = tc::idesc_f16(128, nk, bf16, true, true);
-            const uint32_t id_q = tc::idesc_f16(kRows, DQK, bf16, false, true);
-            int ne = 0, tc_i = 0;
-            bool ok = true;
-            for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
-                const KeyTile kt = decode(g, ws, ti, nk, tpt);
-                if (kt.ntok == 0) continue;
-                if (!tc::mbar_wait(&bars[B_KV_FULL], ne & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                if (ne > 0 && !tc::mbar_wait(&bars[B_ACC_FREE], (ne - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
-                    const int s = tc_i & 1, d = tc_i % DOS;
-                    if (!tc::mbar_wait(&bars[B_Q_FULL0 + s], (tc_i >> 1) & 1, abort_flag, kWaitNs) ||
-                        (!A.early_s && !tc::mbar_wait(&bars[B_DO_FULL0 + d], (tc_i / DOS) & 1, abort_flag, kWaitNs))) {
-                        ok = false;
-                        break;
-                    }
-                    tc::tc_fence_after();
-                    const uint32_t qs = sbase + L::OFF_Q + s * L::Q_STAGE;
-                    const uint32_t ds_ = sbase + L::OFF_DO + d * L::DO_STAGE;
-                    const uint32_t ks = sbase + L::OFF_K, vs = sbase + L::OFF_V;
-                    // S = Q K^T, dP = dY V^T (both operands K-major); with early_s
-                    // S is issued before dY has landed
-                    for (int kk = 0; kk < DQK / 16; ++kk)
-                        tc::mma_f16_ss(tmem + kColS, tc::sw128_desc(qs + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                                       tc::sw128_desc(ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
-                    if (A.early_s && !tc::mbar_wait(&bars[B_DO_FULL0 + d], (tc_i / DOS) & 1, abort_flag, kWaitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::tc_fence_after();
-                    for (int kk = 0; kk < DV / 16; ++kk)
-                        tc::mma_f16_ss(tmem + kColDP, tc::sw128_desc(ds_ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                                       tc::sw128_desc(vs + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
-                    tc::mma_commit(&bars[B_S_FULL]);
-                    if (!tc::mbar_wait(&bars[B_P_FULL], tc_i & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                    tc::tc_fence_after();
-                    const uint32_t ps = sbase + L::OFF_P, dss = sbase + L::OFF_DS;
-                    // dV^T += dY^T P (A: dY tile MN-major, B: P MN-major)
-                    for (int kk = 0; kk < kRows / 16; ++kk)
-                        tc::mma_f16_ss(tmem + kColDV, tc::sw128_desc(ds_ + kk * 2048, 16384, 1024),
-                                       tc::sw128_desc(ps + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
-                    tc::mma_commit(&bars[B_DO_EMPTY0 + d]);
-                    // dK^T += Q^T dS, dims [0,128) and (192 wide) dims [64,192)
-                    for (int kk = 0; kk < kRows / 16; ++kk)
-                        tc::mma_f16_ss(tmem + kColDKlo, tc::sw128_desc(qs + kk * 2048, 16384, 1024),
-                                       tc::sw128_desc(dss + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
-                    if (DQK == 192)
-                        for (int kk = 0; kk < kRows / 16; ++kk)
-                            tc::mma_f16_ss(tmem + kColDKhi, tc::sw128_desc(qs + 16384 + kk * 2048, 16384, 1024),
-                                           tc::sw128_desc(dss + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
-                    tc::mma_commit(&bars[B_Q_EMPTY0 + s]);
-                    if (!det) {
-                        // dQ = dS K (A: dS K-major, B: K tile MN-major, N = Dqk)
-                        if (tc_i > 0 && !tc::mbar_wait(&bars[B_DQ_FREE], (tc_i - 1) & 1, abort_flag, kWaitNs)) {
-                            ok = false;
-                            break;
-                        }
-                        tc::tc_fence_after();
-                        for (int kk = 0; kk < nk / 16; ++kk)
-                            tc::mma_f16_ss(tmem + kColDQ, tc::sw128_desc(dss + kk * 32, 16, 1024),
-                                           tc::sw128_desc(ks + kk * 2048, 8192, 1024), id_q, kk > 0);
-                    }
-                    tc::mma_commit(&bars[B_MMA_DONE]);
+        // With kWarpIssue the whole warp runs the schedule and one elected
+        // lane issues each instruction, else lane 0 alone runs it: measured on
+        // GB300, the warp form is faster in the deterministic mode (long
+        // context 15.35 -> 14.80 ms, max selection 1358 -> 1266 ms) and slower
+        // with the per-tile dQ reductions (9.93 -> 10.45 ms, 961 -> 1031 ms).
+        if (kWarpIssue || lane == 0) {
+        const bool bf16 = !kFp16;
+        const uint32_t id_s = tc::idesc_f16(kRows, nk, bf16, false, false);
+        const uint32_t id_t = tc::idesc_f16(128, nk, bf16, true, true);
+        const uint32_t id_q = tc::idesc_f16(kRows, DQK, bf16, false, true);
+        const uint32_t ks = sbase + L::OFF_K, vs = sbase + L::OFF_V;
+        const uint32_t ps = sbase + L::OFF_P, dss = sbase + L::OFF_DS;
+        auto wait = [&](int b, uint32_t parity) -> bool {
+            const bool w = tc::mbar_wait(&bars[b], parity, abort_flag, kWaitNs);
+            return kWarpIssue ? __all_sync(0xffffffffu, w) : w;
+        };
+        auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t id, bool acc) {
+            if (kWarpIssue) tc::mma_f16_ss_warp(d, a, b, id, acc);
+            else tc::mma_f16_ss(d, a, b, id, acc);
+        };
+        auto commit = [&](uint64_t *bar) {
+            if (kWarpIssue) tc::mma_commit_warp(bar);
+            else tc::mma_commit(bar);
+        };
+        int ne = 0, tc_i = 0;
+        bool ok = true;
+        for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
+            const KeyTile kt = decode(g, ws, ti, nk, tpt);
+            if (kt.ntok == 0) continue;
+            if (!wait(B_KV_FULL, ne & 1)) { ok = false; break; }
+            if (ne > 0 && !wait(B_ACC_FREE, (ne - 1) & 1)) { ok = false; break; }
+            for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
+                const int s = tc_i & 1, d = tc_i % DOS;
+                if (!wait(B_Q_FULL0 + s, (tc_i >> 1) & 1) ||
+                    (!A.early_s && !wait(B_DO_FULL0 + d, (tc_i / DOS) & 1))) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
-                tc::mma_commit(&bars[B_ACC_FULL]);
-                tc::mma_commit(&bars[B_KV_EMPTY]);
-                ++ne;
+                tc::tc_fence_after();
+                const uint32_t qs = sbase + L::OFF_Q + s * L::Q_STAGE;
+                const uint32_t ds_ = sbase + L::OFF_DO + d * L::DO_STAGE;
+                // S = Q K^T, dP = dY V^T (both operands K-major); with early_s
+                // S is issued before dY has landed
+                for (int kk = 0; kk < DQK / 16; ++kk)
+                    mma(tmem + kColS, tc::sw128_desc(qs + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                        tc::sw128_desc(ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+                if (A.early_s && !wait(B_DO_FULL0 + d, (tc_i / DOS) & 1)) { ok = false; break; }
+                tc::tc_fence_after();
+                for (int kk = 0; kk < DV / 16; ++kk)
+                    mma(tmem + kColDP, tc::sw128_desc(ds_ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                        tc::sw128_desc(vs + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+                commit(&bars[B_S_FULL]);
+                if (!wait(B_P_FULL, tc_i & 1)) { ok = false; break; }
+                tc::tc_fence_after();
+                // dV^T += dY^T P (A: dY tile MN-major, B: P MN-major)
+                for (int kk = 0; kk < kRows / 16; ++kk)
+                    mma(tmem + kColDV, tc::sw128_desc(ds_ + kk * 2048, 16384, 1024),
+                        tc::sw128_desc(ps + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
+                commit(&bars[B_DO_EMPTY0 + d]);
+                // dK^T += Q^T dS, dims [0,128) and (192 wide) dims [64,192)
+                for (int kk = 0; kk < kRows / 16; ++kk)
+                    mma(tmem + kColDKlo, tc::sw128_desc(qs + kk * 2048, 16384, 1024),
+                        tc::sw128_desc(dss + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
+                if (DQK == 192)
+                    for (int kk = 0; kk < kRows / 16; ++kk)
+                        mma(tmem + kColDKhi, tc::sw128_desc(qs + 16384 + kk * 2048, 16384, 1024),
+                            tc::sw128_desc(dss + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
+                commit(&bars[B_Q_EMPTY0 + s]);
+                if (!det) {
+                    // dQ = dS K (A: dS K-major, B: K tile MN-major, N = Dqk)
+                    if (tc_i > 0 && !wait(B_DQ_FREE, (tc_i - 1) & 1)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    for (int kk = 0; kk < nk / 16; ++kk)
+                        mma(tmem + kColDQ, tc::sw128_desc(dss + kk * 32, 16, 1024),
+                            tc::sw128_desc(ks + kk * 2048, 8192, 1024), id_q, kk > 0);
+                }
+                commit(&bars[B_MMA_DONE]);
             }
-            if (!ok) fail();
-            // every MMA issued must be complete before TMEM is freed
-            tc::mma_commit(&bars[B_DRAIN]);
-            if (!tc::mbar_wait_drain(&bars[B_DRAIN], 0, kWaitNs)) fail();
+            if (!ok) break;
+            commit(&bars[B_ACC_FULL]);
+            commit(&bars[B_KV_EMPTY]);
+            ++ne;
+        }
+        if (!ok && lane == 0) fail();
+        // every MMA issued must be complete before TMEM is freed
+        commit(&bars[B_DRAIN]);
+        const bool drained = tc::mbar_wait_drain(&bars[B_DRAIN], 0, kWaitNs);
+        if (!(kWarpIssue ? __all_sync(0xffffffffu, drained) : drained) && lane == 0) fail();
         }
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------ softmax / dS
@@ -566,7 +578,8 @@ static cudaError_t launch_tc_t(const Geometry &g, const Workspace &ws, const sag
         !tmap_2d(&mdo, io.attention_out_grad, kFp16, 128, (uint64_t)g.t1 * g.n1, box_rows) ||
         !tmap_3d(&mv, io.value, kFp16, 128, g.n2, g.t2, nk))
         return cudaErrorInvalidValue;
-    auto fn = k_bwd_tc<kFp16, DQK>;
+    // the warp-issued MMA schedule for the deterministic mode (see the MMA role)
+    auto fn = det ? k_bwd_tc<kFp16, DQK, true> : k_bwd_tc<kFp16, DQK, false>;
     const int smem = Smem<DQK>::TOTAL;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

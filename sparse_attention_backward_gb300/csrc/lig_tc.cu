@@ -38,12 +38,14 @@ constexpr int kLiThreads = 320;
 // TMEM columns: S^T stages, dK stages, dQ^T buffers (512 allocated)
 constexpr uint32_t kLiColS = 0, kLiColDK = 128, kLiColDQ = 384;
 
+constexpr int kLiKStages = 3;       // gathered key tiles in flight
+
 struct LiSmem {
     static constexpr int K_STAGE = 2 * kLiChunk * 128;     // 2 chunks of 64 dims x 128 rows
     static constexpr int Q_STAGE = 2 * kLiHeads * 128;     // 2 chunks of 64 dims x 64 head rows
     static constexpr int R_STAGE = kLiChunk * 128;         // 128 key rows x 64 heads (bf16)
     static constexpr int OFF_K = 0;
-    static constexpr int OFF_Q = OFF_K + 2 * K_STAGE;
+    static constexpr int OFF_Q = OFF_K + kLiKStages * K_STAGE;
     static constexpr int OFF_R = OFF_Q + 2 * Q_STAGE;
     static constexpr int OFF_STG = OFF_R + 2 * R_STAGE;      // 4 epilogue warps x 4 KB
     static constexpr int OFF_W = OFF_STG + 16384;            // 2 x 64 weights (fp32), by query stage
@@ -52,8 +54,8 @@ struct LiSmem {
 };
 
 enum LiBar {
-    L_Q_FULL0 = 0, L_Q_FULL1, L_Q_EMPTY0, L_Q_EMPTY1, L_K_FULL0, L_K_FULL1, L_K_EMPTY0, L_K_EMPTY1,
-    L_S_FULL0, L_S_FULL1, L_R_FULL0, L_R_FULL1, L_DK_FULL0, L_DK_FULL1, L_DK_FREE0, L_DK_FREE1,
+    L_Q_FULL0 = 0, L_Q_FULL1, L_Q_EMPTY0, L_Q_EMPTY1, L_K_FULL0, L_K_EMPTY0 = L_K_FULL0 + kLiKStages,
+    L_S_FULL0 = L_K_EMPTY0 + kLiKStages, L_S_FULL1, L_R_FULL0, L_R_FULL1, L_DK_FULL0, L_DK_FULL1, L_DK_FREE0, L_DK_FREE1,
     L_DQ_FULL0, L_DQ_FULL1, L_DQ_FREE0, L_DQ_FREE1, L_DRAIN, L_COUNT
 };
 
@@ -69,19 +71,41 @@ struct LiArgs {
     int nchunks;           // ceil(topk / 128)
 };
 
-// Key row (of the [T2 * n2] rows of the key map) of selection j of unit
-// (t, n2), or -1 for an empty slot, a slot past topk, or an id out of range
-// (reported).
-__device__ __forceinline__ int64_t li_key_row(const LiArgs &A, int t, int n2, int b, int j, bool report) {
-    if (j >= A.g.block_count) return -1;
-    const int id = __ldg(A.idx + ((int64_t)t * A.g.n2 + n2) * A.g.block_count + j);
+// A unit's view of its selections: index list, dy row, the batch's valid key
+// rows and first key-map row.
+struct LiUnit {
+    const int32_t *idx;    // [topk]
+    const float *dy;       // [topk]
+    int s2;                // valid key rows of the batch
+    int topk;
+    int64_t kbase;         // key-map row of the batch's key 0 for this key head
+    int n2;
+};
+
+__device__ __forceinline__ LiUnit li_unit(const LiArgs &A, int t, int n2, int b) {
+    LiUnit u;
+    const int64_t off = ((int64_t)t * A.g.n2 + n2) * A.g.block_count;
+    u.idx = A.idx + off;
+    u.dy = A.dy + off;
+    u.s2 = A.ws.kv_blocks[b];
+    u.topk = A.g.block_count;
+    u.kbase = (int64_t)A.ws.cu_kv[b] * A.g.n2 + n2;
+    u.n2 = A.g.n2;
+    return u;
+}
+
+// Id of selection j (-1 past topk).
+__device__ __forceinline__ int li_id(const LiUnit &u, int j) { return j < u.topk ? __ldg(u.idx + j) : -1; }
+
+// Key row (of the [T2 * n2] rows of the key map) of a selection id, or -1 for
+// an empty slot or an id out of range (reported when `report`).
+__device__ __forceinline__ int64_t li_row(const LiArgs &A, const LiUnit &u, int id, bool report) {
     if (id == -1) return -1;
-    const int s2 = A.ws.kv_blocks[b];                 // valid key rows of the batch
-    if (id < 0 || id >= s2) {
+    if (id < 0 || id >= u.s2) {
         if (report) raise_error(&A.ws.hdr->error, SAG_ERR_INDEX);
         return -1;
     }
-    return ((int64_t)A.ws.cu_kv[b] + id) * A.g.n2 + n2;
+    return u.kbase + (int64_t)id * u.n2;
 }
 
 template <bool kFp16>
@@ -143,11 +167,12 @@ __global__ void __launch_bounds__(kLiThreads, 1)
             tc::prefetch_tmap(&map_k);
         }
         int uu = 0, kc = 0;
-        uint32_t armed_q[2] = {0, 0}, armed_k[2] = {0, 0};
+        uint32_t armed_q[2] = {0, 0}, armed_k[kLiKStages] = {};
         bool ok = true;
         for (int64_t u = blockIdx.x; u < A.n_units && ok; u += gridDim.x) {
             int t, n2, b;
             if (!unit(u, t, n2, b)) continue;
+            const LiUnit lu = li_unit(A, t, n2, b);
             const int qs = uu & 1;
             if (uu >= 2 && !tc::mbar_wait(&bars[L_Q_EMPTY0 + qs], ((uu >> 1) - 1) & 1, abort_flag, kWaitNs)) {
                 ok = false;
@@ -165,19 +190,20 @@ __global__ void __launch_bounds__(kLiThreads, 1)
                     tc::tma_load_2d(smem + L::OFF_Q + qs * L::Q_STAGE + c * (L::Q_STAGE / 2), &map_q, c * 64,
                                     t * g.n1 + n2 * G, &bars[L_Q_FULL0 + qs]);
             }
-            // an empty or bad slot fetches the batch's first key row (its R is 0)
-            const int64_t row0 = (int64_t)ws.cu_kv[b] * g.n2 + n2;
             for (int c = 0; c < A.nchunks; ++c, ++kc) {
-                const int ks = kc & 1;
-                if (kc >= 2 && !tc::mbar_wait(&bars[L_K_EMPTY0 + ks], ((kc >> 1) - 1) & 1, abort_flag, kWaitNs)) {
-                    ok = false;
-                    break;
-                }
+                const int ks = kc % kLiKStages;
+                // the chunk's key rows, read before waiting for the stage; an
+                // empty or bad slot fetches the batch's first key row (its R is 0)
                 int y[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int64_t r = li_key_row(A, t, n2, b, c * kLiChunk + 4 * lane + e, false);
-                    y[e] = (int)(r >= 0 ? r : row0);
+                    const int64_t r = li_row(A, lu, li_id(lu, c * kLiChunk + 4 * lane + e), false);
+                    y[e] = (int)(r >= 0 ? r : lu.kbase);
+                }
+                if (kc >= kLiKStages &&
+                    !tc::mbar_wait(&bars[L_K_EMPTY0 + ks], ((kc / kLiKStages) - 1) & 1, abort_flag, kWaitNs)) {
+                    ok = false;
+                    break;
                 }
                 ++armed_k[ks];
                 if (lane == 0) tc::mbar_arrive_expect_tx(&bars[L_K_FULL0 + ks], (uint32_t)kLiChunk * kLiD * 2);
@@ -191,79 +217,88 @@ __global__ void __launch_bounds__(kLiThreads, 1)
         }
         if (!ok) fail();
         bool drained = true;
-        for (int i = 0; i < 2; ++i)
-            drained = tc::drain_armed(&bars[L_Q_FULL0 + i], armed_q[i], kWaitNs) &&
-                      tc::drain_armed(&bars[L_K_FULL0 + i], armed_k[i], kWaitNs) && drained;
+        for (int i = 0; i < 2; ++i) drained = tc::drain_armed(&bars[L_Q_FULL0 + i], armed_q[i], kWaitNs) && drained;
+        for (int i = 0; i < kLiKStages; ++i)
+            drained = tc::drain_armed(&bars[L_K_FULL0 + i], armed_k[i], kWaitNs) && drained;
         if (!drained) fail();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const bool bf16 = !kFp16;
-            const uint32_t id_s = tc::idesc_f16(kLiChunk, kLiHeads, bf16, false, false);   // S^T = Kc Q^T
-            const uint32_t id_q = tc::idesc_f16(kLiD, kLiHeads, bf16, true, true);         // dQ^T += Kc^T R
-            const uint32_t id_k = tc::idesc_f16(kLiChunk, kLiD, bf16, false, true);        // dKc = R Q
-            struct Prev { int kc, qs, dqb, uu; bool first, last; };
-            Prev pv{};
-            bool have = false, ok = true;
-            int uu = 0, kc = 0;
-            // the dQ / dK MMAs of chunk p once its R is in shared memory
-            auto back = [&](const Prev &p) -> bool {
-                const int rs = p.kc & 1;
-                if (!tc::mbar_wait(&bars[L_R_FULL0 + rs], (p.kc >> 1) & 1, abort_flag, kWaitNs)) return false;
-                if (p.first && p.uu >= 2 &&
-                    !tc::mbar_wait(&bars[L_DQ_FREE0 + p.dqb], ((p.uu >> 1) - 1) & 1, abort_flag, kWaitNs))
-                    return false;
-                if (p.kc >= 2 && !tc::mbar_wait(&bars[L_DK_FREE0 + rs], ((p.kc >> 1) - 1) & 1, abort_flag, kWaitNs))
-                    return false;
-                tc::tc_fence_after();
-                const uint32_t ks = sbase + L::OFF_K + rs * L::K_STAGE;
-                const uint32_t qs = sbase + L::OFF_Q + p.qs * L::Q_STAGE;
-                const uint32_t rr = sbase + L::OFF_R + rs * L::R_STAGE;
-                // dQ^T += Kc^T R: A = key tile MN-major (dims x keys), B = R MN-major (heads x keys)
-                for (int kk = 0; kk < kLiChunk / 16; ++kk)
-                    tc::mma_f16_ss(tmem + kLiColDQ + p.dqb * kLiHeads, tc::sw128_desc(ks + kk * 2048, L::K_STAGE / 2, 1024),
-                                   tc::sw128_desc(rr + kk * 2048, L::R_STAGE, 1024), id_q, (!p.first) || (kk > 0));
-                // dKc = R Q: A = R K-major (keys x heads), B = query tile MN-major (dims x heads)
-                for (int kk = 0; kk < kLiHeads / 16; ++kk)
-                    tc::mma_f16_ss(tmem + kLiColDK + rs * kLiD, tc::sw128_desc(rr + kk * 32, 16, 1024),
-                                   tc::sw128_desc(qs + kk * 2048, L::Q_STAGE / 2, 1024), id_k, kk > 0);
-                tc::mma_commit(&bars[L_DK_FULL0 + rs]);
-                tc::mma_commit(&bars[L_K_EMPTY0 + rs]);      // key tile and R stage free
-                if (p.last) {
-                    tc::mma_commit(&bars[L_DQ_FULL0 + p.dqb]);
-                    tc::mma_commit(&bars[L_Q_EMPTY0 + p.qs]);
-                }
-                return true;
-            };
-            for (int64_t u = blockIdx.x; u < A.n_units && ok; u += gridDim.x) {
-                int t, n2, b;
-                if (!unit(u, t, n2, b)) continue;
-                const int qs = uu & 1;
-                if (!tc::mbar_wait(&bars[L_Q_FULL0 + qs], (uu >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                for (int c = 0; c < A.nchunks; ++c, ++kc) {
-                    const int ks = kc & 1;
-                    if (!tc::mbar_wait(&bars[L_K_FULL0 + ks], (kc >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                    tc::tc_fence_after();
-                    const uint32_t kt = sbase + L::OFF_K + ks * L::K_STAGE;
-                    const uint32_t qt = sbase + L::OFF_Q + qs * L::Q_STAGE;
-                    // S^T = Kc Q^T (both operands K-major)
-                    for (int kk = 0; kk < kLiD / 16; ++kk)
-                        tc::mma_f16_ss(tmem + kLiColS + ks * kLiHeads,
-                                       tc::sw128_desc(kt + (kk >> 2) * (L::K_STAGE / 2) + (kk & 3) * 32, 16, 1024),
-                                       tc::sw128_desc(qt + (kk >> 2) * (L::Q_STAGE / 2) + (kk & 3) * 32, 16, 1024), id_s,
-                                       kk > 0);
-                    tc::mma_commit(&bars[L_S_FULL0 + ks]);
-                    if (have && !back(pv)) { ok = false; break; }
-                    pv = Prev{kc, qs, uu & 1, uu, c == 0, c == A.nchunks - 1};
-                    have = true;
-                }
-                ++uu;
+        // The whole warp runs the schedule; one elected lane issues each
+        // tcgen05 instruction (descriptors stay warp-uniform).
+        const bool bf16 = !kFp16;
+        const uint32_t id_s = tc::idesc_f16(kLiChunk, kLiHeads, bf16, false, false);   // S^T = Kc Q^T
+        const uint32_t id_q = tc::idesc_f16(kLiD, kLiHeads, bf16, true, true);         // dQ^T += Kc^T R
+        const uint32_t id_k = tc::idesc_f16(kLiChunk, kLiD, bf16, false, true);        // dKc = R Q
+        const uint64_t d_k0 = tc::sw128_desc(sbase + L::OFF_K, 16, 1024);                  // key tile, K-major
+        const uint64_t d_kt0 = tc::sw128_desc(sbase + L::OFF_K, L::K_STAGE / 2, 1024);     // key tile, MN-major
+        const uint64_t d_q0 = tc::sw128_desc(sbase + L::OFF_Q, 16, 1024);                  // query tile, K-major
+        const uint64_t d_qt0 = tc::sw128_desc(sbase + L::OFF_Q, L::Q_STAGE / 2, 1024);     // query tile, MN-major
+        const uint64_t d_rt0 = tc::sw128_desc(sbase + L::OFF_R, L::R_STAGE, 1024);         // R, MN-major
+        const uint64_t d_r0 = tc::sw128_desc(sbase + L::OFF_R, 16, 1024);                  // R, K-major
+        auto wait = [&](int bi, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, tc::mbar_wait(&bars[bi], parity, abort_flag, kWaitNs));
+        };
+        struct Prev { int kc, qs, dqb, uu; bool first, last; };
+        Prev pv{};
+        bool have = false, ok = true;
+        int uu = 0, kc = 0;
+        // the dQ / dK MMAs of chunk p once its R is in shared memory
+        auto back = [&](const Prev &p) -> bool {
+            const int rs = p.kc & 1, ks = p.kc % kLiKStages;
+            if (!wait(L_R_FULL0 + rs, (p.kc >> 1) & 1)) return false;
+            if (p.first && p.uu >= 2 && !wait(L_DQ_FREE0 + p.dqb, ((p.uu >> 1) - 1) & 1)) return false;
+            if (p.kc >= 2 && !wait(L_DK_FREE0 + rs, ((p.kc >> 1) - 1) & 1)) return false;
+            tc::tc_fence_after();
+            const uint64_t kt = d_kt0 + (uint64_t)((ks * L::K_STAGE) >> 4);
+            const uint64_t qt = d_qt0 + (uint64_t)((p.qs * L::Q_STAGE) >> 4);
+            const uint64_t rt = d_rt0 + (uint64_t)((rs * L::R_STAGE) >> 4);
+            const uint64_t rk = d_r0 + (uint64_t)((rs * L::R_STAGE) >> 4);
+            // dQ^T += Kc^T R: A = key tile MN-major (dims x keys), B = R MN-major (heads x keys)
+#pragma unroll
+            for (int kk = 0; kk < kLiChunk / 16; ++kk)
+                tc::mma_f16_ss_warp(tmem + kLiColDQ + p.dqb * kLiHeads, kt + ((kk * 2048) >> 4),
+                                    rt + ((kk * 2048) >> 4), id_q, (!p.first) || (kk > 0));
+            // dKc = R Q: A = R K-major (keys x heads), B = query tile MN-major (dims x heads)
+#pragma unroll
+            for (int kk = 0; kk < kLiHeads / 16; ++kk)
+                tc::mma_f16_ss_warp(tmem + kLiColDK + rs * kLiD, rk + ((kk * 32) >> 4), qt + ((kk * 2048) >> 4),
+                                    id_k, kk > 0);
+            tc::mma_commit_warp(&bars[L_DK_FULL0 + rs]);
+            tc::mma_commit_warp(&bars[L_K_EMPTY0 + ks]);      // key tile and R stage free
+            if (p.last) {
+                tc::mma_commit_warp(&bars[L_DQ_FULL0 + p.dqb]);
+                tc::mma_commit_warp(&bars[L_Q_EMPTY0 + p.qs]);
             }
-            if (ok && have && !back(pv)) ok = false;
-            if (!ok) fail();
-            tc::mma_commit(&bars[L_DRAIN]);
-            if (!tc::mbar_wait_drain(&bars[L_DRAIN], 0, kWaitNs)) fail();
+            return true;
+        };
+        for (int64_t u = blockIdx.x; u < A.n_units && ok; u += gridDim.x) {
+            int t, n2, b;
+            if (!unit(u, t, n2, b)) continue;
+            const int qs = uu & 1;
+            if (!wait(L_Q_FULL0 + qs, (uu >> 1) & 1)) { ok = false; break; }
+            const uint64_t dq = d_q0 + (uint64_t)((qs * L::Q_STAGE) >> 4);
+            for (int c = 0; c < A.nchunks; ++c, ++kc) {
+                const int ks = kc % kLiKStages;
+                if (!wait(L_K_FULL0 + ks, (kc / kLiKStages) & 1)) { ok = false; break; }
+                tc::tc_fence_after();
+                const uint64_t dk = d_k0 + (uint64_t)((ks * L::K_STAGE) >> 4);
+                // S^T = Kc Q^T (both operands K-major)
+#pragma unroll
+                for (int kk = 0; kk < kLiD / 16; ++kk)
+                    tc::mma_f16_ss_warp(tmem + kLiColS + (kc & 1) * kLiHeads,
+                                        dk + ((((kk >> 2) * (L::K_STAGE / 2)) + (kk & 3) * 32) >> 4),
+                                        dq + ((((kk >> 2) * (L::Q_STAGE / 2)) + (kk & 3) * 32) >> 4), id_s, kk > 0);
+                tc::mma_commit_warp(&bars[L_S_FULL0 + (kc & 1)]);
+                if (have && !back(pv)) { ok = false; break; }
+                pv = Prev{kc, qs, uu & 1, uu, c == 0, c == A.nchunks - 1};
+                have = true;
+            }
+            ++uu;
         }
+        if (ok && have && !back(pv)) ok = false;
+        if (!ok && lane == 0) fail();
+        tc::mma_commit_warp(&bars[L_DRAIN]);
+        if (!__all_sync(0xffffffffu, tc::mbar_wait_drain(&bars[L_DRAIN], 0, kWaitNs)) && lane == 0) fail();
     } else if (warp < 6) {
         // ------------------------------------------------------ relu / dW
         const int q4 = warp & 3;
@@ -278,12 +313,21 @@ __global__ void __launch_bounds__(kLiThreads, 1)
             ok = tc::mbar_wait(&bars[L_Q_FULL0 + (uu & 1)], (uu >> 1) & 1, abort_flag, kWaitNs);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             const float *wv = wbuf + (uu & 1) * kLiHeads;
+            const LiUnit lu = li_unit(A, t, n2, b);
             float dw0 = 0.f, dw1 = 0.f;                      // this lane's two heads (see below)
+            // this key's id and dy, one chunk ahead of the chunk being processed
+            int id_next = li_id(lu, r);
+            float dy_next = r < lu.topk ? __ldg(lu.dy + r) : 0.f;
             for (int c = 0; c < A.nchunks; ++c, ++kc) {
                 const int ks = kc & 1;
-                const int j = c * kLiChunk + r;
-                const bool valid = li_key_row(A, t, n2, b, j, true) >= 0;
-                const float dyv = valid ? A.dy[((int64_t)t * g.n2 + n2) * g.block_count + j] : 0.f;
+                const int id = id_next;
+                const float dy_c = dy_next;
+                if (c + 1 < A.nchunks) {
+                    const int j = (c + 1) * kLiChunk + r;
+                    id_next = li_id(lu, j);
+                    dy_next = j < lu.topk ? __ldg(lu.dy + j) : 0.f;
+                }
+                const float dyv = li_row(A, lu, id, true) >= 0 ? dy_c : 0.f;
                 ok = tc::mbar_wait(&bars[L_S_FULL0 + ks], (kc >> 1) & 1, abort_flag, kWaitNs);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc::tc_fence_after();
@@ -355,9 +399,10 @@ __global__ void __launch_bounds__(kLiThreads, 1)
         for (int64_t u = blockIdx.x; u < A.n_units && ok; u += gridDim.x) {
             int t, n2, b;
             if (!unit(u, t, n2, b)) continue;
+            const LiUnit lu = li_unit(A, t, n2, b);
             for (int c = 0; c < A.nchunks; ++c, ++kc) {
                 const int ks = kc & 1;
-                const int64_t krow = li_key_row(A, t, n2, b, c * kLiChunk + r, false);
+                const int64_t krow = li_row(A, lu, li_id(lu, c * kLiChunk + r), false);
                 ok = tc::mbar_wait(&bars[L_DK_FULL0 + ks], (kc >> 1) & 1, abort_flag, kWaitNs);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc::tc_fence_after();
