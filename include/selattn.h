@@ -235,7 +235,11 @@ sag_status sel_attn_grad_ex(const sag_desc *desc, const sag_io *io, void *worksp
  *   dq_path           0: dQ reduced with fp32 atomics inside the main kernel;
  *                     1: dS stored and dQ formed by a fixed-order pass (always
  *                     in deterministic mode; in default mode when it moves
- *                     fewer bytes by the library's count)
+ *                     fewer bytes by the library's count);
+ *                     2: the main kernel stores every key tile's fp32 dQ
+ *                     partial per (query row, slot) and a pass sums them in
+ *                     list order (deterministic mode, when that moves fewer
+ *                     bytes than path 1: small blocks and query groups)
  */
 typedef struct sag_plan_info {
     uint64_t workspace_bytes;

@@ -57,10 +57,27 @@ bool prefer_dq_pass(const Geometry &g) {
     return pass < 0.5 * red;
 }
 
+// Fixed-order dQ from per-slot partials instead of the stored dS, per query row:
+//   dS pass:  count * bs * 2 * 2 + count * bs * d_qk * 2 / G (as above)
+//   partials: count * halves * d_qk * 4 * 2 (each key tile's fp32 dQ partial
+//             stored by the main kernel, read back once by the summing pass)
+// taken when the partials move less than half the bytes: small blocks and
+// small query groups, where the dS pass re-reads every selected key block per
+// (token, KV head).  SELATTN_DQ_SLOTS=0 / 1 forces either.
+bool prefer_dq_slots(const Geometry &g) {
+    const char *env = getenv("SELATTN_DQ_SLOTS");
+    if (env && env[0] == '0') return false;
+    if (env && env[0] == '1') return true;
+    const double slots = (double)g.block_count * g.halves * g.d_qk * 4 * 2;
+    const double pass = (double)g.block_count * g.block_size * 4 + (double)g.block_count * g.block_size * g.d_qk * 2 / g.group;
+    return slots < 0.5 * pass;
+}
+
 struct Plan {
     Geometry g;
     bool fp16, det;
-    bool ds_path;                     // dQ from the stored dS by the fixed-order pass (else fp32 reductions)
+    bool ds_path;                     // dQ by a fixed-order pass after the main kernel (else fp32 reductions)
+    bool slot_path;                   // ... summing per-slot dQ partials (else from the stored dS)
     // byte offsets inside the workspace
     size_t o_hdr, o_cu_q, o_cu_kv, o_item_base, o_unit_base, o_wtab_base, o_count, o_offset, o_cursor, o_scan,
         o_entries, o_wtab, o_delta, o_lse2, o_dq_acc, o_ds, o_dkv, total;
@@ -177,12 +194,15 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
         if (!p->use_tc) return SAG_ERR_UNSUPPORTED;
     }
     g.halves = g.block_size > 64 ? g.block_size / 64 : 1;
+    g.dq_slots = 0;
     // token windows: tensor-core default mode on problems whose dQ accumulator
     // is well beyond L2.  SELATTN_WINDOW_TOKENS sets the window length (and
     // forces windows on smaller problems too).
     const char *wenv = getenv(forward ? "SELATTN_FWD_WINDOW_TOKENS" : "SELATTN_WINDOW_TOKENS");
     const int acc_cols = forward ? g.d_v : g.d_qk;
     if (!forward && !p->det) p->ds_path = prefer_dq_pass(g);
+    p->slot_path = !forward && p->ds_path && p->use_tc && prefer_dq_slots(g);
+    g.dq_slots = p->slot_path ? 1 : 0;
     g.windowed = p->use_tc && !p->ds_path &&
                  (rows * acc_cols * 4 > (forward ? kFwdWindowMinAcc : kWindowMinAcc) || (wenv && atoll(wenv) > 0));
     if (wenv && atoll(wenv) < 0) g.windowed = false;
@@ -225,7 +245,9 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     p->o_delta = take(sizeof(float) * rows);
     p->o_lse2 = take(sizeof(float) * rows);
     p->o_dq_acc = p->ds_path ? o : take(sizeof(float) * rows * g.d_qk);
-    const int64_t ds_per_token = (int64_t)g.n2 * g.block_count * g.group * g.block_size * 2;
+    const int64_t ds_per_token = p->slot_path
+                                     ? (int64_t)g.n1 * g.block_count * g.halves * g.d_qk * 4
+                                     : (int64_t)g.n2 * g.block_count * g.group * g.block_size * 2;
     int64_t chunk = kDsChunkBytes / ds_per_token;
     // SELATTN_DS_CHUNK_TOKENS sets the chunk length (tests run the chunked
     // path on small problems with it)
@@ -265,7 +287,8 @@ Workspace carve(const Plan &p, void *base) {
     w.delta = reinterpret_cast<float *>(c + p.o_delta);
     w.lse2 = reinterpret_cast<float *>(c + p.o_lse2);
     w.dq_acc = p.ds_path ? nullptr : reinterpret_cast<float *>(c + p.o_dq_acc);
-    w.ds = p.ds_path ? reinterpret_cast<uint16_t *>(c + p.o_ds) : nullptr;
+    w.ds = (p.ds_path && !p.slot_path) ? reinterpret_cast<uint16_t *>(c + p.o_ds) : nullptr;
+    w.dq_part = p.slot_path ? reinterpret_cast<float *>(c + p.o_ds) : nullptr;
     w.dkv_acc = (p.n_chunks > 1 || p.g.windowed) ? reinterpret_cast<float *>(c + p.o_dkv) : nullptr;
     w.unit_base = reinterpret_cast<int64_t *>(c + p.o_unit_base);
     w.wtab_base = reinterpret_cast<int64_t *>(c + p.o_wtab_base);
@@ -332,7 +355,7 @@ extern "C" sag_status sel_attn_grad_plan_info(const sag_desc *desc, sag_plan_inf
     info->token_chunks = p.n_chunks;
     info->items = p.g.n_items;
     info->main_kernel = p.use_tc ? 1 : 0;
-    info->dq_path = p.ds_path ? 1 : 0;
+    info->dq_path = p.slot_path ? 2 : p.ds_path ? 1 : 0;
     return SAG_OK;
 }
 
@@ -459,7 +482,7 @@ extern "C" sag_status sel_attn_grad_ex(const sag_desc *desc, const sag_io *io, v
         return SAG_OK;
     }
     // deterministic mode (or the dQ pass chosen for the default mode): token
-    // chunks in order; dS of a chunk -> its dQ
+    // chunks in order; dS (or the per-slot dQ partials) of a chunk -> its dQ
     if (g.chunked && cudaMemsetAsync(ws.dkv_acc, 0, sizeof(float) * (size_t)g.t2 * g.n2 * (g.d_qk + g.d_v), s) !=
                          cudaSuccess)
         return SAG_ERR_CUDA;
@@ -469,9 +492,10 @@ extern "C" sag_status sel_attn_grad_ex(const sag_desc *desc, const sag_io *io, v
         gc.tok_lo = c * p.chunk_tokens;
         gc.tok_hi = gc.tok_lo + p.chunk_tokens < g.t1 ? gc.tok_lo + p.chunk_tokens : g.t1;
         if (launch_main(p, gc, ws, *io, true, s, sms) != cudaSuccess) return SAG_ERR_CUDA;
-        if (((p.use_tc && dq_tc_supported(gc)) ? launch_dq_tc(gc, ws, *io, p.fp16, s, sms)
-                                                : launch_dq_from_ds(gc, ws, *io, p.fp16, s, sms)) != cudaSuccess)
-            return SAG_ERR_CUDA;
+        const cudaError_t e = p.slot_path ? launch_dq_slots(gc, ws, *io, p.fp16, s, sms)
+                              : (p.use_tc && dq_tc_supported(gc)) ? launch_dq_tc(gc, ws, *io, p.fp16, s, sms)
+                                                                  : launch_dq_from_ds(gc, ws, *io, p.fp16, s, sms);
+        if (e != cudaSuccess) return SAG_ERR_CUDA;
     }
     if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return SAG_ERR_CUDA;
     if (g.chunked && (launch_cast_dkv(g, ws, io->dk, io->dk_rope, io->dv, p.fp16, s, sms)) != cudaSuccess)

@@ -16,6 +16,8 @@
 // elected lane issuing each tcgen05 instruction.
 #include <stdlib.h>
 
+#include <type_traits>
+
 #include "kernels.cuh"
 #include "tc.cuh"
 #include "tile.cuh"
@@ -45,8 +47,9 @@ struct Smem {
     static constexpr int OFF_DS = OFF_P + 16384;
     static constexpr int OFF_STG = OFF_DS + 16384;       // 4 epilogue warps x 4 KB
     static constexpr int OFF_META = OFF_STG + 16384;     // kMeta x 128 ints
-    static constexpr int OFF_BAR = OFF_META + kMeta * kRows * 4;
-    static constexpr int TOTAL = OFF_BAR + 256 + 1024;   // + slack for 1024-B alignment
+    static constexpr int OFF_RING = OFF_META + kMeta * kRows * 4;   // kURing unit ids
+    static constexpr int OFF_BAR = OFF_RING + 64;
+    static constexpr int TOTAL = OFF_BAR + 512 + 1024;   // + slack for 1024-B alignment
 };
 
 // S_FREE: the softmax has read S (TMEM columns reusable); P_FULL / DS_FULL:
@@ -57,8 +60,11 @@ struct Smem {
 enum Bar {
     B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL, B_Q_EMPTY0 = B_Q_FULL + 6, B_Q_EMPTY1, B_DO_FULL,
     B_DO_EMPTY0 = B_DO_FULL + 4, B_DO_EMPTY1, B_S_FULL, B_S_FREE, B_P_FULL, B_P_FREE, B_DP_FULL, B_DS_FULL,
-    B_DS_FREE, B_MMA_DONE, B_DQ_FREE, B_ACC_FULL, B_ACC_FREE, B_DRAIN, B_COUNT
+    B_DS_FREE, B_MMA_DONE, B_DQ_FREE, B_ACC_FULL, B_ACC_FREE, B_DRAIN, B_U_FULL, B_U_EMPTY = B_U_FULL + kURing,
+    B_COUNT = B_U_EMPTY + kURing
 };
+// warps that read the unit ring: MMA, 4 softmax, 4 epilogue
+constexpr int kRingReaders = 9;
 
 struct TcArgs {
     Geometry g;
@@ -88,6 +94,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = A.nk, tpt = A.tpt, G = g.group;
     const bool det = A.deterministic != 0;
+    // fixed-order dQ: from the stored dS (a later pass re-reads the key
+    // blocks), or from per-slot fp32 partials of dQ = dS K stored here
+    const bool store_ds = det && !g.dq_slots;
     const uint32_t sbase = tc::smem_u32(smem);
     // 64-column chunk c of a q / k row: the main tensor at column 64 c, or
     // with the rope split chunk 2 from the rope tensor at column 0
@@ -118,6 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init(&bars[B_ACC_FULL], 1);
         tc::mbar_init(&bars[B_ACC_FREE], 128);
         tc::mbar_init(&bars[B_DRAIN], 1);
+        for (int q = 0; q < kURing; ++q) {
+            tc::mbar_init(&bars[B_U_FULL + q], 1);
+            tc::mbar_init(&bars[B_U_EMPTY + q], kRingReaders);
+        }
         tc::fence_mbar_init();
     }
     // rows of a Q / dY tile no token fills (when G does not divide 128) must
@@ -140,6 +153,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
         raise_error(&ws.hdr->error, SAG_ERR_TIMEOUT);
     };
+    // work units come from the launch's ticket counter (hot buckets are much
+    // larger than cold ones: a static split would leave SMs idle)
+    const UnitRing ring{reinterpret_cast<int64_t *>(smem + L::OFF_RING), &bars[B_U_FULL], &bars[B_U_EMPTY]};
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -179,7 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ne = 0, tc_i = 0;
         uint32_t armed_kv = 0, armed_q[2] = {0, 0}, armed_do[2] = {0, 0};
         bool ok = true;
-        for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
+        for (int k = 0; ok; ++k) {
+            const int64_t ti = ring_take(ring, &ws.hdr->work_counter, k, abort_flag, lane);
+            if (ti < 0) { ok = false; break; }
+            if (ti >= g.n_units) break;
             const KeyTile kt = decode(g, ws, ti, nk, tpt);
             if (kt.ntok == 0) continue;
             if (ne > 0 && !tc::mbar_wait(&bars[B_KV_EMPTY], (ne - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
@@ -312,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         id_t, (il > 0) || (kk > 0));
             }
             tc::mma_commit_warp(&bars[B_Q_EMPTY0 + (t & 1)]);
-            if (!det) {
+            if (!store_ds) {
                 // dQ = dS K (A: dS K-major, B: K tile MN-major, N = Dqk)
                 if (t > 0 && !wait(B_DQ_FREE, (t - 1) & 1)) return false;
                 tc::tc_fence_after();
@@ -326,7 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_commit_warp(&bars[B_MMA_DONE]);
             return true;
         };
-        for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
+        for (int k = 0; ok; ++k) {
+            const int64_t ti = ring_read(ring, k, abort_flag, lane);
+            if (ti < 0) { ok = false; break; }
+            if (ti >= g.n_units) break;
             const KeyTile kt = decode(g, ws, ti, nk, tpt);
             if (kt.ntok == 0) continue;
             if (!wait(B_KV_FULL, ne & 1)) { ok = false; break; }
@@ -393,7 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *drow = smem + L::OFF_DS;
         int tc_i = 0;
         bool ok = true;
-        for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
+        for (int k = 0; ok; ++k) {
+            const int64_t ti = ring_read(ring, k, abort_flag, lane);
+            if (ti < 0) { ok = false; break; }
+            if (ti >= g.n_units) break;
             const KeyTile kt = decode(g, ws, ti, nk, tpt);
             if (kt.ntok == 0) continue;
             for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
@@ -467,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (c < nk / 8)
                         *reinterpret_cast<uint4 *>(drow + sw_off(r, c)) =
                             make_uint4(dk2[c * 4], dk2[c * 4 + 1], dk2[c * 4 + 2], dk2[c * 4 + 3]);
-                if (det && valid) {
+                if (store_ds && valid) {
                     // dS[t - tok_lo][n2][slot][g][key] in the input dtype
                     const int t = ent / g.block_count, slot = ent % g.block_count;
                     const int64_t base =
@@ -494,7 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int et = threadIdx.x - 192;                 // 0..127
         int ne = 0, tc_i = 0;
         bool ok = true;
-        for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
+        for (int k = 0; ok; ++k) {
+            const int64_t ti = ring_read(ring, k, abort_flag, lane);
+            if (ti < 0) { ok = false; break; }
+            if (ti >= g.n_units) break;
             const KeyTile kt = decode(g, ws, ti, nk, tpt);
             if (kt.ntok == 0) {
                 if (!g.chunked && !g.windowed) {
@@ -508,36 +536,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
-                if (det) continue;
+                if (store_ds) continue;
                 ok = tc::mbar_wait(&bars[B_MMA_DONE], tc_i & 1, abort_flag, kWaitNs);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc::tc_fence_after();
                 const int ent = tt < tpt ? meta[(tc_i % kMeta) * kRows + tt] : -1;
-                const int64_t grow = ent >= 0 ? (int64_t)(ent / g.block_count) * g.n1 + kt.n2 * G + gg : -1;
-                for (int c = 0; c < DQK / 32; ++c) {
-                    uint32_t v0[16], v1[16];
-                    tc::tmem_ld16(trow + kColDQ + c * 32, v0);
-                    tc::tmem_ld16(trow + kColDQ + c * 32 + 16, v1);
-                    tc::tmem_wait_ld();
-                    // stage the warp's 32 rows x 32 floats, then red whole row segments
-#pragma unroll
-                    for (int j4 = 0; j4 < 4; ++j4)
-                        *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j4 ^ (lane & 7)) << 4)) =
-                            make_uint4(v0[4 * j4], v0[4 * j4 + 1], v0[4 * j4 + 2], v0[4 * j4 + 3]);
-#pragma unroll
-                    for (int j4 = 0; j4 < 4; ++j4)
-                        *reinterpret_cast<uint4 *>(stg + lane * 128 + (((j4 + 4) ^ (lane & 7)) << 4)) =
-                            make_uint4(v1[4 * j4], v1[4 * j4 + 1], v1[4 * j4 + 2], v1[4 * j4 + 3]);
-                    __syncwarp();
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int rr = k * 4 + (lane >> 3), j4 = lane & 7;
-                        const int64_t gr = __shfl_sync(0xffffffffu, grow, rr);
-                        const float4 x = *reinterpret_cast<const float4 *>(stg + rr * 128 + ((j4 ^ (rr & 7)) << 4));
-                        if (gr >= 0) tc::red_add_v4(ws.dq_acc + gr * DQK + c * 32 + j4 * 4, x.x, x.y, x.z, x.w);
+                // the tile into the fp32 accumulator (reductions) or into its
+                // partial rows (stores); the choice is taken outside the loop
+                auto drain = [&](auto slots) {
+                    // destination row (of Dqk floats): the query row of the dQ
+                    // accumulator, or the (row, slot, key tile) partial
+                    int64_t grow = -1;
+                    if constexpr (decltype(slots)::value) {
+                        if (ent >= 0)
+                            grow = (((int64_t)(ent / g.block_count - g.tok_lo) * g.n1 + kt.n2 * G + gg) *
+                                        g.block_count + ent % g.block_count) * g.halves + kt.koff / nk;
+                    } else {
+                        grow = ent >= 0 ? (int64_t)(ent / g.block_count) * g.n1 + kt.n2 * G + gg : -1;
                     }
-                    __syncwarp();
-                }
+                    for (int c = 0; c < DQK / 32; ++c) {
+                        uint32_t v0[16], v1[16];
+                        tc::tmem_ld16(trow + kColDQ + c * 32, v0);
+                        tc::tmem_ld16(trow + kColDQ + c * 32 + 16, v1);
+                        tc::tmem_wait_ld();
+                        // stage the warp's 32 rows x 32 floats, then red whole row segments
+#pragma unroll
+                        for (int j4 = 0; j4 < 4; ++j4)
+                            *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j4 ^ (lane & 7)) << 4)) =
+                                make_uint4(v0[4 * j4], v0[4 * j4 + 1], v0[4 * j4 + 2], v0[4 * j4 + 3]);
+#pragma unroll
+                        for (int j4 = 0; j4 < 4; ++j4)
+                            *reinterpret_cast<uint4 *>(stg + lane * 128 + (((j4 + 4) ^ (lane & 7)) << 4)) =
+                                make_uint4(v1[4 * j4], v1[4 * j4 + 1], v1[4 * j4 + 2], v1[4 * j4 + 3]);
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int rr = k * 4 + (lane >> 3), j4 = lane & 7;
+                            const int64_t gr = __shfl_sync(0xffffffffu, grow, rr);
+                            const float4 x = *reinterpret_cast<const float4 *>(stg + rr * 128 + ((j4 ^ (rr & 7)) << 4));
+                            if (gr < 0) continue;
+                            if constexpr (decltype(slots)::value)
+                                __stcs(reinterpret_cast<float4 *>(ws.dq_part + gr * DQK + c * 32 + j4 * 4), x);
+                            else
+                                tc::red_add_v4(ws.dq_acc + gr * DQK + c * 32 + j4 * 4, x.x, x.y, x.z, x.w);
+                        }
+                        __syncwarp();
+                    }
+                };
+                if (g.dq_slots) drain(std::true_type{});
+                else drain(std::false_type{});
                 tc::tc_fence_before();
                 tc::mbar_arrive(&bars[B_DQ_FREE]);
             }
@@ -632,6 +679,8 @@ static cudaError_t launch_tc_t(const Geometry &g, const Workspace &ws, const sag
     if (e != cudaSuccess) return e;
     int64_t grid = a.n_titems < num_sms ? a.n_titems : num_sms;
     if (grid < 1) grid = 1;
+    // the launch's CTAs take their units from this counter
+    if ((e = cudaMemsetAsync(&ws.hdr->work_counter, 0, sizeof(ws.hdr->work_counter), s)) != cudaSuccess) return e;
     fn<<<(int)grid, kThreads, smem, s>>>(m.q, mdo, m.k, mv, m.qr, m.kr, a);
     return cudaGetLastError();
 }

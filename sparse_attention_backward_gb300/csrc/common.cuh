@@ -63,14 +63,16 @@ struct Geometry {
     int32_t window;           // tokens per window
     int32_t halves;           // key tiles per block (block_size / key tile)
     int32_t d_rope;           // columns [d_qk - d_rope, d_qk) of q / k live in the rope tensors
+    int32_t dq_slots;         // 1: fixed-order dQ from fp32 partials per (row, slot, key tile)
     int64_t n_units;          // work units of the main kernel
 };
 
 // Workspace header (first 256 bytes).
 struct WsHeader {
     int32_t error;            // sag_status recorded by the device
-    int32_t work_counter;     // dynamic scheduler ticket
-    int32_t pad[62];
+    int32_t pad0;
+    unsigned long long work_counter;   // next work unit of a dynamically scheduled launch
+    int32_t pad[60];
 };
 
 // Device pointers carved out of the caller's workspace.
@@ -90,6 +92,7 @@ struct Workspace {
     float *lse2;              // [T1 * n1]  (max + ln sum) * log2(e)
     float *dq_acc;            // [T1 * n1 * d_qk] fp32 dQ accumulator (default mode)
     uint16_t *ds;             // [chunk tokens * n2 * count * G * bs] dS in the input dtype (deterministic)
+    float *dq_part;           // [chunk tokens * n1 * count * halves * d_qk] fp32 dQ partials (dq_slots)
     float *dkv_acc;           // [T2 * n2 * (d_qk + d_v)] fp32 dK|dV carried across chunks / windows
     int64_t *unit_base;       // [B+1] first work unit of each batch (windowed)
     int64_t *wtab_base;       // [B+1] first window-table entry of each batch (windowed)

@@ -65,6 +65,11 @@ cudaError_t launch_fwd_finalize(const Geometry &g, const Workspace &ws, void *o,
 // dQ from the stored dS, fixed order (deterministic mode).
 cudaError_t launch_dq_from_ds(const Geometry &g, const Workspace &ws, const sag_io &io, bool fp16, cudaStream_t s,
                               int num_sms);
+// Fixed-order dQ from the per-slot fp32 partials of one token chunk
+// (Geometry::dq_slots): dQ = scale * sum over the row's selections in list
+// order, cast to the dtype (prep.cu).
+cudaError_t launch_dq_slots(const Geometry &g, const Workspace &ws, const sag_io &io, bool fp16, cudaStream_t s,
+                            int num_sms);
 
 // Lightning-indexer backward (tensor cores): head dim 128, G = n1 / n2 <= 64.
 // Geometry: t1 / t2 rows, n1, n2, group, block_count = topk; Workspace: hdr,

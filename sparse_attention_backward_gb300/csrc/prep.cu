@@ -353,6 +353,74 @@ __global__ void __launch_bounds__(256) k_cast_dq(Geometry g, const float *__rest
 }
 
 // ---------------------------------------------------------------------------
+// Fixed-order dQ from per-slot partials.  The main kernel stored, for every
+// (query row, selection slot, key tile of the block), the fp32 partial
+// dS_tile K_tile of that row; here one warp per row of the token chunk sums
+// them in list order (slot, then tile) and writes scale * sum in the dtype
+// (dQ = dS K / sqrt(d), README function description).  Slots whose id is
+// empty, out of range or on a padding token were never stored; they are
+// skipped by the test the inversion applies.  Eight slots are loaded before
+// they are added, always in the same order.
+template <bool kFp16, int DQK>
+__global__ void __launch_bounds__(256) k_dq_slot_sum(Geometry g, Workspace ws, const int32_t *__restrict__ topk,
+                                                     uint16_t *__restrict__ dq, uint16_t *__restrict__ dq_rope) {
+    constexpr int V4 = DQK / 4;                 // float4 per row: 32 or 48
+    constexpr int PER = (V4 + 31) / 32;         // per lane: 1 or 2
+    constexpr int U = 8;                        // slots in flight
+    const int lane = threadIdx.x & 31;
+    const int nsl = g.block_count * g.halves;
+    const int64_t nrows = (int64_t)(g.tok_hi - g.tok_lo) * g.n1;
+    const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r = (((int64_t)blockIdx.x * blockDim.x) >> 5) + (threadIdx.x >> 5); r < nrows; r += warps) {
+        const int t = g.tok_lo + (int)(r / g.n1), h = (int)(r % g.n1);
+        const int b = batch_of(ws.cu_q, g.batch, t);
+        const int nblk = t < ws.q_end[b] ? ws.kv_blocks[b] : 0;
+        const int32_t *ids = topk + ((int64_t)t * g.n2 + h / g.group) * g.block_count;
+        const float4 *part = reinterpret_cast<const float4 *>(ws.dq_part) + r * nsl * V4;
+        float4 acc[PER];
+#pragma unroll
+        for (int q = 0; q < PER; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j0 = 0; j0 < nsl; j0 += U) {
+            float4 v[U][PER];
+            bool use[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = j0 + u;
+                int id = -1;
+                if (j < nsl) id = __ldg(ids + j / g.halves);
+                use[u] = id >= 0 && id < nblk;
+#pragma unroll
+                for (int q = 0; q < PER; ++q) {
+                    const int c = lane + 32 * q;
+                    v[u][q] = (use[u] && c < V4) ? __ldcs(part + (int64_t)j * V4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (use[u])
+#pragma unroll
+                    for (int q = 0; q < PER; ++q) {
+                        acc[q].x += v[u][q].x;
+                        acc[q].y += v[u][q].y;
+                        acc[q].z += v[u][q].z;
+                        acc[q].w += v[u][q].w;
+                    }
+        }
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            const int c = lane + 32 * q;
+            if (c >= V4) continue;
+            ushort4 o;
+            o.x = f_to_u16<kFp16>(acc[q].x * g.scale);
+            o.y = f_to_u16<kFp16>(acc[q].y * g.scale);
+            o.z = f_to_u16<kFp16>(acc[q].z * g.scale);
+            o.w = f_to_u16<kFp16>(acc[q].w * g.scale);
+            *reinterpret_cast<ushort4 *>(split_col(dq, dq_rope, (int64_t)t * g.n1 + h, 4 * c, DQK, g.d_rope)) = o;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host launchers.
 static int grid_for(int64_t work, int per_block, int max_blocks) {
     int64_t b = (work + per_block - 1) / per_block;
@@ -408,6 +476,26 @@ cudaError_t launch_cast_dq(const Geometry &g, const float *dq_acc, void *dq, voi
     if (fp16) k_cast_dq<true><<<grid, 256, 0, s>>>(g, dq_acc, (uint16_t *)dq, (uint16_t *)dq_rope, n4);
     else k_cast_dq<false><<<grid, 256, 0, s>>>(g, dq_acc, (uint16_t *)dq, (uint16_t *)dq_rope, n4);
     return cudaGetLastError();
+}
+
+template <bool kFp16, int DQK>
+static cudaError_t launch_dq_slots_t(const Geometry &g, const Workspace &ws, const sag_io &io, cudaStream_t s,
+                                     int num_sms) {
+    const int64_t rows = (int64_t)(g.tok_hi - g.tok_lo) * g.n1;
+    if (rows == 0) return cudaSuccess;
+    const int grid = grid_for(rows, 8, num_sms * 8);
+    k_dq_slot_sum<kFp16, DQK><<<grid, 256, 0, s>>>(g, ws, io.topk_indices, (uint16_t *)io.dq, (uint16_t *)io.dq_rope);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dq_slots(const Geometry &g, const Workspace &ws, const sag_io &io, bool fp16, cudaStream_t s,
+                            int num_sms) {
+    if (g.d_qk != 128 && g.d_qk != 192) return cudaErrorInvalidValue;
+    if (fp16)
+        return g.d_qk == 192 ? launch_dq_slots_t<true, 192>(g, ws, io, s, num_sms)
+                             : launch_dq_slots_t<true, 128>(g, ws, io, s, num_sms);
+    return g.d_qk == 192 ? launch_dq_slots_t<false, 192>(g, ws, io, s, num_sms)
+                         : launch_dq_slots_t<false, 128>(g, ws, io, s, num_sms);
 }
 
 }  // namespace sag

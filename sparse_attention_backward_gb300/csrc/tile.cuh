@@ -4,6 +4,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace sag {
 namespace {
@@ -66,6 +67,42 @@ __device__ __forceinline__ KeyTile decode(const Geometry &g, const Workspace &ws
     kt.key0 = ws.cu_kv[kt.b] + (int64_t)kb * g.block_size + kt.koff;
     kt.ntiles = (kt.ntok + tpt - 1) / tpt;
     return kt;
+}
+
+// Dynamic work distribution.  Warp 0 of a CTA takes the next work unit from
+// a launch-wide ticket counter (atomic add) and publishes it in a small shared
+// ring; every other role reads the units from the ring in the same order.  A
+// unit index >= n_units ends the sequence.  The functions are warp-collective
+// and return -1 when a bounded wait ran out.
+constexpr int kURing = 4;
+struct UnitRing {
+    int64_t *slot;          // [kURing] in shared memory
+    uint64_t *full;         // [kURing] mbarriers, one arrival (the producer)
+    uint64_t *empty;        // [kURing] mbarriers, one arrival per consumer warp
+};
+
+__device__ __forceinline__ int64_t ring_take(const UnitRing &r, unsigned long long *counter, int k,
+                                             volatile int *abort, int lane) {
+    const int q = k % kURing;
+    if (k >= kURing &&
+        !__all_sync(0xffffffffu, tc::mbar_wait(&r.empty[q], ((k / kURing) - 1) & 1, abort, kWaitNs)))
+        return -1;
+    int64_t ti = 0;
+    if (lane == 0) {
+        ti = (int64_t)atomicAdd(counter, 1ull);
+        r.slot[q] = ti;
+        tc::mbar_arrive(&r.full[q]);
+    }
+    return __shfl_sync(0xffffffffu, ti, 0);
+}
+
+__device__ __forceinline__ int64_t ring_read(const UnitRing &r, int k, volatile int *abort, int lane) {
+    const int q = k % kURing;
+    if (!__all_sync(0xffffffffu, tc::mbar_wait(&r.full[q], (k / kURing) & 1, abort, kWaitNs))) return -1;
+    const int64_t ti = *reinterpret_cast<volatile int64_t *>(&r.slot[q]);
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&r.empty[q]);
+    return ti;
 }
 
 __device__ __forceinline__ float ex2(float x) {

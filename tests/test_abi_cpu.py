@@ -224,15 +224,31 @@ def test_bsnd_and_rope_descriptors(lib):
 
 
 def test_dq_path_of_the_plan(lib, monkeypatch):
-    """The deterministic mode always forms dQ by the fixed-order pass; the
-    default mode reduces it in the main kernel on the five workloads (the
-    pass would move more bytes on each), unless SELATTN_DQ_PASS forces it."""
+    """The deterministic mode always forms dQ by a fixed-order pass: from the
+    stored dS, or (small blocks and groups: the small-group workload) from
+    per-slot fp32 partials; the default mode reduces it in the main kernel on
+    the five workloads (the pass would move more bytes on each), unless
+    SELATTN_DQ_PASS forces it."""
     import synth
     for w in synth.WORKLOADS:
         for det in (False, True):
             d = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
                               sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, det)
-            assert sab.plan_info(d).dq_path == (1 if det else 0), (w.name, det)
+            want = (2 if w.name == "small_group" else 1) if det else 0
+            assert sab.plan_info(d).dq_path == want, (w.name, det)
+    # the per-slot partials take count * halves * d_qk fp32 per query row
+    w = synth.WORKLOADS[4]
+    d = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
+                      sab.SAG_FP16, True)
+    monkeypatch.setenv("SELATTN_DQ_SLOTS", "0")
+    small = sab.plan_info(d).workspace_bytes
+    monkeypatch.setenv("SELATTN_DQ_SLOTS", "1")
+    big = sab.plan_info(d).workspace_bytes
+    t1 = w.cu_q[-1]
+    parts = t1 * w.n1 * w.block_count * w.d_qk * 4
+    dss = t1 * w.n2 * w.block_count * (w.n1 // w.n2) * w.block_size * 2
+    assert big - small == parts - dss
+    monkeypatch.delenv("SELATTN_DQ_SLOTS")
     monkeypatch.setenv("SELATTN_DQ_PASS", "1")
     w = synth.WORKLOADS[2]
     d = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale)

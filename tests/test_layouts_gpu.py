@@ -212,9 +212,12 @@ def test_bsnd_forward(bsnd_data, name):
         assert not S.f64(o[b, n:]).any() and not m[b, n:].any() and not l[b, n:].any()
 
 
-def test_bsnd_with_rope_split_chunked_deterministic(bsnd_data, monkeypatch):
-    """Both at once, in the deterministic mode's chunked path."""
+@pytest.mark.parametrize("slots", ["0", "1"])
+def test_bsnd_with_rope_split_chunked_deterministic(bsnd_data, slots, monkeypatch):
+    """Both at once, in the deterministic mode's chunked path, with dQ from
+    the stored dS or from per-slot partials."""
     monkeypatch.setenv("SELATTN_DS_CHUNK_TOKENS", "900")
+    monkeypatch.setenv("SELATTN_DQ_SLOTS", slots)
     w, xb, s1, s2, (rdq, rdk, rdv), _ = bsnd_data("varlen")
     t = {k: v.cuda() for k, v in xb.items()}
     q, qr = _split(t["q"])

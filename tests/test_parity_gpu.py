@@ -186,6 +186,46 @@ def test_deterministic_token_chunks(small_data, name, chunk, monkeypatch):
         assert torch.equal(u.view(torch.int16), v.view(torch.int16))
 
 
+@pytest.mark.parametrize("slots", ["0", "1"])
+@pytest.mark.parametrize("name", ["tiny", "varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127"])
+def test_deterministic_dq_sources(small_data, name, slots, monkeypatch):
+    """Deterministic mode with dQ summed from per-slot fp32 partials (the
+    plan's choice for small blocks and groups) or from the stored dS, each
+    forced on: parity with the oracle, bit-identical over two runs."""
+    monkeypatch.setenv("SELATTN_DQ_SLOTS", slots)
+    w, x, (rdq, rdk, rdv) = small_data(name)
+    desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
+                         sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, True)
+    assert sab.plan_info(desc).dq_path == (2 if slots == "1" else 1)
+    a = _run(w, x, True)
+    S.assert_close(f"{name} slots={slots} dq", S.f64(a[0]), rdq)
+    S.assert_close(f"{name} slots={slots} dk", S.f64(a[1]), rdk)
+    S.assert_close(f"{name} slots={slots} dv", S.f64(a[2]), rdv)
+    b = _run(w, x, True)
+    for u, v in zip(a, b):
+        assert torch.equal(u.view(torch.int16), v.view(torch.int16))
+
+
+@pytest.mark.parametrize("name,chunk", [("varlen", 1000), ("g32_bs128", 7), ("ragged_fp16", 30)])
+def test_slot_partials_in_token_chunks(small_data, name, chunk, monkeypatch):
+    """The per-slot dQ partials of a token chunk indexed from the chunk's first
+    token: several chunks, parity and bit-identical repeats."""
+    monkeypatch.setenv("SELATTN_DQ_SLOTS", "1")
+    monkeypatch.setenv("SELATTN_DS_CHUNK_TOKENS", str(chunk))
+    w, x, (rdq, rdk, rdv) = small_data(name)
+    desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
+                         sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, True)
+    info = sab.plan_info(desc)
+    assert info.dq_path == 2 and info.token_chunks == -(-w.t1 // chunk) >= 3
+    a = _run(w, x, True)
+    S.assert_close(f"{name} slot chunks dq", S.f64(a[0]), rdq)
+    S.assert_close(f"{name} slot chunks dk", S.f64(a[1]), rdk)
+    S.assert_close(f"{name} slot chunks dv", S.f64(a[2]), rdv)
+    b = _run(w, x, True)
+    for u, v in zip(a, b):
+        assert torch.equal(u.view(torch.int16), v.view(torch.int16))
+
+
 def test_bucket_beyond_the_shared_memory_sort():
     """Every one of 40000 query tokens selects block 0 (as NSA's always-kept
     first block would be): a bucket of 40000 entries, sorted in place through
@@ -211,19 +251,21 @@ def test_bucket_beyond_the_shared_memory_sort():
         assert torch.equal(u.view(torch.int16), v.view(torch.int16))
 
 
+@pytest.mark.parametrize("slots", ["0", "1"])
 @pytest.mark.parametrize("name", ["varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127"])
-def test_default_mode_with_the_dq_pass(small_data, name, monkeypatch):
-    """The default mode with dQ formed from the stored dS by the fixed-order
-    pass (the plan's other dQ path), forced on."""
+def test_default_mode_with_the_dq_pass(small_data, name, slots, monkeypatch):
+    """The default mode with dQ formed by a fixed-order pass (the plan's other
+    dQ paths: from the stored dS or from per-slot partials), forced on."""
     monkeypatch.setenv("SELATTN_DQ_PASS", "1")
+    monkeypatch.setenv("SELATTN_DQ_SLOTS", slots)
     w, x, (rdq, rdk, rdv) = small_data(name)
     desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
                          sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, False)
-    assert sab.plan_info(desc).dq_path == 1
+    assert sab.plan_info(desc).dq_path == (2 if slots == "1" else 1)
     dq, dk, dv = _run(w, x, False)
-    S.assert_close(f"{name} dq pass dq", S.f64(dq), rdq)
-    S.assert_close(f"{name} dq pass dk", S.f64(dk), rdk)
-    S.assert_close(f"{name} dq pass dv", S.f64(dv), rdv)
+    S.assert_close(f"{name} dq pass slots={slots} dq", S.f64(dq), rdq)
+    S.assert_close(f"{name} dq pass slots={slots} dk", S.f64(dk), rdk)
+    S.assert_close(f"{name} dq pass slots={slots} dv", S.f64(dv), rdv)
 
 
 def test_bounded_wait_runs_out_and_the_context_stays_usable(small_data):
