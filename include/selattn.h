@@ -288,8 +288,8 @@ sag_status sel_attn_grad_timed(const sag_desc *desc, const void *query, const vo
  *     what has to start at zero, so earlier contents do not matter, but calls
  *     whose work overlaps on the GPU (different streams, or another thread)
  *     race on it: serialise them.
- *   - The device status (SAG_ERR_INDEX, ...) is not readable through
- *     sel_attn_grad_query_error, which needs the workspace pointer.
+ *   - The device status (SAG_ERR_INDEX, ...) lives in the fixed array:
+ *     sel_attn_grad_noalloc_query_error reads it.
  * Returns the statuses of sel_attn_grad, or SAG_ERR_WORKSPACE as above.
  */
 #define SEL_ATTN_GRAD_NOALLOC_MAX_SCRATCH ((size_t)64 << 20)
@@ -299,6 +299,15 @@ sag_status sel_attn_grad_noalloc(const sag_desc *desc, const void *query, const 
                                  const void *attention_out_grad, const float *softmax_max,
                                  const float *softmax_sum, const int32_t *topk_indices, void *dq,
                                  void *dk, void *dv, void *stream);
+
+/*
+ * sel_attn_grad_query_error for the allocation-free path: synchronises
+ * `stream` and returns the device-recorded status of the last
+ * sel_attn_grad_noalloc on the stream's device (SAG_OK, SAG_ERR_INDEX,
+ * SAG_ERR_TIMEOUT), or SAG_ERR_CUDA.  The status is that of the shared array:
+ * with overlapping calls it belongs to whichever wrote it last.
+ */
+sag_status sel_attn_grad_noalloc_query_error(void *stream);
 
 /*
  * Forward of selected attention: the step before the backward, producing the

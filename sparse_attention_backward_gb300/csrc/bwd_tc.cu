@@ -23,8 +23,6 @@
 // 2-5 softmax / dS (thread = query row = TMEM lane), 6-9 epilogue (dQ reds per
 // tile, dK / dV per key tile).  Every wait is bounded; a timeout records
 // SAG_ERR_TIMEOUT and the CTA winds down.
-#include <type_traits>
-
 #include "kernels.cuh"
 #include "tc.cuh"
 #include "tile.cuh"
@@ -75,7 +73,12 @@ struct TcArgs {
     int64_t n_titems;
 };
 
-template <bool kFp16, int DQK, bool kWarpIssue>
+// dQ modes of a launch (compile-time, so each mode's loops carry no branch
+// for the others): reductions into the fp32 accumulator, dS stored for the
+// fixed-order pass, or per-slot fp32 partials for the summing pass
+enum DqMode { kDqRed = 0, kDqStoreDs = 1, kDqSlots = 2 };
+
+template <bool kFp16, int DQK, int kMode>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     k_bwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
              const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -94,10 +97,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const Workspace &ws = A.ws;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = A.nk, tpt = A.tpt, G = g.group;
-    const bool det = A.deterministic != 0;
     // fixed-order dQ: from the stored dS (a later pass re-reads the key
     // blocks), or from per-slot fp32 partials of dQ = dS K stored here
-    const bool store_ds = det && !g.dq_slots;
+    constexpr bool store_ds = kMode == kDqStoreDs;
+    // the whole MMA warp runs the schedule when dS is stored (see the MMA role)
+    constexpr bool kWarpIssue = kMode == kDqStoreDs;
     const uint32_t sbase = tc::smem_u32(smem);
     // 64-column chunk c of a q / k row: the main tensor at column 64 c, or
     // with the rope split chunk 2 from the rope tensor at column 0
@@ -469,50 +473,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc::tc_fence_after();
                 const int ent = tt < tpt ? meta[(tc_i % kMeta) * kRows + tt] : -1;
-                // the tile into the fp32 accumulator (reductions) or into its
-                // partial rows (stores); the choice is taken outside the loop
-                auto drain = [&](auto slots) {
-                    // destination row (of Dqk floats): the query row of the dQ
-                    // accumulator, or the (row, slot, key tile) partial
-                    int64_t grow = -1;
-                    if constexpr (decltype(slots)::value) {
-                        if (ent >= 0)
-                            grow = (((int64_t)(ent / g.block_count - g.tok_lo) * g.n1 + kt.n2 * G + gg) *
-                                        g.block_count + ent % g.block_count) * g.halves + kt.koff / nk;
-                    } else {
-                        grow = ent >= 0 ? (int64_t)(ent / g.block_count) * g.n1 + kt.n2 * G + gg : -1;
-                    }
-                    for (int c = 0; c < DQK / 32; ++c) {
-                        uint32_t v0[16], v1[16];
-                        tc::tmem_ld16(trow + kColDQ + c * 32, v0);
-                        tc::tmem_ld16(trow + kColDQ + c * 32 + 16, v1);
-                        tc::tmem_wait_ld();
-                        // stage the warp's 32 rows x 32 floats, then red whole row segments
+                // destination row (of Dqk floats): the query row of the dQ
+                // accumulator, or the (row, slot, key tile) partial
+                int64_t grow = -1;
+                if constexpr (kMode == kDqSlots) {
+                    if (ent >= 0)
+                        grow = (((int64_t)(ent / g.block_count - g.tok_lo) * g.n1 + kt.n2 * G + gg) *
+                                    g.block_count + ent % g.block_count) * g.halves + kt.koff / nk;
+                } else {
+                    grow = ent >= 0 ? (int64_t)(ent / g.block_count) * g.n1 + kt.n2 * G + gg : -1;
+                }
+                for (int c = 0; c < DQK / 32; ++c) {
+                    uint32_t v0[16], v1[16];
+                    tc::tmem_ld16(trow + kColDQ + c * 32, v0);
+                    tc::tmem_ld16(trow + kColDQ + c * 32 + 16, v1);
+                    tc::tmem_wait_ld();
+                    // stage the warp's 32 rows x 32 floats, then red whole row segments
 #pragma unroll
-                        for (int j4 = 0; j4 < 4; ++j4)
-                            *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j4 ^ (lane & 7)) << 4)) =
-                                make_uint4(v0[4 * j4], v0[4 * j4 + 1], v0[4 * j4 + 2], v0[4 * j4 + 3]);
+                    for (int j4 = 0; j4 < 4; ++j4)
+                        *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j4 ^ (lane & 7)) << 4)) =
+                            make_uint4(v0[4 * j4], v0[4 * j4 + 1], v0[4 * j4 + 2], v0[4 * j4 + 3]);
 #pragma unroll
-                        for (int j4 = 0; j4 < 4; ++j4)
-                            *reinterpret_cast<uint4 *>(stg + lane * 128 + (((j4 + 4) ^ (lane & 7)) << 4)) =
-                                make_uint4(v1[4 * j4], v1[4 * j4 + 1], v1[4 * j4 + 2], v1[4 * j4 + 3]);
-                        __syncwarp();
+                    for (int j4 = 0; j4 < 4; ++j4)
+                        *reinterpret_cast<uint4 *>(stg + lane * 128 + (((j4 + 4) ^ (lane & 7)) << 4)) =
+                            make_uint4(v1[4 * j4], v1[4 * j4 + 1], v1[4 * j4 + 2], v1[4 * j4 + 3]);
+                    __syncwarp();
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const int rr = k * 4 + (lane >> 3), j4 = lane & 7;
-                            const int64_t gr = __shfl_sync(0xffffffffu, grow, rr);
-                            const float4 x = *reinterpret_cast<const float4 *>(stg + rr * 128 + ((j4 ^ (rr & 7)) << 4));
-                            if (gr < 0) continue;
-                            if constexpr (decltype(slots)::value)
-                                __stcs(reinterpret_cast<float4 *>(ws.dq_part + gr * DQK + c * 32 + j4 * 4), x);
-                            else
-                                tc::red_add_v4(ws.dq_acc + gr * DQK + c * 32 + j4 * 4, x.x, x.y, x.z, x.w);
+                    for (int k = 0; k < 8; ++k) {
+                        const int rr = k * 4 + (lane >> 3), j4 = lane & 7;
+                        const int64_t gr = __shfl_sync(0xffffffffu, grow, rr);
+                        const float4 x = *reinterpret_cast<const float4 *>(stg + rr * 128 + ((j4 ^ (rr & 7)) << 4));
+                        if constexpr (kMode == kDqSlots) {
+                            if (gr >= 0) __stcs(reinterpret_cast<float4 *>(ws.dq_part + gr * DQK + c * 32 + j4 * 4), x);
+                        } else {
+                            if (gr >= 0) tc::red_add_v4(ws.dq_acc + gr * DQK + c * 32 + j4 * 4, x.x, x.y, x.z, x.w);
                         }
-                        __syncwarp();
                     }
-                };
-                if (g.dq_slots) drain(std::true_type{});
-                else drain(std::false_type{});
+                    __syncwarp();
+                }
                 tc::tc_fence_before();
                 tc::mbar_arrive(&bars[B_DQ_FREE]);
             }
@@ -602,8 +600,8 @@ static cudaError_t launch_tc_t(const Geometry &g, const Workspace &ws, const sag
         !tmap_2d(&mdo, io.attention_out_grad, kFp16, 128, (uint64_t)g.t1 * g.n1, box_rows) ||
         !tmap_3d(&mv, io.value, kFp16, 128, g.n2, g.t2, nk))
         return cudaErrorInvalidValue;
-    // the warp-issued MMA schedule when dS is stored (see the MMA role)
-    auto fn = (det && !g.dq_slots) ? k_bwd_tc<kFp16, DQK, true> : k_bwd_tc<kFp16, DQK, false>;
+    auto fn = !det ? k_bwd_tc<kFp16, DQK, kDqRed>
+              : g.dq_slots ? k_bwd_tc<kFp16, DQK, kDqSlots> : k_bwd_tc<kFp16, DQK, kDqStoreDs>;
     const int smem = Smem<DQK>::TOTAL;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

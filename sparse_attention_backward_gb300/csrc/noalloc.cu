@@ -57,3 +57,12 @@ extern "C" sag_status sel_attn_grad_noalloc(const sag_desc *desc, const void *qu
     return sel_attn_grad(desc, query, key, value, attention_out, attention_out_grad, softmax_max,
                          softmax_sum, topk_indices, dq, dk, dv, scratch, kScratchBytes, stream);
 }
+
+extern "C" sag_status sel_attn_grad_noalloc_query_error(void *stream) {
+    sag::DeviceGuard dg;
+    if (!dg.bind(static_cast<cudaStream_t>(stream))) return SAG_ERR_CUDA;
+    void *scratch = nullptr;
+    const sag_status st = scratch_for_current_device(&scratch);
+    if (st != SAG_OK) return st;
+    return sel_attn_grad_query_error(scratch, stream);
+}

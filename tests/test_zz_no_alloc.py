@@ -71,6 +71,29 @@ def test_noalloc_matches_workspace_entry_point(deterministic):
             S.assert_close(f"call {call} {name}", S.f64(g), S.f64(r))
 
 
+def test_noalloc_reports_out_of_range_ids():
+    """An id past the batch's blocks is skipped and reported; the status is
+    read back from the fixed scratch, and a clean call clears it."""
+    lib = sab.load()
+    f = _entry(lib)
+    q_err = lib.sel_attn_grad_noalloc_query_error
+    q_err.argtypes = [ctypes.c_void_p]
+    q_err.restype = ctypes.c_int
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    w = synth.WORKLOADS[0]
+    ins = _inputs(w, dev, 303)
+    bad = ins[7].clone()
+    bad[3, 0, 1] = 10 ** 6
+    outs = [torch.empty_like(t) for t in (ins[0], ins[1], ins[2])]
+    desc = _desc(w, False)
+    for topk, want in ((bad, sab.SAG_ERR_INDEX), (ins[7], sab.SAG_OK)):
+        st = f(ctypes.byref(desc), *[t.data_ptr() for t in ins[:7]], topk.data_ptr(),
+               *[t.data_ptr() for t in outs], stream.cuda_stream)
+        assert st == sab.SAG_OK, sab.status_string(st)
+        assert q_err(stream.cuda_stream) == want
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     lib = sab.load()
     f = _entry(lib)
