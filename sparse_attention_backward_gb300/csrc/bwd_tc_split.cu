@@ -27,6 +27,11 @@ namespace sag {
 namespace {
 
 constexpr int kMeta = 4;            // depth of the tile-metadata ring
+// Warps: 0 lead producer, 1 MMA, 2-5 softmax, 6-9 epilogue, 10-11 loaders
+// (12 warps: three per SM sub-partition, so 168 registers a thread fit)
+constexpr int kLoaders = 3;
+constexpr int kLoaderWarp1 = 10;
+constexpr int kSplitThreads = (kLoaderWarp1 + kLoaders - 1) * 32;
 
 // TMEM columns (512 allocated)
 constexpr uint32_t kColS = 0, kColDP = 64, kColDV = 128, kColDKlo = 192, kColDKhi = 256, kColDQ = 320;
@@ -48,7 +53,8 @@ struct Smem {
     static constexpr int OFF_STG = OFF_DS + 16384;       // 4 epilogue warps x 4 KB
     static constexpr int OFF_META = OFF_STG + 16384;     // kMeta x 128 ints
     static constexpr int OFF_RING = OFF_META + kMeta * kRows * 4;   // kURing unit ids
-    static constexpr int OFF_BAR = OFF_RING + 64;
+    static constexpr int OFF_LENT = OFF_RING + 64;                   // kLoaders x 128 ints
+    static constexpr int OFF_BAR = OFF_LENT + kLoaders * kRows * 4;
     static constexpr int TOTAL = OFF_BAR + 512 + 1024;   // + slack for 1024-B alignment
 };
 
@@ -63,8 +69,8 @@ enum Bar {
     B_DS_FREE, B_MMA_DONE, B_DQ_FREE, B_ACC_FULL, B_ACC_FREE, B_DRAIN, B_U_FULL, B_U_EMPTY = B_U_FULL + kURing,
     B_COUNT = B_U_EMPTY + kURing
 };
-// warps that read the unit ring: MMA, 4 softmax, 4 epilogue
-constexpr int kRingReaders = 9;
+// warps that read the unit ring: MMA, 4 softmax, 4 epilogue, the other loaders
+constexpr int kRingReaders = 9 + kLoaders - 1;
 
 struct TcArgs {
     Geometry g;
@@ -75,7 +81,7 @@ struct TcArgs {
 };
 
 template <bool kFp16, int DQK>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kSplitThreads, 1)
     k_bwd_tc_split(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
              const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
              const __grid_constant__ CUtensorMap map_qr, const __grid_constant__ CUtensorMap map_kr, TcArgs A) {
@@ -110,8 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init(&bars[B_KV_FULL], 1);
         tc::mbar_init(&bars[B_KV_EMPTY], 1);
         for (int s = 0; s < 2; ++s) {
-            for (int c = 0; c < 3; ++c) tc::mbar_init(&bars[B_Q_FULL + s * 3 + c], 1);
-            for (int c = 0; c < 2; ++c) tc::mbar_init(&bars[B_DO_FULL + s * 2 + c], 1);
+            for (int c = 0; c < 3; ++c) tc::mbar_init(&bars[B_Q_FULL + s * 3 + c], kLoaders);
+            for (int c = 0; c < 2; ++c) tc::mbar_init(&bars[B_DO_FULL + s * 2 + c], kLoaders);
             tc::mbar_init(&bars[B_Q_EMPTY0 + s], 1);
             tc::mbar_init(&bars[B_DO_EMPTY0 + s], 1);
         }
@@ -136,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows of a Q / dY tile no token fills (when G does not divide 128) must
     // hold finite values: zero the staging buffers once
     if (tpt * G < kRows) {
-        for (int i = threadIdx.x; i < (2 * L::Q_STAGE + DOS * L::DO_STAGE) / 16; i += kThreads)
+        for (int i = threadIdx.x; i < (2 * L::Q_STAGE + DOS * L::DO_STAGE) / 16; i += kSplitThreads)
             reinterpret_cast<uint4 *>(smem + L::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
         tc::fence_proxy_async_smem();
     }
@@ -157,9 +163,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // larger than cold ones: a static split would leave SMs idle)
     const UnitRing ring{reinterpret_cast<int64_t *>(smem + L::OFF_RING), &bars[B_U_FULL], &bars[B_U_EMPTY]};
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+    if (warp == 0 || warp >= kLoaderWarp1) {
+        // ------------------------------------------------------ TMA producers
+        // kLoaders warps share each tile's query-side loads: one warp issues a
+        // gather4 (or a token box) about every 70 cycles, which alone would
+        // bound the small-group tiles.  Warp 0 leads: it takes the units from
+        // the ticket counter, loads the K / V tile and writes the tile's
+        // metadata; every loader arms each Q / dY barrier with its own bytes.
+        const int lq = warp == 0 ? 0 : warp - kLoaderWarp1 + 1;
+        const bool lead = lq == 0;
+        if (lead && lane == 0) {
             tc::prefetch_tmap(&map_q);
             if (rope) {
                 tc::prefetch_tmap(&map_qr);
@@ -171,114 +184,106 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int oob_row = g.t1 * g.n1;   // out of range: the TMA fills zeros
         // small groups: one box per token would be a single row, so rows are
-        // fetched four at a time (tile::gather4) instead; lane k then covers
-        // tile rows 4k..4k+3, otherwise tokens k, k+32, ...
+        // fetched four at a time (tile::gather4): a load is (plane, group of 4
+        // rows); otherwise (plane, token).  Load idx of a stage goes to loader
+        // idx % kLoaders.
         const bool gather = G <= 4 && 4 % G == 0;
-        auto tok_of = [&](int j) { return gather ? (4 * lane + j) / G : lane + 32 * j; };
-        // bucket entries of this lane's tokens in tile i (-1: no token)
-        auto fetch = [&](const KeyTile &kt, int i, int (&e)[4]) {
-            const int nt = min(tpt, kt.ntok - i * tpt);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int tk = tok_of(j);
-                e[j] = tk < nt ? ws.entries[kt.e0 + i * tpt + tk] : -1;
-            }
+        const int per_plane = gather ? kRows / 4 : tpt;
+        const uint32_t load_bytes = gather ? 4 * 128 : (uint32_t)G * 128;
+        auto my_bytes = [&](int c) {
+            const int first = ((lq - c * per_plane) % kLoaders + kLoaders) % kLoaders;
+            return first < per_plane ? (uint32_t)((per_plane - 1 - first) / kLoaders + 1) * load_bytes : 0u;
         };
-        // gather rows; rows past the last token re-read the first token's row
-        // (their P and dS are 0)
-        auto gather_rows = [&](const KeyTile &kt, const int (&e)[4], int (&y)[4]) {
-            const int e_first = __shfl_sync(0xffffffffu, e[0], 0);
+        int *ent = reinterpret_cast<int *>(smem + L::OFF_LENT) + lq * kRows;   // this warp's copy of the tile's entries
+        // the loads of `planes` 64-column planes of a stage: destination plane c
+        // at dst + 16 KB c, barrier bar0 + c
+        auto issue = [&](const KeyTile &kt, int planes, uint8_t *dst, uint64_t *bar0, bool is_q) {
+            for (int idx = lq + kLoaders * lane; idx < planes * per_plane; idx += kLoaders * 32) {
+                const int c = idx / per_plane, x = idx % per_plane;
+                const CUtensorMap *mp = is_q ? qmap(c) : &map_do;
+                const int col = is_q ? cx(c) : c * 64;
+                if (gather) {
+                    // rows past the last token re-read the first token's row (their P and dS are 0)
+                    int y[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                y[j] = ((e[j] >= 0 ? e[j] : e_first) / g.block_count) * g.n1 + kt.n2 * G + (4 * lane + j) % G;
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = 4 * x + e, en = ent[r / G];
+                        y[e] = ((en >= 0 ? en : ent[0]) / g.block_count) * g.n1 + kt.n2 * G + r % G;
+                    }
+                    tc::tma_gather4(dst + c * 16384 + x * 512, mp, col, y[0], y[1], y[2], y[3], bar0 + c);
+                } else {
+                    const int y = ent[x] >= 0 ? (ent[x] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
+                    tc::tma_load_2d(dst + c * 16384 + x * G * 128, mp, col, y, bar0 + c);
+                }
+            }
         };
         int ne = 0, tc_i = 0;
         uint32_t armed_kv = 0, armed_q[2] = {0, 0}, armed_do[2] = {0, 0};
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            const int64_t ti = ring_take(ring, &ws.hdr->work_counter, k, abort_flag, lane);
+            const int64_t ti = lead ? ring_take(ring, &ws.hdr->work_counter, k, abort_flag, lane)
+                                    : ring_read(ring, k, abort_flag, lane);
             if (ti < 0) { ok = false; break; }
             if (ti >= g.n_units) break;
             const KeyTile kt = decode(g, ws, ti, nk, tpt);
             if (kt.ntok == 0) continue;
-            if (ne > 0 && !tc::mbar_wait(&bars[B_KV_EMPTY], (ne - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-            ++armed_kv;
-            if (lane == 0) {
-                tc::mbar_arrive_expect_tx(&bars[B_KV_FULL], (uint32_t)nk * (DQK + DV) * 2);
-                for (int c = 0; c < KC; ++c)
-                    tc::tma_load_3d(smem + L::OFF_K + c * 8192, kmap(c), cx(c), kt.n2, (int)kt.key0, &bars[B_KV_FULL]);
-                for (int c = 0; c < 2; ++c)
-                    tc::tma_load_3d(smem + L::OFF_V + c * 8192, &map_v, c * 64, kt.n2, (int)kt.key0, &bars[B_KV_FULL]);
-            }
-            for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
-                const int s = tc_i & 1;
-                int e[4];
-                fetch(kt, i, e);
-                if (tc_i >= 2 && !tc::mbar_wait(&bars[B_Q_EMPTY0 + s], ((tc_i >> 1) - 1) & 1, abort_flag, kWaitNs)) {
+            if (lead) {
+                if (ne > 0 && !__all_sync(0xffffffffu, tc::mbar_wait(&bars[B_KV_EMPTY], (ne - 1) & 1, abort_flag,
+                                                                       kWaitNs))) {
                     ok = false;
                     break;
                 }
-                int *m = meta + (tc_i % kMeta) * kRows;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int tk = tok_of(j);
-                    if (tk < tpt && (!gather || (4 * lane + j) % G == 0)) m[tk] = e[j];
+                ++armed_kv;
+                if (lane == 0) {
+                    tc::mbar_arrive_expect_tx(&bars[B_KV_FULL], (uint32_t)nk * (DQK + DV) * 2);
+                    for (int c = 0; c < KC; ++c)
+                        tc::tma_load_3d(smem + L::OFF_K + c * 8192, kmap(c), cx(c), kt.n2, (int)kt.key0,
+                                        &bars[B_KV_FULL]);
+                    for (int c = 0; c < 2; ++c)
+                        tc::tma_load_3d(smem + L::OFF_V + c * 8192, &map_v, c * 64, kt.n2, (int)kt.key0,
+                                        &bars[B_KV_FULL]);
                 }
+            }
+            for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
+                const int s = tc_i & 1;
+                const int nt = min(tpt, kt.ntok - i * tpt);
+                // the tile's bucket entries (-1 past the last token), read
+                // before waiting for the stage
+                for (int tt = lane; tt < tpt; tt += 32) ent[tt] = tt < nt ? ws.entries[kt.e0 + i * tpt + tt] : -1;
                 __syncwarp();
+                if (tc_i >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(&bars[B_Q_EMPTY0 + s], ((tc_i >> 1) - 1) & 1,
+                                                                          abort_flag, kWaitNs))) {
+                    ok = false;
+                    break;
+                }
+                if (lead) {
+                    int *m = meta + (tc_i % kMeta) * kRows;
+                    for (int tt = lane; tt < tpt; tt += 32) m[tt] = ent[tt];
+                    __syncwarp();
+                }
                 ++armed_q[s];
                 if (lane == 0)
-                    for (int c = 0; c < KC; ++c)
-                        tc::mbar_arrive_expect_tx(&bars[B_Q_FULL + s * 3 + c], (uint32_t)tpt * G * 64 * 2);
+                    for (int c = 0; c < KC; ++c) tc::mbar_arrive_expect_tx(&bars[B_Q_FULL + s * 3 + c], my_bytes(c));
                 __syncwarp();
-                uint8_t *qdst = smem + L::OFF_Q + s * L::Q_STAGE;
-                int y4[4];
-                if (gather) {
-                    gather_rows(kt, e, y4);
-                    for (int c = 0; c < KC; ++c)
-                        tc::tma_gather4(qdst + c * 16384 + lane * 512, qmap(c), cx(c), y4[0], y4[1], y4[2], y4[3],
-                                        &bars[B_Q_FULL + s * 3 + c]);
-                } else {
-                    for (int c = 0; c < KC; ++c)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int tk = tok_of(j);
-                            if (tk >= tpt) continue;
-                            const int y = e[j] >= 0 ? (e[j] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
-                            tc::tma_load_2d(qdst + c * 16384 + tk * G * 128, qmap(c), cx(c), y,
-                                            &bars[B_Q_FULL + s * 3 + c]);
-                        }
-                }
+                issue(kt, KC, smem + L::OFF_Q + s * L::Q_STAGE, &bars[B_Q_FULL + s * 3], true);
                 const int d = tc_i % DOS;
                 if (tc_i >= DOS &&
-                    !tc::mbar_wait(&bars[B_DO_EMPTY0 + d], ((tc_i / DOS) - 1) & 1, abort_flag, kWaitNs)) {
+                    !__all_sync(0xffffffffu, tc::mbar_wait(&bars[B_DO_EMPTY0 + d], ((tc_i / DOS) - 1) & 1, abort_flag,
+                                                           kWaitNs))) {
                     ok = false;
                     break;
                 }
                 ++armed_do[d];
                 if (lane == 0)
-                    for (int c = 0; c < 2; ++c)
-                        tc::mbar_arrive_expect_tx(&bars[B_DO_FULL + d * 2 + c], (uint32_t)tpt * G * 64 * 2);
+                    for (int c = 0; c < 2; ++c) tc::mbar_arrive_expect_tx(&bars[B_DO_FULL + d * 2 + c], my_bytes(c));
                 __syncwarp();
-                uint8_t *ddst = smem + L::OFF_DO + d * L::DO_STAGE;
-                if (gather) {
-                    for (int c = 0; c < 2; ++c)
-                        tc::tma_gather4(ddst + c * 16384 + lane * 512, &map_do, c * 64, y4[0], y4[1], y4[2], y4[3],
-                                        &bars[B_DO_FULL + d * 2 + c]);
-                } else {
-                    for (int c = 0; c < 2; ++c)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int tk = tok_of(j);
-                            if (tk >= tpt) continue;
-                            const int y = e[j] >= 0 ? (e[j] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
-                            tc::tma_load_2d(ddst + c * 16384 + tk * G * 128, &map_do, c * 64, y,
-                                            &bars[B_DO_FULL + d * 2 + c]);
-                        }
-                }
+                issue(kt, 2, smem + L::OFF_DO + d * L::DO_STAGE, &bars[B_DO_FULL + d * 2], false);
+                // the entries copy is rewritten for the next tile
+                __syncwarp();
             }
             ++ne;
         }
-        if (!ok) fail();
+        if (!ok && lane == 0) fail();
         // let every load this warp issued land before the CTA exits
         bool drained = tc::drain_armed(&bars[B_KV_FULL], armed_kv, kWaitNs);
         for (int i = 0; i < 2; ++i) {
@@ -681,7 +686,7 @@ static cudaError_t launch_tc_t(const Geometry &g, const Workspace &ws, const sag
     if (grid < 1) grid = 1;
     // the launch's CTAs take their units from this counter
     if ((e = cudaMemsetAsync(&ws.hdr->work_counter, 0, sizeof(ws.hdr->work_counter), s)) != cudaSuccess) return e;
-    fn<<<(int)grid, kThreads, smem, s>>>(m.q, mdo, m.k, mv, m.qr, m.kr, a);
+    fn<<<(int)grid, kSplitThreads, smem, s>>>(m.q, mdo, m.k, mv, m.qr, m.kr, a);
     return cudaGetLastError();
 }
 
