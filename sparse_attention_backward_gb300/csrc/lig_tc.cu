@@ -33,7 +33,11 @@ namespace {
 constexpr int kLiD = 128;            // head dim
 constexpr int kLiChunk = 128;        // gathered keys per chunk (MMA M)
 constexpr int kLiHeads = 64;         // heads per unit, padded (MMA N)
-constexpr int kLiThreads = 320;
+// warps: 0 lead producer, 1 MMA, 2-5 relu / dW, 6-9 epilogue, 10 second key
+// loader (a warp issues one tile::gather4 about every 66 cycles: one warp
+// alone would spend ~4k cycles per chunk on the key rows)
+constexpr int kLiLoader2 = 10;
+constexpr int kLiThreads = (kLiLoader2 + 1) * 32;
 
 // TMEM columns: S^T stages, dK stages, dQ^T buffers (512 allocated)
 constexpr uint32_t kLiColS = 0, kLiColDK = 128, kLiColDQ = 384;
@@ -127,9 +131,10 @@ __global__ void __launch_bounds__(kLiThreads, 1)
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         for (int i = 0; i < L_COUNT; ++i) {
+            const bool two_loaders = i >= L_K_FULL0 && i < L_K_FULL0 + kLiKStages;
             const bool from_threads = i == L_R_FULL0 || i == L_R_FULL1 || i == L_DK_FREE0 || i == L_DK_FREE1 ||
                                       i == L_DQ_FREE0 || i == L_DQ_FREE1;
-            tc::mbar_init(&bars[i], from_threads ? 128 : 1);
+            tc::mbar_init(&bars[i], from_threads ? 128 : two_loaders ? 2 : 1);
         }
         tc::fence_mbar_init();
     }
@@ -160,9 +165,14 @@ __global__ void __launch_bounds__(kLiThreads, 1)
         return t < ws.q_end[b];
     };
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+    if (warp == 0 || warp == kLiLoader2) {
+        // ------------------------------------------------------ TMA producers
+        // Warp 0 loads the query tile and weights of each unit and the first
+        // 64 dims of every gathered key row; warp 10 the other 64 dims.  Each
+        // arms the key-stage barrier with its own bytes.
+        const bool lead = warp == 0;
+        const int h = lead ? 0 : 1;
+        if (lead && lane == 0) {
             tc::prefetch_tmap(&map_q);
             tc::prefetch_tmap(&map_k);
         }
@@ -174,21 +184,23 @@ __global__ void __launch_bounds__(kLiThreads, 1)
             if (!unit(u, t, n2, b)) continue;
             const LiUnit lu = li_unit(A, t, n2, b);
             const int qs = uu & 1;
-            if (uu >= 2 && !tc::mbar_wait(&bars[L_Q_EMPTY0 + qs], ((uu >> 1) - 1) & 1, abort_flag, kWaitNs)) {
-                ok = false;
-                break;
-            }
-            // the unit's weights (0 past G) for the relu warps; the arrive below
-            // publishes them with the query tile
-            for (int h = lane; h < kLiHeads; h += 32)
-                wbuf[qs * kLiHeads + h] = h < G ? u16_to_f<kFp16>(A.w[(int64_t)t * g.n1 + n2 * G + h]) : 0.f;
-            __syncwarp();
-            ++armed_q[qs];
-            if (lane == 0) {
-                tc::mbar_arrive_expect_tx(&bars[L_Q_FULL0 + qs], (uint32_t)G * kLiD * 2);
-                for (int c = 0; c < 2; ++c)
-                    tc::tma_load_2d(smem + L::OFF_Q + qs * L::Q_STAGE + c * (L::Q_STAGE / 2), &map_q, c * 64,
-                                    t * g.n1 + n2 * G, &bars[L_Q_FULL0 + qs]);
+            if (lead) {
+                if (uu >= 2 && !tc::mbar_wait(&bars[L_Q_EMPTY0 + qs], ((uu >> 1) - 1) & 1, abort_flag, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                // the unit's weights (0 past G) for the relu warps; the arrive below
+                // publishes them with the query tile
+                for (int hh = lane; hh < kLiHeads; hh += 32)
+                    wbuf[qs * kLiHeads + hh] = hh < G ? u16_to_f<kFp16>(A.w[(int64_t)t * g.n1 + n2 * G + hh]) : 0.f;
+                __syncwarp();
+                ++armed_q[qs];
+                if (lane == 0) {
+                    tc::mbar_arrive_expect_tx(&bars[L_Q_FULL0 + qs], (uint32_t)G * kLiD * 2);
+                    for (int c = 0; c < 2; ++c)
+                        tc::tma_load_2d(smem + L::OFF_Q + qs * L::Q_STAGE + c * (L::Q_STAGE / 2), &map_q, c * 64,
+                                        t * g.n1 + n2 * G, &bars[L_Q_FULL0 + qs]);
+                }
             }
             for (int c = 0; c < A.nchunks; ++c, ++kc) {
                 const int ks = kc % kLiKStages;
@@ -206,16 +218,15 @@ __global__ void __launch_bounds__(kLiThreads, 1)
                     break;
                 }
                 ++armed_k[ks];
-                if (lane == 0) tc::mbar_arrive_expect_tx(&bars[L_K_FULL0 + ks], (uint32_t)kLiChunk * kLiD * 2);
+                if (lane == 0) tc::mbar_arrive_expect_tx(&bars[L_K_FULL0 + ks], (uint32_t)kLiChunk * 64 * 2);
                 __syncwarp();
                 uint8_t *kdst = smem + L::OFF_K + ks * L::K_STAGE;
-                for (int h = 0; h < 2; ++h)
-                    tc::tma_gather4(kdst + h * (L::K_STAGE / 2) + lane * 512, &map_k, h * 64, y[0], y[1], y[2], y[3],
-                                    &bars[L_K_FULL0 + ks]);
+                tc::tma_gather4(kdst + h * (L::K_STAGE / 2) + lane * 512, &map_k, h * 64, y[0], y[1], y[2], y[3],
+                                &bars[L_K_FULL0 + ks]);
             }
             ++uu;
         }
-        if (!ok) fail();
+        if (!ok && lane == 0) fail();
         bool drained = true;
         for (int i = 0; i < 2; ++i) drained = tc::drain_armed(&bars[L_Q_FULL0 + i], armed_q[i], kWaitNs) && drained;
         for (int i = 0; i < kLiKStages; ++i)
