@@ -218,16 +218,19 @@ constexpr int kSortCap = 16384;
 
 // The steps of stage k whose strides are < kSortCap, on one chunk of the
 // bucket held in shared memory (keys[0 .. len) real, the rest +infinity).
+// Each thread takes compare-exchange pairs q (lower index i, upper l), p2 / 2
+// of them per step: i keeps bit j clear (l = i + j), or for the mirror step i
+// is in the lower half of its k-block (l = i ^ (k - 1)).
 __device__ __forceinline__ void sort_steps_smem(int32_t *keys, int p2, int k_lo, int k_hi, bool mirror_first) {
     for (int k = k_lo; k <= k_hi; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
             const bool mirror = mirror_first && j == (k >> 1);
-            for (int i = threadIdx.x; i < p2; i += blockDim.x) {
-                const int l = mirror ? (i ^ (k - 1)) : (i ^ j);
-                if (l > i) {
-                    const int32_t x = keys[i], y = keys[l];
-                    if (x > y) { keys[i] = y; keys[l] = x; }
-                }
+            const int lj = __ffs(j) - 1;   // j = 2^lj (for the mirror step also k / 2)
+            for (int q = threadIdx.x; q < (p2 >> 1); q += blockDim.x) {
+                const int i = ((q >> lj) << (lj + 1)) + (q & (j - 1));
+                const int l = mirror ? (i ^ (k - 1)) : (i + j);
+                const int32_t x = keys[i], y = keys[l];
+                if (x > y) { keys[i] = y; keys[l] = x; }
             }
             __syncthreads();
         }
@@ -277,12 +280,11 @@ __device__ void sort_large_bucket(int32_t *a, int n, int32_t *keys) {
         for (int c = 0; c < nchunks; ++c) {
             chunk_load(keys, a, n, c);
             for (int j = kSortCap >> 1; j > 0; j >>= 1) {
-                for (int i = threadIdx.x; i < kSortCap; i += blockDim.x) {
-                    const int l = i ^ j;
-                    if (l > i) {
-                        const int32_t x = keys[i], y = keys[l];
-                        if (x > y) { keys[i] = y; keys[l] = x; }
-                    }
+                const int lj = __ffs(j) - 1;
+                for (int q = threadIdx.x; q < (kSortCap >> 1); q += blockDim.x) {
+                    const int i = ((q >> lj) << (lj + 1)) + (q & (j - 1)), l = i + j;
+                    const int32_t x = keys[i], y = keys[l];
+                    if (x > y) { keys[i] = y; keys[l] = x; }
                 }
                 __syncthreads();
             }
