@@ -92,9 +92,17 @@ def host_cpu() -> str:
     return f"Arm CPU implementer {impl} part {part}" if impl else "unknown CPU"
 
 
-def kernel_source_hash() -> str:
+# The sources a profiled kernel is built from: its translation unit, the
+# shared device headers and the C ABI header.
+KERNEL_SOURCES = {"main": "bwd_tc.cu", "forward": "fwd_tc.cu"}
+
+
+def kernel_source_hash(kernel: str = "main") -> str:
+    csrc = os.path.join(ROOT, "sparse_attention_backward_gb300", "csrc")
+    files = [os.path.join(csrc, KERNEL_SOURCES[kernel])] + sorted(glob.glob(os.path.join(csrc, "*.cuh")))
+    files.append(os.path.join(ROOT, "include", "selattn.h"))
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "sparse_attention_backward_gb300", "csrc", "*"))):
+    for p in files:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -103,7 +111,7 @@ def kernel_source_hash() -> str:
 def profiled_traffic(workload: str, det: bool, mode: str = ""):
     """DRAM bytes per launch of the main kernel (per call of both forward
     passes with mode "forward") from a committed ncu summary, used only while
-    the kernel sources are unchanged since the capture."""
+    that kernel's sources are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -111,7 +119,7 @@ def profiled_traffic(workload: str, det: bool, mode: str = ""):
         d = json.load(f)
     key = f"{workload}:{mode or ('deterministic' if det else 'default')}"
     e = d.get(key)
-    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+    if not e or e.get("kernel_source_hash") != kernel_source_hash("forward" if mode == "forward" else "main"):
         return None
     return e.get("dram_bytes_per_launch")
 
