@@ -16,7 +16,9 @@
 //
 // Warp roles as in the backward: 0 TMA producer (K / V per key tile, Q per
 // query tile, three Q stages), 1 MMA issuer and TMEM owner, 2-5 softmax
-// (thread = query row = TMEM lane), 6-9 O drain (pass 2).
+// (thread = query row = TMEM lane), 6-9 O drain (pass 2), 10 second Q loader
+// (odd 64-column planes: one warp issues a tile::gather4 about every 66
+// cycles, so a single warp would bound the small-group tiles).
 #include "kernels.cuh"
 #include "tc.cuh"
 #include "tile.cuh"
@@ -26,6 +28,8 @@ namespace sag {
 namespace {
 
 constexpr int kQStages = 3;
+constexpr int kFwdLoader2 = 10;
+constexpr int kFwdThreads = (kFwdLoader2 + 1) * 32;
 constexpr int kMetaF = 8;                    // tile-metadata ring depth
 constexpr uint32_t kColS = 0, kColO = 128;   // TMEM columns (256 allocated)
 
@@ -65,7 +69,7 @@ __device__ __forceinline__ void atomic_max_f32(float *addr, float v) {
 }
 
 template <bool kFp16, int DQK, int PASS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
              const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_qr,
              const __grid_constant__ CUtensorMap map_kr, FwdArgs A) {
@@ -98,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init(&bars[F_KV_FULL], 1);
         tc::mbar_init(&bars[F_KV_EMPTY], 1);
         for (int s = 0; s < kQStages; ++s) {
-            tc::mbar_init(&bars[F_Q_FULL + s], 1);
+            tc::mbar_init(&bars[F_Q_FULL + s], 2);   // the two Q loaders
             tc::mbar_init(&bars[F_Q_EMPTY + s], 1);
         }
         tc::mbar_init(&bars[F_S_FULL], 1);
@@ -111,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows of a Q tile no token fills (when G does not divide 128) must hold
     // finite values: zero the stages once
     if (tpt * G < kRows) {
-        for (int i = threadIdx.x; i < kQStages * L::Q_STAGE / 16; i += kThreads)
+        for (int i = threadIdx.x; i < kQStages * L::Q_STAGE / 16; i += kFwdThreads)
             reinterpret_cast<uint4 *>(smem + L::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
         tc::fence_proxy_async_smem();
     }
@@ -129,9 +133,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         raise_error(&ws.hdr->error, SAG_ERR_TIMEOUT);
     };
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+    if (warp == 0 || warp == kFwdLoader2) {
+        // ------------------------------------------------------ TMA producers
+        // Warp 0 loads K / V, writes the tile metadata and the even 64-column
+        // planes of each Q tile; warp 10 the odd planes.  Each arms the Q
+        // stage barrier (two arrivals) with its own bytes.
+        const bool lead = warp == 0;
+        const int lq = lead ? 0 : 1;
+        if (lead && lane == 0) {
             tc::prefetch_tmap(&map_q);
             tc::prefetch_tmap(&map_k);
             if (rope) {
@@ -142,65 +151,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int oob_row = g.t1 * g.n1;   // out of range: the TMA fills zeros
         const bool gather = G <= 4 && 4 % G == 0;
+        const int my_planes = (KC - lq + 1) / 2;   // planes lq, lq + 2, ...
         int ne = 0, tc_i = 0;
         uint32_t armed_kv = 0, armed_q[kQStages] = {};
         bool ok = true;
         for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
             const KeyTile kt = decode(g, ws, ti, nk, tpt);
             if (kt.ntok == 0) continue;
-            if (ne > 0 && !tc::mbar_wait(&bars[F_KV_EMPTY], (ne - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-            ++armed_kv;
-            if (lane == 0) {
-                tc::mbar_arrive_expect_tx(&bars[F_KV_FULL], (uint32_t)nk * (DQK + (PASS == 2 ? DV : 0)) * 2);
-                for (int c = 0; c < KC; ++c)
-                    tc::tma_load_3d(smem + L::OFF_K + c * 8192, kmap(c), cx(c), kt.n2, (int)kt.key0, &bars[F_KV_FULL]);
-                if (PASS == 2)
-                    for (int c = 0; c < 2; ++c)
-                        tc::tma_load_3d(smem + L::OFF_V + c * 8192, &map_v, c * 64, kt.n2, (int)kt.key0,
-                                        &bars[F_KV_FULL]);
-            }
-            for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
-                const int s = tc_i % kQStages, use = tc_i / kQStages;
-                if (use > 0 && !tc::mbar_wait(&bars[F_Q_EMPTY + s], (use - 1) & 1, abort_flag, kWaitNs)) {
+            if (lead) {
+                if (ne > 0 && !__all_sync(0xffffffffu, tc::mbar_wait(&bars[F_KV_EMPTY], (ne - 1) & 1, abort_flag,
+                                                                       kWaitNs))) {
                     ok = false;
                     break;
                 }
+                ++armed_kv;
+                if (lane == 0) {
+                    tc::mbar_arrive_expect_tx(&bars[F_KV_FULL], (uint32_t)nk * (DQK + (PASS == 2 ? DV : 0)) * 2);
+                    for (int c = 0; c < KC; ++c)
+                        tc::tma_load_3d(smem + L::OFF_K + c * 8192, kmap(c), cx(c), kt.n2, (int)kt.key0,
+                                        &bars[F_KV_FULL]);
+                    if (PASS == 2)
+                        for (int c = 0; c < 2; ++c)
+                            tc::tma_load_3d(smem + L::OFF_V + c * 8192, &map_v, c * 64, kt.n2, (int)kt.key0,
+                                            &bars[F_KV_FULL]);
+                }
+            }
+            for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
+                const int s = tc_i % kQStages, use = tc_i / kQStages;
                 const int nt = min(tpt, kt.ntok - i * tpt);
-                int *m = meta + (tc_i % kMetaF) * kRows;
-                for (int tt = lane; tt < tpt; tt += 32) m[tt] = tt < nt ? ws.entries[kt.e0 + i * tpt + tt] : -1;
-                __syncwarp();
+                // this lane's tokens: gather rows 4 lane .. 4 lane + 3 (rows past
+                // the last token re-read the first token's row, their P is 0),
+                // else tokens lane, lane + 32, ...
+                int ent[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int tk = gather ? (4 * lane + j) / G : lane + 32 * j;
+                    ent[j] = tk < nt ? ws.entries[kt.e0 + i * tpt + tk] : (gather ? ws.entries[kt.e0 + i * tpt] : -1);
+                }
+                if (use > 0 && !__all_sync(0xffffffffu, tc::mbar_wait(&bars[F_Q_EMPTY + s], (use - 1) & 1, abort_flag,
+                                                                       kWaitNs))) {
+                    ok = false;
+                    break;
+                }
+                if (lead) {
+                    int *m = meta + (tc_i % kMetaF) * kRows;
+                    for (int tt = lane; tt < tpt; tt += 32) m[tt] = tt < nt ? ws.entries[kt.e0 + i * tpt + tt] : -1;
+                    __syncwarp();
+                }
                 ++armed_q[s];
-                if (lane == 0) tc::mbar_arrive_expect_tx(&bars[F_Q_FULL + s], (uint32_t)tpt * G * DQK * 2);
+                if (lane == 0)
+                    tc::mbar_arrive_expect_tx(&bars[F_Q_FULL + s], (uint32_t)my_planes * tpt * G * 128);
                 __syncwarp();
                 uint8_t *qdst = smem + L::OFF_Q + s * L::Q_STAGE;
                 if (gather) {
-                    // G in {1, 2, 4}: lane k fetches tile rows 4k..4k+3 with one gather4 per chunk;
-                    // rows past the last token re-read the first token's row (their P is 0)
+                    // G in {1, 2, 4}: lane k fetches tile rows 4k..4k+3 with one gather4 per plane
                     int y[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const int row = 4 * lane + j, tk = row / G;
-                        y[j] = (m[tk < nt ? tk : 0] / g.block_count) * g.n1 + kt.n2 * G + row % G;
+                        const int row = 4 * lane + j;
+                        y[j] = (ent[j] / g.block_count) * g.n1 + kt.n2 * G + row % G;
                     }
-                    for (int c = 0; c < KC; ++c)
+                    for (int c = lq; c < KC; c += 2)
                         tc::tma_gather4(qdst + c * 16384 + lane * 512, qmap(c), cx(c), y[0], y[1], y[2], y[3],
                                         &bars[F_Q_FULL + s]);
                 } else {
-                    // one (token, chunk) box per lane: the issue is spread over the warp
-                    for (int j = lane; j < tpt * KC; j += 32) {
-                        const int tt = j / KC, c = j % KC;
-                        const int y = tt < nt ? (m[tt] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
-                        tc::tma_load_2d(qdst + c * 16384 + tt * G * 128, qmap(c), cx(c), y, &bars[F_Q_FULL + s]);
+                    // one (token, plane) box per load, tokens over the lanes
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int tt = lane + 32 * j;
+                        if (tt >= tpt) break;
+                        const int y = ent[j] >= 0 ? (ent[j] / g.block_count) * g.n1 + kt.n2 * G : oob_row;
+                        for (int c = lq; c < KC; c += 2)
+                            tc::tma_load_2d(qdst + c * 16384 + tt * G * 128, qmap(c), cx(c), y, &bars[F_Q_FULL + s]);
                     }
                 }
             }
             ++ne;
         }
-        if (!ok) fail();
+        if (!ok && lane == 0) fail();
         // let every load this warp issued land before the CTA exits
         bool drained = tc::drain_armed(&bars[F_KV_FULL], armed_kv, kWaitNs);
         for (int i = 0; i < kQStages; ++i) drained = tc::drain_armed(&bars[F_Q_FULL + i], armed_q[i], kWaitNs) && drained;
-        if (!drained) fail();
+        if (!drained && lane == 0) fail();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -433,7 +465,7 @@ cudaError_t launch_fwd_t(const Geometry &g, const Workspace &ws, const sag_io &i
     if (e != cudaSuccess) return e;
     int64_t grid = g.n_units < num_sms ? g.n_units : num_sms;
     if (grid < 1) grid = 1;
-    fn<<<(int)grid, kThreads, smem, s>>>(m.q, m.k, mv, m.qr, m.kr, a);
+    fn<<<(int)grid, kFwdThreads, smem, s>>>(m.q, m.k, mv, m.qr, m.kr, a);
     return cudaGetLastError();
 }
 
