@@ -138,53 +138,58 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = tc::idesc_f16(128, A.n_pad, !kFp16, true, false);
-            int it = 0, np = 0;
-            bool ok = true;
-            for (int64_t cp = blockIdx.x; cp < npairs && ok; cp += gridDim.x, ++np) {
-                const int t = g.tok_lo + (int)(cp / g.n2), n2 = (int)(cp % g.n2);
-                const int64_t pair = (int64_t)t * g.n2 + n2;
-                const int b = batch_of(ws.cu_q, g.batch, t);
-                const int nblk = t < ws.q_end[b] ? ws.kv_blocks[b] : 0;   // ids must be below; none for padding
-                const int ab = np & 1;
-                if (np >= 2 && !tc::mbar_wait(&bars[D_ACC_FREE0 + ab], ((np >> 1) - 1) & 1, abort_flag, kDqWaitNs)) {
+        // The whole warp runs the schedule; one elected lane issues each
+        // instruction (a pair is 8-16 small MMAs per slot: the issue rate
+        // matters).
+        const uint32_t idesc = tc::idesc_f16(128, A.n_pad, !kFp16, true, false);
+        auto wait = [&](int b, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, tc::mbar_wait(&bars[b], parity, abort_flag, kDqWaitNs));
+        };
+        int it = 0, np = 0;
+        bool ok = true;
+        for (int64_t cp = blockIdx.x; cp < npairs && ok; cp += gridDim.x, ++np) {
+            const int t = g.tok_lo + (int)(cp / g.n2), n2 = (int)(cp % g.n2);
+            const int64_t pair = (int64_t)t * g.n2 + n2;
+            const int b = batch_of(ws.cu_q, g.batch, t);
+            const int nblk = t < ws.q_end[b] ? ws.kv_blocks[b] : 0;   // ids must be below; none for padding
+            const int ab = np & 1;
+            if (np >= 2 && !wait(D_ACC_FREE0 + ab, ((np >> 1) - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            bool first = true;
+            for (int slot = 0; slot < g.block_count; ++slot) {
+                if (!slot_ok(g, ws, A.topk, pair, slot, nblk)) continue;
+                const int s = it % kStages;
+                if (!wait(D_FULL0 + s, (it / kStages) & 1)) {
                     ok = false;
                     break;
                 }
-                bool first = true;
-                for (int slot = 0; slot < g.block_count; ++slot) {
-                    if (!slot_ok(g, ws, A.topk, pair, slot, nblk)) continue;
-                    const int s = it % kStages;
-                    if (!tc::mbar_wait(&bars[D_FULL0 + s], (it / kStages) & 1, abort_flag, kDqWaitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::tc_fence_after();
-                    const uint32_t kst = tc::smem_u32(smem + s * L::STAGE);
-                    const uint32_t dst = kst + L::K_BYTES;
-                    for (int kk = 0; kk < BS / 16; ++kk) {
-                        // A = K^T (dims x keys, MN-major), B = dS^T (keys x G, K-major)
-                        const uint64_t bdesc = tc::sw128_desc(dst + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024);
-                        tc::mma_f16_ss(tmem + acc_col(ab, 0), tc::sw128_desc(kst + kk * 2048, BS * 128, 1024), bdesc,
-                                       idesc, !first || kk > 0);
-                        if (DQK == 192)
-                            tc::mma_f16_ss(tmem + acc_col(ab, 1),
-                                           tc::sw128_desc(kst + BS * 128 + kk * 2048, BS * 128, 1024), bdesc, idesc,
-                                           !first || kk > 0);
-                    }
-                    tc::mma_commit(&bars[D_EMPTY0 + s]);
-                    first = false;
-                    ++it;
+                tc::tc_fence_after();
+                const uint32_t kst = tc::smem_u32(smem + s * L::STAGE);
+                const uint32_t dst = kst + L::K_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BS / 16; ++kk) {
+                    // A = K^T (dims x keys, MN-major), B = dS^T (keys x G, K-major)
+                    const uint64_t bdesc = tc::sw128_desc(dst + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024);
+                    tc::mma_f16_ss_warp(tmem + acc_col(ab, 0), tc::sw128_desc(kst + kk * 2048, BS * 128, 1024), bdesc,
+                                        idesc, !first || kk > 0);
+                    if (DQK == 192)
+                        tc::mma_f16_ss_warp(tmem + acc_col(ab, 1),
+                                            tc::sw128_desc(kst + BS * 128 + kk * 2048, BS * 128, 1024), bdesc, idesc,
+                                            !first || kk > 0);
                 }
-                if (!ok) break;
-                tc::mma_commit(&bars[D_ACC_FULL0 + ab]);
+                tc::mma_commit_warp(&bars[D_EMPTY0 + s]);
+                first = false;
+                ++it;
             }
-            if (!ok) fail();
-            // every MMA issued must be complete before TMEM is freed
-            tc::mma_commit(&bars[D_DRAIN]);
-            if (!tc::mbar_wait_drain(&bars[D_DRAIN], 0, kDqWaitNs)) fail();
+            if (!ok) break;
+            tc::mma_commit_warp(&bars[D_ACC_FULL0 + ab]);
         }
+        if (!ok && lane == 0) fail();
+        // every MMA issued must be complete before TMEM is freed
+        tc::mma_commit_warp(&bars[D_DRAIN]);
+        if (!__all_sync(0xffffffffu, tc::mbar_wait_drain(&bars[D_DRAIN], 0, kDqWaitNs)) && lane == 0) fail();
     } else {
         // ------------------------------------------------------ epilogue
         const int q4 = warp & 3;
