@@ -30,6 +30,9 @@ struct DqSmem {
     static constexpr int STAGE = K_BYTES + DS_BYTES;
     static constexpr int OFF_BAR = kStages * STAGE;
     static constexpr int TOTAL = OFF_BAR + 256 + 1024;
+    // two CTAs per SM where their shared memory fits (64-key blocks): two
+    // MMA warps then issue the pass's small MMAs side by side
+    static constexpr int CTAS_PER_SM = 2 * (TOTAL + 1024) <= 227 * 1024 ? 2 : 1;
 };
 
 enum DqBar { D_FULL0 = 0, D_EMPTY0 = kStages, D_ACC_FULL0 = 2 * kStages, D_ACC_FREE0 = 2 * kStages + 2,
@@ -50,7 +53,7 @@ __device__ __forceinline__ bool slot_ok(const Geometry &g, const Workspace &ws, 
 }
 
 template <bool kFp16, int DQK, int BS>
-__global__ void __launch_bounds__(kDqThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, DqSmem<DQK, BS>::CTAS_PER_SM)
     k_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_ds,
             const __grid_constant__ CUtensorMap map_kr, DqArgs A) {
     using L = DqSmem<DQK, BS>;
@@ -267,7 +270,8 @@ static cudaError_t launch_dq_tc_t(const Geometry &g, const Workspace &ws, const 
     const int smem = DqSmem<DQK, BS>::TOTAL;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int64_t grid = npairs < num_sms ? npairs : num_sms;
+    const int64_t slots = (int64_t)num_sms * DqSmem<DQK, BS>::CTAS_PER_SM;
+    const int64_t grid = npairs < slots ? npairs : slots;
     fn<<<(int)grid, kDqThreads, smem, s>>>(mk, mds, mkr, a);
     return cudaGetLastError();
 }
