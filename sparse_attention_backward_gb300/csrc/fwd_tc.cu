@@ -235,53 +235,56 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!drained && lane == 0) fail();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const bool bf16 = !kFp16;
-            const uint32_t id_s = tc::idesc_f16(kRows, nk, bf16, false, false);
-            const uint32_t id_o = tc::idesc_f16(kRows, DV, bf16, false, true);
-            const uint32_t ks = sbase + L::OFF_K, vs = sbase + L::OFF_V, ps = sbase + L::OFF_P;
-            int ne = 0, tc_i = 0;
-            bool ok = true;
-            for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
-                const KeyTile kt = decode(g, ws, ti, nk, tpt);
-                if (kt.ntok == 0) continue;
-                if (!tc::mbar_wait(&bars[F_KV_FULL], ne & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
-                    const int s = tc_i % kQStages, use = tc_i / kQStages;
-                    if (!tc::mbar_wait(&bars[F_Q_FULL + s], use & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                    tc::tc_fence_after();
-                    const uint32_t qs = sbase + L::OFF_Q + s * L::Q_STAGE;
-                    // S = Q K^T (both operands K-major)
-                    for (int kk = 0; kk < DQK / 16; ++kk)
-                        tc::mma_f16_ss(tmem + kColS, tc::sw128_desc(qs + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                                       tc::sw128_desc(ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
-                    tc::mma_commit(&bars[F_S_FULL]);
-                    // the softmax is done with S (and its tile's metadata)
-                    if (!tc::mbar_wait(&bars[F_P_FULL], tc_i & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                    tc::tc_fence_after();
-                    tc::mma_commit(&bars[F_Q_EMPTY + s]);
-                    if (PASS == 2) {
-                        // O = P V (A: P K-major, B: V tile MN-major, N = Dv)
-                        if (tc_i > 0 && !tc::mbar_wait(&bars[F_O_FREE], (tc_i - 1) & 1, abort_flag, kWaitNs)) {
-                            ok = false;
-                            break;
-                        }
-                        tc::tc_fence_after();
-                        for (int kk = 0; kk < nk / 16; ++kk)
-                            tc::mma_f16_ss(tmem + kColO, tc::sw128_desc(ps + kk * 32, 16, 1024),
-                                           tc::sw128_desc(vs + kk * 2048, 8192, 1024), id_o, kk > 0);
-                        tc::mma_commit(&bars[F_O_DONE]);
+        // The whole warp runs the schedule; one elected lane issues each
+        // instruction.
+        const bool bf16 = !kFp16;
+        const uint32_t id_s = tc::idesc_f16(kRows, nk, bf16, false, false);
+        const uint32_t id_o = tc::idesc_f16(kRows, DV, bf16, false, true);
+        const uint32_t ks = sbase + L::OFF_K, vs = sbase + L::OFF_V, ps = sbase + L::OFF_P;
+        auto wait = [&](int b, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, tc::mbar_wait(&bars[b], parity, abort_flag, kWaitNs));
+        };
+        int ne = 0, tc_i = 0;
+        bool ok = true;
+        for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
+            const KeyTile kt = decode(g, ws, ti, nk, tpt);
+            if (kt.ntok == 0) continue;
+            if (!wait(F_KV_FULL, ne & 1)) { ok = false; break; }
+            for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
+                const int s = tc_i % kQStages, use = tc_i / kQStages;
+                if (!wait(F_Q_FULL + s, use & 1)) { ok = false; break; }
+                tc::tc_fence_after();
+                const uint32_t qs = sbase + L::OFF_Q + s * L::Q_STAGE;
+                // S = Q K^T (both operands K-major)
+                for (int kk = 0; kk < DQK / 16; ++kk)
+                    tc::mma_f16_ss_warp(tmem + kColS, tc::sw128_desc(qs + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                                        tc::sw128_desc(ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+                tc::mma_commit_warp(&bars[F_S_FULL]);
+                // the softmax is done with S (and its tile's metadata)
+                if (!wait(F_P_FULL, tc_i & 1)) { ok = false; break; }
+                tc::tc_fence_after();
+                tc::mma_commit_warp(&bars[F_Q_EMPTY + s]);
+                if (PASS == 2) {
+                    // O = P V (A: P K-major, B: V tile MN-major, N = Dv)
+                    if (tc_i > 0 && !wait(F_O_FREE, (tc_i - 1) & 1)) {
+                        ok = false;
+                        break;
                     }
+                    tc::tc_fence_after();
+                    for (int kk = 0; kk < nk / 16; ++kk)
+                        tc::mma_f16_ss_warp(tmem + kColO, tc::sw128_desc(ps + kk * 32, 16, 1024),
+                                            tc::sw128_desc(vs + kk * 2048, 8192, 1024), id_o, kk > 0);
+                    tc::mma_commit_warp(&bars[F_O_DONE]);
                 }
-                if (!ok) break;
-                tc::mma_commit(&bars[F_KV_EMPTY]);
-                ++ne;
             }
-            if (!ok) fail();
-            // every MMA issued must be complete before TMEM is freed
-            tc::mma_commit(&bars[F_DRAIN]);
-            if (!tc::mbar_wait_drain(&bars[F_DRAIN], 0, kWaitNs)) fail();
+            if (!ok) break;
+            tc::mma_commit_warp(&bars[F_KV_EMPTY]);
+            ++ne;
         }
+        if (!ok && lane == 0) fail();
+        // every MMA issued must be complete before TMEM is freed
+        tc::mma_commit_warp(&bars[F_DRAIN]);
+        if (!__all_sync(0xffffffffu, tc::mbar_wait_drain(&bars[F_DRAIN], 0, kWaitNs)) && lane == 0) fail();
     } else if (warp < 6) {
         // ------------------------------------------------------ softmax
         const int q4 = warp & 3;
