@@ -21,17 +21,21 @@ constexpr int kDqThreads = 192;
 constexpr int kStages = 3;
 constexpr uint64_t kDqWaitNs = 2000000000ull;
 
-template <int DQK, int BS>
+// A stage holds 64 keys of one selected block (a 128-key block takes two
+// stages): the key rows, KC chunks of 64 rows x 128 B, and the dS plane of
+// those keys, up to 32 rows x 128 B.
+constexpr int kSub = 64;
+
+template <int DQK>
 struct DqSmem {
     static constexpr int KC = DQK / 64;
-    static constexpr int K_BYTES = KC * BS * 128;          // K block: KC chunks of BS rows x 128 B
-    static constexpr int DS_CHUNKS = BS / 64;
-    static constexpr int DS_BYTES = DS_CHUNKS * 32 * 128;  // dS tile: chunks of 32 rows x 128 B
+    static constexpr int K_BYTES = KC * kSub * 128;
+    static constexpr int DS_BYTES = 32 * 128;
     static constexpr int STAGE = K_BYTES + DS_BYTES;
     static constexpr int OFF_BAR = kStages * STAGE;
     static constexpr int TOTAL = OFF_BAR + 256 + 1024;
-    // two CTAs per SM where their shared memory fits (64-key blocks): two
-    // MMA warps then issue the pass's small MMAs side by side
+    // two CTAs per SM (their shared memory fits): two MMA warps then issue
+    // the pass's small MMAs side by side
     static constexpr int CTAS_PER_SM = 2 * (TOTAL + 1024) <= 227 * 1024 ? 2 : 1;
 };
 
@@ -53,11 +57,12 @@ __device__ __forceinline__ bool slot_ok(const Geometry &g, const Workspace &ws, 
 }
 
 template <bool kFp16, int DQK, int BS>
-__global__ void __launch_bounds__(kDqThreads, DqSmem<DQK, BS>::CTAS_PER_SM)
+__global__ void __launch_bounds__(kDqThreads, DqSmem<DQK>::CTAS_PER_SM)
     k_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_ds,
             const __grid_constant__ CUtensorMap map_kr, DqArgs A) {
-    using L = DqSmem<DQK, BS>;
+    using L = DqSmem<DQK>;
     constexpr int KC = L::KC;
+    constexpr int kSubs = BS / kSub;   // stages per selected block
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
@@ -111,26 +116,27 @@ __global__ void __launch_bounds__(kDqThreads, DqSmem<DQK, BS>::CTAS_PER_SM)
                 const int64_t pair = (int64_t)t * g.n2 + n2;
                 const int b = batch_of(ws.cu_q, g.batch, t);
                 const int nblk = t < ws.q_end[b] ? ws.kv_blocks[b] : 0;   // ids must be below; none for padding
-                for (int slot = 0; slot < g.block_count; ++slot) {
+                for (int slot = 0; slot < g.block_count && ok; ++slot) {
                     if (!slot_ok(g, ws, A.topk, pair, slot, nblk)) continue;
-                    const int s = it % kStages;
-                    if (it >= kStages &&
-                        !tc::mbar_wait(&bars[D_EMPTY0 + s], ((it / kStages) - 1) & 1, abort_flag, kDqWaitNs)) {
-                        ok = false;
-                        break;
-                    }
                     const int id = __ldg(A.topk + pair * g.block_count + slot);
-                    const int key0 = ws.cu_kv[b] + id * BS;
-                    uint8_t *st = smem + s * L::STAGE;
-                    ++armed[s];
-                    tc::mbar_arrive_expect_tx(&bars[D_FULL0 + s], (uint32_t)(BS * DQK * 2 + G * BS * 2));
-                    for (int c = 0; c < KC; ++c)
-                        tc::tma_load_3d(st + c * BS * 128, (g.d_rope && c == 2) ? &map_kr : &map_k,
-                                        (g.d_rope && c == 2) ? 0 : c * 64, n2, key0, &bars[D_FULL0 + s]);
                     const int dsrow = (int)(((int64_t)cp * g.block_count + slot) * G);
-                    for (int c = 0; c < L::DS_CHUNKS; ++c)
-                        tc::tma_load_2d(st + L::K_BYTES + c * 4096, &map_ds, c * 64, dsrow, &bars[D_FULL0 + s]);
-                    ++it;
+                    for (int h = 0; h < kSubs; ++h) {
+                        const int s = it % kStages;
+                        if (it >= kStages &&
+                            !tc::mbar_wait(&bars[D_EMPTY0 + s], ((it / kStages) - 1) & 1, abort_flag, kDqWaitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        const int key0 = ws.cu_kv[b] + id * BS + h * kSub;
+                        uint8_t *st = smem + s * L::STAGE;
+                        ++armed[s];
+                        tc::mbar_arrive_expect_tx(&bars[D_FULL0 + s], (uint32_t)(kSub * DQK * 2 + G * kSub * 2));
+                        for (int c = 0; c < KC; ++c)
+                            tc::tma_load_3d(st + c * kSub * 128, (g.d_rope && c == 2) ? &map_kr : &map_k,
+                                            (g.d_rope && c == 2) ? 0 : c * 64, n2, key0, &bars[D_FULL0 + s]);
+                        tc::tma_load_2d(st + L::K_BYTES, &map_ds, h * kSub, dsrow, &bars[D_FULL0 + s]);
+                        ++it;
+                    }
                 }
             }
             if (!ok) fail();
@@ -161,30 +167,32 @@ __global__ void __launch_bounds__(kDqThreads, DqSmem<DQK, BS>::CTAS_PER_SM)
                 break;
             }
             bool first = true;
-            for (int slot = 0; slot < g.block_count; ++slot) {
+            for (int slot = 0; slot < g.block_count && ok; ++slot) {
                 if (!slot_ok(g, ws, A.topk, pair, slot, nblk)) continue;
-                const int s = it % kStages;
-                if (!wait(D_FULL0 + s, (it / kStages) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc::tc_fence_after();
-                const uint32_t kst = tc::smem_u32(smem + s * L::STAGE);
-                const uint32_t dst = kst + L::K_BYTES;
+                for (int h = 0; h < kSubs; ++h) {
+                    const int s = it % kStages;
+                    if (!wait(D_FULL0 + s, (it / kStages) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint32_t kst = tc::smem_u32(smem + s * L::STAGE);
+                    const uint32_t dst = kst + L::K_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BS / 16; ++kk) {
-                    // A = K^T (dims x keys, MN-major), B = dS^T (keys x G, K-major)
-                    const uint64_t bdesc = tc::sw128_desc(dst + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024);
-                    tc::mma_f16_ss_warp(tmem + acc_col(ab, 0), tc::sw128_desc(kst + kk * 2048, BS * 128, 1024), bdesc,
-                                        idesc, !first || kk > 0);
-                    if (DQK == 192)
-                        tc::mma_f16_ss_warp(tmem + acc_col(ab, 1),
-                                            tc::sw128_desc(kst + BS * 128 + kk * 2048, BS * 128, 1024), bdesc, idesc,
-                                            !first || kk > 0);
+                    for (int kk = 0; kk < kSub / 16; ++kk) {
+                        // A = K^T (dims x keys, MN-major), B = dS^T (keys x G, K-major)
+                        const uint64_t bdesc = tc::sw128_desc(dst + kk * 32, 16, 1024);
+                        tc::mma_f16_ss_warp(tmem + acc_col(ab, 0), tc::sw128_desc(kst + kk * 2048, kSub * 128, 1024),
+                                            bdesc, idesc, !first || kk > 0);
+                        if (DQK == 192)
+                            tc::mma_f16_ss_warp(tmem + acc_col(ab, 1),
+                                                tc::sw128_desc(kst + kSub * 128 + kk * 2048, kSub * 128, 1024), bdesc,
+                                                idesc, !first || kk > 0);
+                    }
+                    tc::mma_commit_warp(&bars[D_EMPTY0 + s]);
+                    first = false;
+                    ++it;
                 }
-                tc::mma_commit_warp(&bars[D_EMPTY0 + s]);
-                first = false;
-                ++it;
             }
             if (!ok) break;
             tc::mma_commit_warp(&bars[D_ACC_FULL0 + ab]);
@@ -259,18 +267,18 @@ static cudaError_t launch_dq_tc_t(const Geometry &g, const Workspace &ws, const 
     CUtensorMap mk, mkr, mds;
     const uint64_t ds_rows = (uint64_t)npairs * g.block_count * g.group;
     const uint64_t d_main = (uint64_t)(g.d_qk - g.d_rope);
-    if (!tmap_3d(&mk, io.key, kFp16, d_main, g.n2, g.t2, BS) || !tmap_2d(&mds, ws.ds, kFp16, BS, ds_rows, g.group))
+    if (!tmap_3d(&mk, io.key, kFp16, d_main, g.n2, g.t2, kSub) || !tmap_2d(&mds, ws.ds, kFp16, BS, ds_rows, g.group))
         return cudaErrorInvalidValue;
     if (g.d_rope) {
-        if (!tmap_3d(&mkr, io.key_rope, kFp16, g.d_rope, g.n2, g.t2, BS)) return cudaErrorInvalidValue;
+        if (!tmap_3d(&mkr, io.key_rope, kFp16, g.d_rope, g.n2, g.t2, kSub)) return cudaErrorInvalidValue;
     } else {
         mkr = mk;
     }
     auto fn = k_dq_tc<kFp16, DQK, BS>;
-    const int smem = DqSmem<DQK, BS>::TOTAL;
+    const int smem = DqSmem<DQK>::TOTAL;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int64_t slots = (int64_t)num_sms * DqSmem<DQK, BS>::CTAS_PER_SM;
+    const int64_t slots = (int64_t)num_sms * DqSmem<DQK>::CTAS_PER_SM;
     const int64_t grid = npairs < slots ? npairs : slots;
     fn<<<(int)grid, kDqThreads, smem, s>>>(mk, mds, mkr, a);
     return cudaGetLastError();
