@@ -46,6 +46,15 @@ def _small_cases():
         # value head dim 192 (K and V head dims may differ)
         "dv192": base.with_(name="dv192", cu_q=(0, 40), cu_kv=(0, 384), n1=8, n2=2, d_qk=128, d_v=192,
                             block_size=64, block_count=3, scale=128 ** -0.5, seed=14),
+        # groups that do not divide a 128-row tile (126 rows used, 2 zero-filled): G = 6, and G = 3
+        # (too large for gathers of four rows, so per-token boxes of 3 rows)
+        "g6": base.with_(name="g6", cu_q=(0, 50, 97), cu_kv=(0, 256, 512), n1=12, n2=2, block_size=32,
+                         block_count=5, seed=17),
+        "g3_fp16": base.with_(name="g3_fp16", cu_q=(0, 90), cu_kv=(0, 320), n1=3, n2=1, d_qk=128, d_v=128,
+                              dtype="f16", block_size=64, block_count=3, scale=128 ** -0.5, seed=18),
+        # G = 8 with two KV heads
+        "g8": base.with_(name="g8", cu_q=(0, 70), cu_kv=(0, 512), n1=16, n2=2, block_size=64, block_count=4,
+                         seed=19),
     }
 
 
@@ -95,7 +104,7 @@ def test_token_windows_parity(small_data, name, window, monkeypatch):
 
 @pytest.mark.parametrize("deterministic", [False, True])
 @pytest.mark.parametrize("split", ["0", "1"])
-@pytest.mark.parametrize("name", ["tiny", "varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127"])
+@pytest.mark.parametrize("name", ["tiny", "varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127", "g6", "g3_fp16"])
 def test_both_tensor_core_schedules(small_data, name, split, deterministic, monkeypatch):
     """Both tensor-core schedules (softmax between the MMA groups, or split in
     two phases beside them) forced on shapes either can take, both modes."""
@@ -187,7 +196,7 @@ def test_deterministic_token_chunks(small_data, name, chunk, monkeypatch):
 
 
 @pytest.mark.parametrize("slots", ["0", "1"])
-@pytest.mark.parametrize("name", ["tiny", "varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127"])
+@pytest.mark.parametrize("name", ["tiny", "varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127", "g6", "g8"])
 def test_deterministic_dq_sources(small_data, name, slots, monkeypatch):
     """Deterministic mode with dQ summed from per-slot fp32 partials (the
     plan's choice for small blocks and groups) or from the stored dS, each
