@@ -15,7 +15,7 @@ from tests.test_parity_gpu import SMALL
 
 pytestmark = pytest.mark.gpu
 
-FWD_CASES = ["tiny", "varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127", "g6", "g3_fp16", "g8"]
+FWD_CASES = ["tiny", "varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127", "g6", "g3_fp16", "g8", "d128_bs128", "bs48"]
 
 
 def _gpu_forward(w, x):

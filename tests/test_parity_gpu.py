@@ -55,6 +55,14 @@ def _small_cases():
         # G = 8 with two KV heads
         "g8": base.with_(name="g8", cu_q=(0, 70), cu_kv=(0, 512), n1=16, n2=2, block_size=64, block_count=4,
                          seed=19),
+        # 128-key blocks with 128-wide heads; 48-key blocks (N = 48 MMAs); 96-key blocks (the CUDA-core
+        # kernel: no tensor-core tile for them)
+        "d128_bs128": base.with_(name="d128_bs128", cu_q=(0, 33, 60), cu_kv=(0, 512, 768), n1=16, n2=2,
+                                 d_qk=128, d_v=128, block_size=128, block_count=2, scale=128 ** -0.5, seed=20),
+        "bs48": base.with_(name="bs48", cu_q=(0, 64), cu_kv=(0, 480), n1=16, n2=1, block_size=48, block_count=3,
+                           seed=21),
+        "bs96": base.with_(name="bs96", cu_q=(0, 40), cu_kv=(0, 384), n1=4, n2=1, block_size=96, block_count=2,
+                           seed=22),
     }
 
 
@@ -104,7 +112,8 @@ def test_token_windows_parity(small_data, name, window, monkeypatch):
 
 @pytest.mark.parametrize("deterministic", [False, True])
 @pytest.mark.parametrize("split", ["0", "1"])
-@pytest.mark.parametrize("name", ["tiny", "varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127", "g6", "g3_fp16"])
+@pytest.mark.parametrize("name", ["tiny", "varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127", "g6", "g3_fp16",
+                                  "d128_bs128", "bs48"])
 def test_both_tensor_core_schedules(small_data, name, split, deterministic, monkeypatch):
     """Both tensor-core schedules (softmax between the MMA groups, or split in
     two phases beside them) forced on shapes either can take, both modes."""
@@ -196,7 +205,8 @@ def test_deterministic_token_chunks(small_data, name, chunk, monkeypatch):
 
 
 @pytest.mark.parametrize("slots", ["0", "1"])
-@pytest.mark.parametrize("name", ["tiny", "varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127", "g6", "g8"])
+@pytest.mark.parametrize("name", ["tiny", "varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127", "g6", "g8",
+                                  "d128_bs128", "bs48"])
 def test_deterministic_dq_sources(small_data, name, slots, monkeypatch):
     """Deterministic mode with dQ summed from per-slot fp32 partials (the
     plan's choice for small blocks and groups) or from the stored dS, each
