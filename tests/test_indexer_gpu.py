@@ -54,6 +54,25 @@ def test_indexer_full_parity_small(idx):
     _close(w.name, _run(w, x), _oracle_full(_problem(w, x)))
 
 
+@pytest.mark.parametrize("shape", [
+    # one query head per key head; 5 heads per key head; a single selection; 300 selections (three
+    # chunks, the last one ragged) in fp16 with empty slots
+    dict(name="indexer_g1", cu_q=(0, 90), cu_kv=(0, 200), n1=4, n2=4, topk=64, seed=31),
+    dict(name="indexer_g5", cu_q=(0, 37, 100), cu_kv=(0, 150, 260), n1=10, n2=2, topk=96, seed=32),
+    dict(name="indexer_topk1", cu_q=(0, 50), cu_kv=(0, 64), n1=16, n2=1, topk=1, seed=33),
+    dict(name="indexer_topk300", cu_q=(0, 40), cu_kv=(0, 512), n1=8, n2=1, topk=300, kind="f16",
+         empty_frac=0.1, seed=34),
+])
+def test_indexer_shapes(shape):
+    shape = dict(shape)
+    kind = shape.pop("kind", None)
+    if kind is not None:
+        shape["dtype"] = kind
+    w = synth.INDEXER_WORKLOADS[0].with_(**shape)
+    x = synth.make_indexer_inputs(w)
+    _close(w.name, _run(w, x), _oracle_full(_problem(w, x)))
+
+
 def test_indexer_position_selected_twice_and_two_key_heads():
     w = synth.INDEXER_WORKLOADS[0].with_(name="indexer_dup", cu_q=(0, 70, 130), cu_kv=(0, 96, 200), n1=32, n2=2,
                                          topk=40, seed=7)
