@@ -63,6 +63,11 @@ def _small_cases():
                            seed=21),
         "bs96": base.with_(name="bs96", cu_q=(0, 40), cu_kv=(0, 384), n1=4, n2=1, block_size=96, block_count=2,
                            seed=22),
+        # a single selected block per token; the largest group with the smallest blocks
+        "cnt1": base.with_(name="cnt1", cu_q=(0, 45, 100), cu_kv=(0, 128, 320), n1=16, n2=1, block_size=64,
+                           block_count=1, seed=23),
+        "g32_bs16": base.with_(name="g32_bs16", cu_q=(0, 30), cu_kv=(0, 256), n1=32, n2=1, block_size=16,
+                               block_count=6, seed=24),
     }
 
 
