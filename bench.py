@@ -92,14 +92,16 @@ def host_cpu() -> str:
     return f"Arm CPU implementer {impl} part {part}" if impl else "unknown CPU"
 
 
-# The sources a profiled kernel is built from: its translation unit, the
-# shared device headers and the C ABI header.
-KERNEL_SOURCES = {"main": "bwd_tc.cu", "forward": "fwd_tc.cu"}
+# The sources the profiled kernels are built from: their translation units,
+# the shared device headers and the C ABI header.  "main" is the main kernel
+# with in-kernel dQ reductions, "main_dq_pass" the main kernel storing dS and
+# the fixed-order dQ pass after it.
+KERNEL_SOURCES = {"main": ["bwd_tc.cu"], "main_dq_pass": ["bwd_tc.cu", "dq_tc.cu"], "forward": ["fwd_tc.cu"]}
 
 
 def kernel_source_hash(kernel: str = "main") -> str:
     csrc = os.path.join(ROOT, "sparse_attention_backward_gb300", "csrc")
-    files = [os.path.join(csrc, KERNEL_SOURCES[kernel])] + sorted(glob.glob(os.path.join(csrc, "*.cuh")))
+    files = [os.path.join(csrc, f) for f in KERNEL_SOURCES[kernel]] + sorted(glob.glob(os.path.join(csrc, "*.cuh")))
     files.append(os.path.join(ROOT, "include", "selattn.h"))
     h = hashlib.sha256()
     for p in files:
@@ -108,10 +110,11 @@ def kernel_source_hash(kernel: str = "main") -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, det: bool, mode: str = ""):
-    """DRAM bytes per launch of the main kernel (per call of both forward
-    passes with mode "forward") from a committed ncu summary, used only while
-    that kernel's sources are unchanged since the capture."""
+def profiled_traffic(workload: str, det: bool, mode: str = "", dq_path: int = 0):
+    """DRAM bytes per call of the timed kernels from a committed ncu summary:
+    the main kernel, plus the fixed-order dQ pass when the plan takes it
+    (dq_path 1), or both forward passes with mode "forward".  Used only while
+    those kernels' sources are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -119,7 +122,8 @@ def profiled_traffic(workload: str, det: bool, mode: str = ""):
         d = json.load(f)
     key = f"{workload}:{mode or ('deterministic' if det else 'default')}"
     e = d.get(key)
-    if not e or e.get("kernel_source_hash") != kernel_source_hash("forward" if mode == "forward" else "main"):
+    kernel = "forward" if mode == "forward" else ("main_dq_pass" if dq_path == 1 else "main")
+    if not e or e.get("kernels") != kernel or e.get("kernel_source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -426,7 +430,9 @@ def main():
         workloads = time_workloads(dev, stream, peak)
 
     if rank == 0:
-        traffic = profiled_traffic(w.name, args.deterministic)
+        traffic = profiled_traffic(w.name, args.deterministic, dq_path=int(info.dq_path))
+        timed_kernels = ("main backward (stores dS) + fixed-order dQ pass" if info.dq_path == 1 else
+                         "main backward (dQ slot partials) + slot sum" if info.dq_path == 2 else "main backward")
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -434,7 +440,7 @@ def main():
             "config": workload_config(w, args.deterministic),
             "pct_of_roofline": 100.0 * roofline_ms / ms,
             "roofline_ms": roofline_ms,
-            "roofline": {"bound": "tensor", "kernel": "main backward", "achieved": achieved, "peak": peak,
+            "roofline": {"bound": "tensor", "kernel": timed_kernels, "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": f"{pk_src} bf16 burst",
                          "peak_sustained": float(pk.get("bf16_tflops_sustained", peak)),
                          "frac_sustained": achieved / float(pk.get("bf16_tflops_sustained", peak)),

@@ -42,19 +42,25 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Default mode: reduce dQ with fp32 atomics inside the main kernel, or store
 // dS and form dQ by the fixed-order pass.  Bytes moved per query row:
-//   reductions: count * halves * d_qk * 4 (one fp32 partial per key tile)
+//   reductions: count * halves * d_qk * 4 (one fp32 partial per 64-key tile)
 //   dS pass:    count * bs * 2 * 2 (dS out and back) + count * bs * d_qk * 2 / G
 //               (every selected key block re-read per (token, KV head))
-// The pass is taken only when it moves less than half the reductions' bytes:
-// measured on GB300 it has overheads the count misses (token chunks, its own
-// launch).  SELATTN_DQ_PASS=0 / 1 forces either.
-bool prefer_dq_pass(const Geometry &g) {
+// For the tensor-core kernel of the larger query groups (G >= 8) the pass is
+// taken when it moves less than 2.5x the reductions' bytes counted once per
+// selected block: the 64-key tiles of a larger block reduce into the same
+// rows back to back and measure like one, and the pass's key re-reads are
+// served from L2.  Measured on GB300: 64-key blocks with G = 16 (ratio 2.33)
+// 9.93 ms with the reductions, 9.46 ms with the pass; 128-key blocks with
+// G = 32 (ratio 2.67) 953 ms against 965 ms.  Elsewhere (the split schedule of
+// the small groups, the CUDA-core kernel) it is taken only when it moves less
+// than half the reductions' bytes.  SELATTN_DQ_PASS=0 / 1 forces either.
+bool prefer_dq_pass(const Geometry &g, bool main_tc_kernel) {
     const char *env = getenv("SELATTN_DQ_PASS");
     if (env && env[0] == '0') return false;
     if (env && env[0] == '1') return true;
-    const double red = (double)g.block_count * g.halves * g.d_qk * 4;
+    const double red = (double)g.block_count * g.d_qk * 4;
     const double pass = (double)g.block_count * g.block_size * 4 + (double)g.block_count * g.block_size * g.d_qk * 2 / g.group;
-    return pass < 0.5 * red;
+    return main_tc_kernel ? pass < 2.5 * red : pass < 0.5 * red * g.halves;
 }
 
 // Fixed-order dQ from per-slot partials instead of the stored dS, per query row:
@@ -200,7 +206,7 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     // forces windows on smaller problems too).
     const char *wenv = getenv(forward ? "SELATTN_FWD_WINDOW_TOKENS" : "SELATTN_WINDOW_TOKENS");
     const int acc_cols = forward ? g.d_v : g.d_qk;
-    if (!forward && !p->det) p->ds_path = prefer_dq_pass(g);
+    if (!forward && !p->det) p->ds_path = prefer_dq_pass(g, p->use_tc && !bwd_split_preferred(g));
     p->slot_path = !forward && p->ds_path && p->use_tc && prefer_dq_slots(g);
     g.dq_slots = p->slot_path ? 1 : 0;
     g.windowed = p->use_tc && !p->ds_path &&
@@ -266,9 +272,11 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     return SAG_OK;
 }
 
-// Buckets are sorted by token where their order matters: the fixed-order dQ
-// path (deterministic accumulation, token chunks) and token windows.
-bool buckets_sorted(const Plan &p) { return p.ds_path || p.g.windowed; }
+// Buckets are sorted by token where their order matters: the deterministic
+// mode (dK / dV accumulated in a fixed order), token chunks and token windows
+// (their ranges are found by token).  The default mode's dQ pass reads dS by
+// (token, slot), whatever the order in which the main kernel wrote it.
+bool buckets_sorted(const Plan &p) { return p.det || p.n_chunks > 1 || p.g.windowed; }
 
 Workspace carve(const Plan &p, void *base) {
     char *c = static_cast<char *>(base);

@@ -61,7 +61,8 @@ struct Smem {
 
 enum Bar {
     B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL0, B_Q_FULL1, B_Q_EMPTY0, B_Q_EMPTY1, B_DO_FULL0, B_DO_FULL1,
-    B_DO_EMPTY0, B_DO_EMPTY1, B_S_FULL, B_P_FULL, B_MMA_DONE, B_DQ_FREE, B_ACC_FULL, B_ACC_FREE, B_DRAIN, B_COUNT
+    B_DO_EMPTY0, B_DO_EMPTY1, B_S_FULL, B_DP_FULL, B_P_FULL, B_DS_FULL, B_MMA_DONE, B_DQ_FREE, B_ACC_FULL, B_ACC_FREE,
+    B_DRAIN, B_COUNT
 };
 
 struct TcArgs {
@@ -102,6 +103,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     constexpr bool store_ds = kMode == kDqStoreDs;
     // the whole MMA warp runs the schedule when dS is stored (see the MMA role)
     constexpr bool kWarpIssue = kMode == kDqStoreDs;
+    // when dS is stored, the softmax forms P as soon as S has landed and dS
+    // once dP has, and dV is issued between the two; otherwise it waits for
+    // both and hands P and dS over at once
+    constexpr bool kSplitPhases = kMode == kDqStoreDs;
     const uint32_t sbase = tc::smem_u32(smem);
     // 64-column chunk c of a q / k row: the main tensor at column 64 c, or
     // with the rope split chunk 2 from the rope tensor at column 0
@@ -121,7 +126,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc::mbar_init(&bars[B_DO_EMPTY0 + s], 1);
         }
         tc::mbar_init(&bars[B_S_FULL], 1);
+        tc::mbar_init(&bars[B_DP_FULL], 1);
         tc::mbar_init(&bars[B_P_FULL], kSoftmaxWarps * 32);
+        tc::mbar_init(&bars[B_DS_FULL], kSoftmaxWarps * 32);
         tc::mbar_init(&bars[B_MMA_DONE], 1);
         tc::mbar_init(&bars[B_DQ_FREE], 128);
         tc::mbar_init(&bars[B_ACC_FULL], 1);
@@ -306,24 +313,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc::tc_fence_after();
                 const uint32_t qs = sbase + L::OFF_Q + s * L::Q_STAGE;
                 const uint32_t ds_ = sbase + L::OFF_DO + d * L::DO_STAGE;
-                // S = Q K^T, dP = dY V^T (both operands K-major); with early_s
-                // S is issued before dY has landed
+                // S = Q K^T, dP = dY V^T (both operands K-major); with split
+                // phases each is committed on its own, so the softmax forms P
+                // while dP runs; with early_s S is issued before dY has landed
                 for (int kk = 0; kk < DQK / 16; ++kk)
                     mma(tmem + kColS, tc::sw128_desc(qs + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                         tc::sw128_desc(ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+                if (kSplitPhases) commit(&bars[B_S_FULL]);
                 if (A.early_s && !wait(B_DO_FULL0 + d, (tc_i / DOS) & 1)) { ok = false; break; }
                 tc::tc_fence_after();
                 for (int kk = 0; kk < DV / 16; ++kk)
                     mma(tmem + kColDP, tc::sw128_desc(ds_ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                         tc::sw128_desc(vs + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
-                commit(&bars[B_S_FULL]);
+                commit(&bars[kSplitPhases ? B_DP_FULL : B_S_FULL]);
                 if (!wait(B_P_FULL, tc_i & 1)) { ok = false; break; }
                 tc::tc_fence_after();
-                // dV^T += dY^T P (A: dY tile MN-major, B: P MN-major)
+                // dV^T += dY^T P (A: dY tile MN-major, B: P MN-major); with
+                // split phases while the softmax forms dS
                 for (int kk = 0; kk < kRows / 16; ++kk)
                     mma(tmem + kColDV, tc::sw128_desc(ds_ + kk * 2048, 16384, 1024),
                         tc::sw128_desc(ps + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
                 commit(&bars[B_DO_EMPTY0 + d]);
+                if (kSplitPhases) {
+                    if (!wait(B_DS_FULL, tc_i & 1)) { ok = false; break; }
+                    tc::tc_fence_after();
+                }
                 // dK^T += Q^T dS, dims [0,128) and (192 wide) dims [64,192)
                 for (int kk = 0; kk < kRows / 16; ++kk)
                     mma(tmem + kColDKlo, tc::sw128_desc(qs + kk * 2048, 16384, 1024),
@@ -381,66 +395,140 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 ok = tc::mbar_wait(&bars[B_S_FULL], tc_i & 1, abort_flag, kWaitNs);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc::tc_fence_after();
-                // S and dP in two rounds of 32 keys, each round's loads in flight
-                // before one wait
-                uint32_t pk[32], dk2[32];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (32 * h >= nk) break;
-                    uint32_t sv[4][8], dv[4][8];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (32 * h + 8 * j < nk) {
-                            tc::tmem_ld8(trow + kColS + 32 * h + 8 * j, sv[j]);
-                            tc::tmem_ld8(trow + kColDP + 32 * h + 8 * j, dv[j]);
-                        }
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (32 * h + 8 * j >= nk) break;
-#pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            float p0 = 0.f, p1 = 0.f, d0 = 0.f, d1 = 0.f;
-                            if (valid) {
-                                p0 = ex2(fmaf(__uint_as_float(sv[j][e]), g.scale_log2, -lse2));
-                                p1 = ex2(fmaf(__uint_as_float(sv[j][e + 1]), g.scale_log2, -lse2));
-                                d0 = p0 * (__uint_as_float(dv[j][e]) - delta);
-                                d1 = p1 * (__uint_as_float(dv[j][e + 1]) - delta);
-                            }
-                            pk[16 * h + j * 4 + e / 2] = pack2<kFp16>(p0, p1);
-                            dk2[16 * h + j * 4 + e / 2] = pack2<kFp16>(d0, d1);
-                        }
-                    }
-                }
-                // the previous tile's MMAs must be done with the P / dS buffers
-                if (tc_i > 0) {
-                    ok = tc::mbar_wait(&bars[B_MMA_DONE], (tc_i - 1) & 1, abort_flag, kWaitNs);
-                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                }
                 uint8_t *prow = smem + L::OFF_P;
                 uint8_t *drow = smem + L::OFF_DS;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (8 * j >= nk) break;
-                    *reinterpret_cast<uint4 *>(prow + sw_off(r, j)) =
-                        make_uint4(pk[j * 4], pk[j * 4 + 1], pk[j * 4 + 2], pk[j * 4 + 3]);
-                    *reinterpret_cast<uint4 *>(drow + sw_off(r, j)) =
-                        make_uint4(dk2[j * 4], dk2[j * 4 + 1], dk2[j * 4 + 2], dk2[j * 4 + 3]);
-                }
-                if (store_ds && valid) {
+                if constexpr (kSplitPhases) {
+                    // the previous tile's MMAs must be done with the P / dS
+                    // buffers (they are: S of this tile was issued after them)
+                    if (tc_i > 0) {
+                        ok = tc::mbar_wait(&bars[B_MMA_DONE], (tc_i - 1) & 1, abort_flag, kWaitNs);
+                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    }
                     // dS[t - tok_lo][n2][slot][g][key] in the input dtype
-                    const int t = ent / g.block_count, slot = ent % g.block_count;
-                    const int64_t base =
-                        ((((int64_t)(t - g.tok_lo) * g.n2 + kt.n2) * g.block_count + slot) * G + gg) * g.block_size +
-                        kt.koff;
-                    uint4 *dst = reinterpret_cast<uint4 *>(ws.ds + base);
+                    uint4 *dst = nullptr;
+                    if (valid) {
+                        const int t = ent / g.block_count, slot = ent % g.block_count;
+                        dst = reinterpret_cast<uint4 *>(
+                            ws.ds + ((((int64_t)(t - g.tok_lo) * g.n2 + kt.n2) * g.block_count + slot) * G + gg) *
+                                        g.block_size + kt.koff);
+                    }
+                    // P from S in two rounds of 32 keys, each round's loads in
+                    // flight before one wait; P stays in fp32 for dS
+                    float pf[64];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (8 * j < nk) dst[j] = make_uint4(dk2[j * 4], dk2[j * 4 + 1], dk2[j * 4 + 2], dk2[j * 4 + 3]);
+                    for (int h = 0; h < 2; ++h) {
+                        if (32 * h >= nk) break;
+                        uint32_t sv[4][8];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (32 * h + 8 * j < nk) tc::tmem_ld8(trow + kColS + 32 * h + 8 * j, sv[j]);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (32 * h + 8 * j >= nk) break;
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int e = 0; e < 8; e += 2) {
+                                const int k = 32 * h + 8 * j + e;
+                                float p0 = 0.f, p1 = 0.f;
+                                if (valid) {
+                                    p0 = ex2(fmaf(__uint_as_float(sv[j][e]), g.scale_log2, -lse2));
+                                    p1 = ex2(fmaf(__uint_as_float(sv[j][e + 1]), g.scale_log2, -lse2));
+                                }
+                                pf[k] = p0;
+                                pf[k + 1] = p1;
+                                pk[e / 2] = pack2<kFp16>(p0, p1);
+                            }
+                            *reinterpret_cast<uint4 *>(prow + sw_off(r, 4 * h + j)) =
+                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
+                    }
+                    tc::fence_proxy_async_smem();
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(&bars[B_P_FULL]);
+                    // dS = P (dP - Delta) once dP has landed
+                    ok = tc::mbar_wait(&bars[B_DP_FULL], tc_i & 1, abort_flag, kWaitNs);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc::tc_fence_after();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (32 * h >= nk) break;
+                        uint32_t dv[4][8];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (32 * h + 8 * j < nk) tc::tmem_ld8(trow + kColDP + 32 * h + 8 * j, dv[j]);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (32 * h + 8 * j >= nk) break;
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int e = 0; e < 8; e += 2) {
+                                const int k = 32 * h + 8 * j + e;
+                                float d0 = 0.f, d1 = 0.f;
+                                if (valid) {
+                                    d0 = pf[k] * (__uint_as_float(dv[j][e]) - delta);
+                                    d1 = pf[k + 1] * (__uint_as_float(dv[j][e + 1]) - delta);
+                                }
+                                w4[e / 2] = pack2<kFp16>(d0, d1);
+                            }
+                            const uint4 v4 = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                            *reinterpret_cast<uint4 *>(drow + sw_off(r, 4 * h + j)) = v4;
+                            if (valid) dst[4 * h + j] = v4;
+                        }
+                    }
+                    tc::fence_proxy_async_smem();
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(&bars[B_DS_FULL]);
+                } else {
+                    // S and dP in two rounds of 32 keys, each round's loads in
+                    // flight before one wait
+                    uint32_t pk[32], dk2[32];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (32 * h >= nk) break;
+                        uint32_t sv[4][8], dv[4][8];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (32 * h + 8 * j < nk) {
+                                tc::tmem_ld8(trow + kColS + 32 * h + 8 * j, sv[j]);
+                                tc::tmem_ld8(trow + kColDP + 32 * h + 8 * j, dv[j]);
+                            }
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (32 * h + 8 * j >= nk) break;
+#pragma unroll
+                            for (int e = 0; e < 8; e += 2) {
+                                float p0 = 0.f, p1 = 0.f, d0 = 0.f, d1 = 0.f;
+                                if (valid) {
+                                    p0 = ex2(fmaf(__uint_as_float(sv[j][e]), g.scale_log2, -lse2));
+                                    p1 = ex2(fmaf(__uint_as_float(sv[j][e + 1]), g.scale_log2, -lse2));
+                                    d0 = p0 * (__uint_as_float(dv[j][e]) - delta);
+                                    d1 = p1 * (__uint_as_float(dv[j][e + 1]) - delta);
+                                }
+                                pk[16 * h + j * 4 + e / 2] = pack2<kFp16>(p0, p1);
+                                dk2[16 * h + j * 4 + e / 2] = pack2<kFp16>(d0, d1);
+                            }
+                        }
+                    }
+                    // the previous tile's MMAs must be done with the P / dS buffers
+                    if (tc_i > 0) {
+                        ok = tc::mbar_wait(&bars[B_MMA_DONE], (tc_i - 1) & 1, abort_flag, kWaitNs);
+                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (8 * j >= nk) break;
+                        *reinterpret_cast<uint4 *>(prow + sw_off(r, j)) =
+                            make_uint4(pk[j * 4], pk[j * 4 + 1], pk[j * 4 + 2], pk[j * 4 + 3]);
+                        *reinterpret_cast<uint4 *>(drow + sw_off(r, j)) =
+                            make_uint4(dk2[j * 4], dk2[j * 4 + 1], dk2[j * 4 + 2], dk2[j * 4 + 3]);
+                    }
+                    tc::fence_proxy_async_smem();
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(&bars[B_P_FULL]);
                 }
-                tc::fence_proxy_async_smem();
-                tc::tc_fence_before();
-                tc::mbar_arrive(&bars[B_P_FULL]);
             }
         }
         if (!ok) fail();

@@ -226,16 +226,24 @@ def test_bsnd_and_rope_descriptors(lib):
 def test_dq_path_of_the_plan(lib, monkeypatch):
     """The deterministic mode always forms dQ by a fixed-order pass: from the
     stored dS, or (small blocks and groups: the small-group workload) from
-    per-slot fp32 partials; the default mode reduces it in the main kernel on
-    the five workloads (the pass would move more bytes on each), unless
-    SELATTN_DQ_PASS forces it."""
+    per-slot fp32 partials.  The default mode takes the pass from the stored
+    dS on 64-key blocks with G = 16 (long context and the varlen case: under
+    2.5x the reductions' bytes per selected block) and reduces dQ in the main
+    kernel on the others; SELATTN_DQ_PASS forces either."""
     import synth
     for w in synth.WORKLOADS:
         for det in (False, True):
             d = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
                               sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, det)
-            want = (2 if w.name == "small_group" else 1) if det else 0
+            if det:
+                want = 2 if w.name == "small_group" else 1
+            else:
+                want = 1 if w.name in ("varlen", "long_context") else 0
             assert sab.plan_info(d).dq_path == want, (w.name, det)
+            if not det:
+                monkeypatch.setenv("SELATTN_DQ_PASS", "0")
+                assert sab.plan_info(d).dq_path == 0
+                monkeypatch.delenv("SELATTN_DQ_PASS")
     # the per-slot partials take count * halves * d_qk fp32 per query row
     w = synth.WORKLOADS[4]
     d = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
@@ -253,7 +261,8 @@ def test_dq_path_of_the_plan(lib, monkeypatch):
     w = synth.WORKLOADS[2]
     d = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale)
     info = sab.plan_info(d)
-    assert info.dq_path == 1 and info.token_chunks == 1 and info.launches == 9
+    # one token chunk: the default mode leaves the buckets unsorted
+    assert info.dq_path == 1 and info.token_chunks == 1 and info.launches == 8
 
 
 

@@ -1,6 +1,8 @@
 """Host-side legs of bench.py that need no GPU: the oracle's CPU-baseline
 timing (backward and forward) on a bounded sample, the workload description,
 the flop counts and the traffic lookup."""
+import os
+
 import pytest
 import torch
 
@@ -43,3 +45,15 @@ def test_flop_counts():
 def test_traffic_lookup_misses_unknown_keys():
     assert bench.profiled_traffic("no_such_workload", False) is None
     assert bench.profiled_traffic("long_context", False, "no_such_mode") is None
+
+
+def test_traffic_lookup_follows_the_dq_path():
+    """The long-context entries cover the main kernel storing dS and the
+    fixed-order dQ pass after it: no figure for the in-kernel reductions."""
+    import json
+    with open(os.path.join(os.path.dirname(bench.__file__), "profiles", "traffic.json")) as f:
+        e = json.load(f)["long_context:default"]
+    assert e["kernels"] == "main_dq_pass"
+    assert bench.profiled_traffic("long_context", False, dq_path=0) is None
+    got = bench.profiled_traffic("long_context", False, dq_path=1)
+    assert got is None or got == e["dram_bytes_per_launch"]

@@ -103,8 +103,10 @@ def test_full_parity_small(small_data, name, deterministic):
 @pytest.mark.parametrize("window", [37, 300])
 @pytest.mark.parametrize("name", ["varlen", "ragged_fp16", "g32_bs128", "bs16_cnt127"])
 def test_token_windows_parity(small_data, name, window, monkeypatch):
-    """Default mode with the work split into token windows (dK/dV as partials)."""
+    """Default mode with the work split into token windows (dK/dV as partials);
+    windows belong to the in-kernel dQ reductions, forced on."""
     monkeypatch.setenv("SELATTN_WINDOW_TOKENS", str(window))
+    monkeypatch.setenv("SELATTN_DQ_PASS", "0")
     w, x, (rdq, rdk, rdv) = small_data(name)
     desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
                          sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, False)
@@ -290,6 +292,21 @@ def test_default_mode_with_the_dq_pass(small_data, name, slots, monkeypatch):
     S.assert_close(f"{name} dq pass slots={slots} dq", S.f64(dq), rdq)
     S.assert_close(f"{name} dq pass slots={slots} dk", S.f64(dk), rdk)
     S.assert_close(f"{name} dq pass slots={slots} dv", S.f64(dv), rdv)
+
+
+@pytest.mark.parametrize("name", ["varlen", "bs48", "cnt1", "g32_bs16"])
+def test_default_mode_with_the_reductions(small_data, name, monkeypatch):
+    """The default mode with dQ reduced in the main kernel, forced on shapes
+    whose plan takes the fixed-order pass."""
+    monkeypatch.setenv("SELATTN_DQ_PASS", "0")
+    w, x, (rdq, rdk, rdv) = small_data(name)
+    desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
+                         sab.SAG_FP16 if w.dtype == "f16" else sab.SAG_BF16, False)
+    assert sab.plan_info(desc).dq_path == 0
+    dq, dk, dv = _run(w, x, False)
+    S.assert_close(f"{name} reductions dq", S.f64(dq), rdq)
+    S.assert_close(f"{name} reductions dk", S.f64(dk), rdk)
+    S.assert_close(f"{name} reductions dv", S.f64(dv), rdv)
 
 
 def test_bounded_wait_runs_out_and_the_context_stays_usable(small_data):
