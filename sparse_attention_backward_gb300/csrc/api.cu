@@ -46,21 +46,22 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 //   dS pass:    count * bs * 2 * 2 (dS out and back) + count * bs * d_qk * 2 / G
 //               (every selected key block re-read per (token, KV head))
 // For the tensor-core kernel of the larger query groups (G >= 8) the pass is
-// taken when it moves less than 2.5x the reductions' bytes counted once per
+// taken when it moves less than 3x the reductions' bytes counted once per
 // selected block: the 64-key tiles of a larger block reduce into the same
 // rows back to back and measure like one, and the pass's key re-reads are
-// served from L2.  Measured on GB300: 64-key blocks with G = 16 (ratio 2.33)
-// 9.93 ms with the reductions, 9.46 ms with the pass; 128-key blocks with
-// G = 32 (ratio 2.67) 953 ms against 965 ms.  Elsewhere (the split schedule of
-// the small groups, the CUDA-core kernel) it is taken only when it moves less
-// than half the reductions' bytes.  SELATTN_DQ_PASS=0 / 1 forces either.
+// served from L2.  Measured on GB300 (the main kernel storing dS with two
+// query tiles in flight): 64-key blocks with G = 16 (ratio 2.33) 9.93 ms with
+// the reductions, 9.15 ms with the pass; 128-key blocks with G = 32 (ratio
+// 2.67) 954 ms against 919 ms.  Elsewhere (the split schedule of the small
+// groups, the CUDA-core kernel) it is taken only when it moves less than half
+// the reductions' bytes.  SELATTN_DQ_PASS=0 / 1 forces either.
 bool prefer_dq_pass(const Geometry &g, bool main_tc_kernel) {
     const char *env = getenv("SELATTN_DQ_PASS");
     if (env && env[0] == '0') return false;
     if (env && env[0] == '1') return true;
     const double red = (double)g.block_count * g.d_qk * 4;
     const double pass = (double)g.block_count * g.block_size * 4 + (double)g.block_count * g.block_size * g.d_qk * 2 / g.group;
-    return main_tc_kernel ? pass < 2.5 * red : pass < 0.5 * red * g.halves;
+    return main_tc_kernel ? pass < 3.0 * red : pass < 0.5 * red * g.halves;
 }
 
 // Fixed-order dQ from per-slot partials instead of the stored dS, per query row:

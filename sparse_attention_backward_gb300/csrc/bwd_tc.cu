@@ -36,8 +36,10 @@ constexpr int kSoftmaxWarps = 4;    // one per TMEM lane quarter
 constexpr int kEpiWarp0 = 2 + kSoftmaxWarps;
 constexpr int kBwdThreads = (kEpiWarp0 + 4) * 32;
 
-// TMEM columns (512 allocated)
+// TMEM columns (512 allocated); when dS is stored the dQ columns hold a
+// second S / dP set (S at kColSet1, dP at kColSet1 + 64)
 constexpr uint32_t kColS = 0, kColDP = 64, kColDV = 128, kColDKlo = 192, kColDKhi = 256, kColDQ = 320;
+constexpr uint32_t kColSet1 = 320;
 
 template <int DQK>
 struct Smem {
@@ -61,8 +63,8 @@ struct Smem {
 
 enum Bar {
     B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL0, B_Q_FULL1, B_Q_EMPTY0, B_Q_EMPTY1, B_DO_FULL0, B_DO_FULL1,
-    B_DO_EMPTY0, B_DO_EMPTY1, B_S_FULL, B_DP_FULL, B_P_FULL, B_DS_FULL, B_MMA_DONE, B_DQ_FREE, B_ACC_FULL, B_ACC_FREE,
-    B_DRAIN, B_COUNT
+    B_DO_EMPTY0, B_DO_EMPTY1, B_S_FULL, B_S_FULL1, B_DP_FULL, B_DP_FULL1, B_P_FULL, B_P_FREE, B_DS_FULL,
+    B_MMA_DONE, B_MMA_DONE1, B_DQ_FREE, B_ACC_FULL, B_ACC_FREE, B_DRAIN, B_COUNT
 };
 
 struct TcArgs {
@@ -103,10 +105,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     constexpr bool store_ds = kMode == kDqStoreDs;
     // the whole MMA warp runs the schedule when dS is stored (see the MMA role)
     constexpr bool kWarpIssue = kMode == kDqStoreDs;
-    // when dS is stored, the softmax forms P as soon as S has landed and dS
-    // once dP has, and dV is issued between the two; otherwise it waits for
-    // both and hands P and dS over at once
-    constexpr bool kSplitPhases = kMode == kDqStoreDs;
+    // when dS is stored, two query tiles are in flight (see the MMA role);
+    // otherwise one tile at a time, P and dS handed over at once
+    constexpr bool kPipelined = kMode == kDqStoreDs;
     const uint32_t sbase = tc::smem_u32(smem);
     // 64-column chunk c of a q / k row: the main tensor at column 64 c, or
     // with the rope split chunk 2 from the rope tensor at column 0
@@ -125,11 +126,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc::mbar_init(&bars[B_DO_FULL0 + s], 1);
             tc::mbar_init(&bars[B_DO_EMPTY0 + s], 1);
         }
-        tc::mbar_init(&bars[B_S_FULL], 1);
-        tc::mbar_init(&bars[B_DP_FULL], 1);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&bars[B_S_FULL + b], 1);
+            tc::mbar_init(&bars[B_DP_FULL + b], 1);
+            tc::mbar_init(&bars[B_MMA_DONE + b], 1);
+        }
         tc::mbar_init(&bars[B_P_FULL], kSoftmaxWarps * 32);
+        tc::mbar_init(&bars[B_P_FREE], 1);
         tc::mbar_init(&bars[B_DS_FULL], kSoftmaxWarps * 32);
-        tc::mbar_init(&bars[B_MMA_DONE], 1);
         tc::mbar_init(&bars[B_DQ_FREE], 128);
         tc::mbar_init(&bars[B_ACC_FULL], 1);
         tc::mbar_init(&bars[B_ACC_FREE], 128);
@@ -298,6 +302,78 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         };
         int ne = 0, tc_i = 0;
         bool ok = true;
+        if constexpr (kPipelined) {
+            // Two query tiles in flight.  Tile t has TMEM set t & 1 for S / dP
+            // and shared tile t & 1 for P, then (once dV has read P) dS.  Per
+            // tile t: dV(t) once P(t) has landed, S(t+1), dK(t) once dS(t) has
+            // landed, dP(t+1); the softmax forms P(t+1) while dK(t) and dP(t+1)
+            // run.  Set t & 1 is free for S(t+2) once dS(t) has landed (the
+            // softmax has loaded dP(t) by then).  Tiles of one key tile only:
+            // the next key tile's K / V wait for this one's MMAs.
+            auto set_col = [](int t) { return (t & 1) ? kColSet1 : 0u; };
+            auto issue_s = [&](int t) -> bool {
+                const int st = t & 1;
+                if (!wait(B_Q_FULL0 + st, (t >> 1) & 1)) return false;
+                tc::tc_fence_after();
+                const uint32_t qs = sbase + L::OFF_Q + st * L::Q_STAGE;
+                for (int kk = 0; kk < DQK / 16; ++kk)
+                    mma(tmem + set_col(t) + kColS, tc::sw128_desc(qs + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                        tc::sw128_desc(ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+                commit(&bars[B_S_FULL + st]);
+                return true;
+            };
+            auto issue_dp = [&](int t) -> bool {
+                const int d = t % DOS;
+                if (!wait(B_DO_FULL0 + d, (t / DOS) & 1)) return false;
+                tc::tc_fence_after();
+                const uint32_t ds_ = sbase + L::OFF_DO + d * L::DO_STAGE;
+                for (int kk = 0; kk < DV / 16; ++kk)
+                    mma(tmem + set_col(t) + kColDP, tc::sw128_desc(ds_ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                        tc::sw128_desc(vs + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
+                commit(&bars[B_DP_FULL + (t & 1)]);
+                return true;
+            };
+            for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
+                const KeyTile kt = decode(g, ws, ti, nk, tpt);
+                if (kt.ntok == 0) continue;
+                if (!wait(B_KV_FULL, ne & 1)) { ok = false; break; }
+                if (ne > 0 && !wait(B_ACC_FREE, (ne - 1) & 1)) { ok = false; break; }
+                if (!issue_s(tc_i) || !issue_dp(tc_i)) { ok = false; break; }
+                for (int i = 0; i < kt.ntiles; ++i, ++tc_i) {
+                    const int s = tc_i & 1, d = tc_i % DOS;
+                    const bool more = i + 1 < kt.ntiles;
+                    const uint32_t qs = sbase + L::OFF_Q + s * L::Q_STAGE;
+                    const uint32_t ds_ = sbase + L::OFF_DO + d * L::DO_STAGE;
+                    const uint32_t pds = s ? dss : ps;
+                    if (!wait(B_P_FULL, tc_i & 1)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    // dV^T += dY^T P (A: dY tile MN-major, B: P MN-major)
+                    for (int kk = 0; kk < kRows / 16; ++kk)
+                        mma(tmem + kColDV, tc::sw128_desc(ds_ + kk * 2048, 16384, 1024),
+                            tc::sw128_desc(pds + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
+                    commit(&bars[B_P_FREE]);
+                    commit(&bars[B_DO_EMPTY0 + d]);
+                    if (more && !issue_s(tc_i + 1)) { ok = false; break; }
+                    if (!wait(B_DS_FULL, tc_i & 1)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    // dK^T += Q^T dS, dims [0,128) and (192 wide) dims [64,192)
+                    for (int kk = 0; kk < kRows / 16; ++kk)
+                        mma(tmem + kColDKlo, tc::sw128_desc(qs + kk * 2048, 16384, 1024),
+                            tc::sw128_desc(pds + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
+                    if (DQK == 192)
+                        for (int kk = 0; kk < kRows / 16; ++kk)
+                            mma(tmem + kColDKhi, tc::sw128_desc(qs + 16384 + kk * 2048, 16384, 1024),
+                                tc::sw128_desc(pds + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
+                    commit(&bars[B_Q_EMPTY0 + s]);
+                    commit(&bars[B_MMA_DONE + s]);
+                    if (more && !issue_dp(tc_i + 1)) { ok = false; break; }
+                }
+                if (!ok) break;
+                commit(&bars[B_ACC_FULL]);
+                commit(&bars[B_KV_EMPTY]);
+                ++ne;
+            }
+        } else {
         for (int64_t ti = blockIdx.x; ti < g.n_units && ok; ti += gridDim.x) {
             const KeyTile kt = decode(g, ws, ti, nk, tpt);
             if (kt.ntok == 0) continue;
@@ -313,31 +389,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc::tc_fence_after();
                 const uint32_t qs = sbase + L::OFF_Q + s * L::Q_STAGE;
                 const uint32_t ds_ = sbase + L::OFF_DO + d * L::DO_STAGE;
-                // S = Q K^T, dP = dY V^T (both operands K-major); with split
-                // phases each is committed on its own, so the softmax forms P
-                // while dP runs; with early_s S is issued before dY has landed
+                // S = Q K^T, dP = dY V^T (both operands K-major); with early_s
+                // S is issued before dY has landed
                 for (int kk = 0; kk < DQK / 16; ++kk)
                     mma(tmem + kColS, tc::sw128_desc(qs + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                         tc::sw128_desc(ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
-                if (kSplitPhases) commit(&bars[B_S_FULL]);
                 if (A.early_s && !wait(B_DO_FULL0 + d, (tc_i / DOS) & 1)) { ok = false; break; }
                 tc::tc_fence_after();
                 for (int kk = 0; kk < DV / 16; ++kk)
                     mma(tmem + kColDP, tc::sw128_desc(ds_ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                         tc::sw128_desc(vs + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0);
-                commit(&bars[kSplitPhases ? B_DP_FULL : B_S_FULL]);
+                commit(&bars[B_S_FULL]);
                 if (!wait(B_P_FULL, tc_i & 1)) { ok = false; break; }
                 tc::tc_fence_after();
-                // dV^T += dY^T P (A: dY tile MN-major, B: P MN-major); with
-                // split phases while the softmax forms dS
+                // dV^T += dY^T P (A: dY tile MN-major, B: P MN-major)
                 for (int kk = 0; kk < kRows / 16; ++kk)
                     mma(tmem + kColDV, tc::sw128_desc(ds_ + kk * 2048, 16384, 1024),
                         tc::sw128_desc(ps + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
                 commit(&bars[B_DO_EMPTY0 + d]);
-                if (kSplitPhases) {
-                    if (!wait(B_DS_FULL, tc_i & 1)) { ok = false; break; }
-                    tc::tc_fence_after();
-                }
                 // dK^T += Q^T dS, dims [0,128) and (192 wide) dims [64,192)
                 for (int kk = 0; kk < kRows / 16; ++kk)
                     mma(tmem + kColDKlo, tc::sw128_desc(qs + kk * 2048, 16384, 1024),
@@ -347,20 +416,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mma(tmem + kColDKhi, tc::sw128_desc(qs + 16384 + kk * 2048, 16384, 1024),
                             tc::sw128_desc(dss + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
                 commit(&bars[B_Q_EMPTY0 + s]);
-                if (!store_ds) {
-                    // dQ = dS K (A: dS K-major, B: K tile MN-major, N = Dqk)
-                    if (tc_i > 0 && !wait(B_DQ_FREE, (tc_i - 1) & 1)) { ok = false; break; }
-                    tc::tc_fence_after();
-                    for (int kk = 0; kk < nk / 16; ++kk)
-                        mma(tmem + kColDQ, tc::sw128_desc(dss + kk * 32, 16, 1024),
-                            tc::sw128_desc(ks + kk * 2048, 8192, 1024), id_q, kk > 0);
-                }
+                // dQ = dS K (A: dS K-major, B: K tile MN-major, N = Dqk)
+                if (tc_i > 0 && !wait(B_DQ_FREE, (tc_i - 1) & 1)) { ok = false; break; }
+                tc::tc_fence_after();
+                for (int kk = 0; kk < nk / 16; ++kk)
+                    mma(tmem + kColDQ, tc::sw128_desc(dss + kk * 32, 16, 1024),
+                        tc::sw128_desc(ks + kk * 2048, 8192, 1024), id_q, kk > 0);
                 commit(&bars[B_MMA_DONE]);
             }
             if (!ok) break;
             commit(&bars[B_ACC_FULL]);
             commit(&bars[B_KV_EMPTY]);
             ++ne;
+        }
         }
         if (!ok && lane == 0) fail();
         // every MMA issued must be complete before TMEM is freed
@@ -392,16 +460,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     lse2 = ws.lse2[grow];
                     delta = ws.delta[grow];
                 }
-                ok = tc::mbar_wait(&bars[B_S_FULL], tc_i & 1, abort_flag, kWaitNs);
+                if constexpr (kPipelined)
+                    ok = tc::mbar_wait(&bars[B_S_FULL + s], (tc_i >> 1) & 1, abort_flag, kWaitNs);
+                else
+                    ok = tc::mbar_wait(&bars[B_S_FULL], tc_i & 1, abort_flag, kWaitNs);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc::tc_fence_after();
                 uint8_t *prow = smem + L::OFF_P;
                 uint8_t *drow = smem + L::OFF_DS;
-                if constexpr (kSplitPhases) {
-                    // the previous tile's MMAs must be done with the P / dS
-                    // buffers (they are: S of this tile was issued after them)
-                    if (tc_i > 0) {
-                        ok = tc::mbar_wait(&bars[B_MMA_DONE], (tc_i - 1) & 1, abort_flag, kWaitNs);
+                if constexpr (kPipelined) {
+                    // this tile's S / dP set and shared tile (P, then dS)
+                    uint8_t *buf = s ? drow : prow;
+                    const uint32_t tset = trow + (s ? kColSet1 : 0u);
+                    // dK two tiles back must be done with the shared tile (it
+                    // is: S of this tile was issued after it)
+                    if (tc_i >= 2) {
+                        ok = tc::mbar_wait(&bars[B_MMA_DONE + s], ((tc_i >> 1) - 1) & 1, abort_flag, kWaitNs);
                         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     }
                     // dS[t - tok_lo][n2][slot][g][key] in the input dtype
@@ -421,7 +495,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         uint32_t sv[4][8];
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            if (32 * h + 8 * j < nk) tc::tmem_ld8(trow + kColS + 32 * h + 8 * j, sv[j]);
+                            if (32 * h + 8 * j < nk) tc::tmem_ld8(tset + kColS + 32 * h + 8 * j, sv[j]);
                         tc::tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -439,24 +513,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 pf[k + 1] = p1;
                                 pk[e / 2] = pack2<kFp16>(p0, p1);
                             }
-                            *reinterpret_cast<uint4 *>(prow + sw_off(r, 4 * h + j)) =
+                            *reinterpret_cast<uint4 *>(buf + sw_off(r, 4 * h + j)) =
                                 make_uint4(pk[0], pk[1], pk[2], pk[3]);
                         }
                     }
                     tc::fence_proxy_async_smem();
                     tc::tc_fence_before();
                     tc::mbar_arrive(&bars[B_P_FULL]);
-                    // dS = P (dP - Delta) once dP has landed
-                    ok = tc::mbar_wait(&bars[B_DP_FULL], tc_i & 1, abort_flag, kWaitNs);
+                    // dS = P (dP - Delta) once dP has landed and dV has read P
+                    // (dS takes P's place in the shared tile), and to the workspace
+                    ok = tc::mbar_wait(&bars[B_DP_FULL + s], (tc_i >> 1) & 1, abort_flag, kWaitNs);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     tc::tc_fence_after();
+                    // dV must be done reading P before dS overwrites it
+                    ok = tc::mbar_wait(&bars[B_P_FREE], tc_i & 1, abort_flag, kWaitNs);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         if (32 * h >= nk) break;
                         uint32_t dv[4][8];
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            if (32 * h + 8 * j < nk) tc::tmem_ld8(trow + kColDP + 32 * h + 8 * j, dv[j]);
+                            if (32 * h + 8 * j < nk) tc::tmem_ld8(tset + kColDP + 32 * h + 8 * j, dv[j]);
                         tc::tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -473,7 +551,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 w4[e / 2] = pack2<kFp16>(d0, d1);
                             }
                             const uint4 v4 = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                            *reinterpret_cast<uint4 *>(drow + sw_off(r, 4 * h + j)) = v4;
+                            *reinterpret_cast<uint4 *>(buf + sw_off(r, 4 * h + j)) = v4;
                             if (valid) dst[4 * h + j] = v4;
                         }
                     }

@@ -227,9 +227,9 @@ def test_dq_path_of_the_plan(lib, monkeypatch):
     """The deterministic mode always forms dQ by a fixed-order pass: from the
     stored dS, or (small blocks and groups: the small-group workload) from
     per-slot fp32 partials.  The default mode takes the pass from the stored
-    dS on 64-key blocks with G = 16 (long context and the varlen case: under
-    2.5x the reductions' bytes per selected block) and reduces dQ in the main
-    kernel on the others; SELATTN_DQ_PASS forces either."""
+    dS on long context, max selection and the varlen case (under 3x the
+    reductions' bytes per selected block) and reduces dQ in the main kernel
+    on the others; SELATTN_DQ_PASS forces either."""
     import synth
     for w in synth.WORKLOADS:
         for det in (False, True):
@@ -238,7 +238,7 @@ def test_dq_path_of_the_plan(lib, monkeypatch):
             if det:
                 want = 2 if w.name == "small_group" else 1
             else:
-                want = 1 if w.name in ("varlen", "long_context") else 0
+                want = 1 if w.name in ("varlen", "long_context", "max_selection") else 0
             assert sab.plan_info(d).dq_path == want, (w.name, det)
             if not det:
                 monkeypatch.setenv("SELATTN_DQ_PASS", "0")

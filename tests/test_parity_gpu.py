@@ -294,7 +294,7 @@ def test_default_mode_with_the_dq_pass(small_data, name, slots, monkeypatch):
     S.assert_close(f"{name} dq pass slots={slots} dv", S.f64(dv), rdv)
 
 
-@pytest.mark.parametrize("name", ["varlen", "bs48", "cnt1", "g32_bs16"])
+@pytest.mark.parametrize("name", ["varlen", "bs48", "cnt1", "g32_bs16", "g32_bs128", "g6"])
 def test_default_mode_with_the_reductions(small_data, name, monkeypatch):
     """The default mode with dQ reduced in the main kernel, forced on shapes
     whose plan takes the fixed-order pass."""
