@@ -16,8 +16,9 @@
 //                                                               the dQ accumulator
 // (dV = P^T dY, dK = dS^T Q / sqrt(d), dQ = dS K / sqrt(d): README function
 // description; dS = P * (dP - Delta): softmax adjoint of the dense formulas of
-// "aclnnFlashAttentionUnpaddingScoreGradV3").  In deterministic mode dQ is not
-// formed here: dS is stored and reduced in a fixed order by a second pass.
+// "aclnnFlashAttentionUnpaddingScoreGradV3").  When dQ is formed by the
+// fixed-order pass (always in deterministic mode) it is not formed here: dS
+// is stored, and two query tiles are in flight (see the MMA role).
 //
 // Warp roles (320 threads): 0 TMA producer, 1 MMA issuer and TMEM owner,
 // 2-5 softmax / dS (thread = query row = TMEM lane), 6-9 epilogue (dQ reds per
