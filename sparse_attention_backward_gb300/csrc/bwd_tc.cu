@@ -64,7 +64,7 @@ struct Smem {
 
 enum Bar {
     B_KV_FULL = 0, B_KV_EMPTY, B_Q_FULL0, B_Q_FULL1, B_Q_EMPTY0, B_Q_EMPTY1, B_DO_FULL0, B_DO_FULL1,
-    B_DO_EMPTY0, B_DO_EMPTY1, B_S_FULL, B_S_FULL1, B_DP_FULL, B_DP_FULL1, B_P_FULL, B_P_FREE, B_DS_FULL,
+    B_DO_EMPTY0, B_DO_EMPTY1, B_S_FULL, B_S_FULL1, B_DP_FULL, B_DP_FULL1, B_P_FULL, B_DS_FULL,
     B_MMA_DONE, B_MMA_DONE1, B_DQ_FREE, B_ACC_FULL, B_ACC_FREE, B_DRAIN, B_COUNT
 };
 
@@ -133,7 +133,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc::mbar_init(&bars[B_MMA_DONE + b], 1);
         }
         tc::mbar_init(&bars[B_P_FULL], kSoftmaxWarps * 32);
-        tc::mbar_init(&bars[B_P_FREE], 1);
         tc::mbar_init(&bars[B_DS_FULL], kSoftmaxWarps * 32);
         tc::mbar_init(&bars[B_DQ_FREE], 128);
         tc::mbar_init(&bars[B_ACC_FULL], 1);
@@ -305,12 +304,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         if constexpr (kPipelined) {
             // Two query tiles in flight.  Tile t has TMEM set t & 1 for S / dP
-            // and shared tile t & 1 for P, then (once dV has read P) dS.  Per
-            // tile t: dV(t) once P(t) has landed, S(t+1), dK(t) once dS(t) has
-            // landed, dP(t+1); the softmax forms P(t+1) while dK(t) and dP(t+1)
-            // run.  Set t & 1 is free for S(t+2) once dS(t) has landed (the
-            // softmax has loaded dP(t) by then).  Tiles of one key tile only:
-            // the next key tile's K / V wait for this one's MMAs.
+            // and shared tile t & 1 for P; dS has one shared tile (the dQ
+            // staging area, unused here).  Per tile t: dV(t) once P(t) has
+            // landed, S(t+1), dK(t) once dS(t) has landed, dP(t+1); the
+            // softmax forms P(t+1) while dK(t) and dP(t+1) run.  Set t & 1 is
+            // free for S(t+2) once dS(t) has landed (the softmax has loaded
+            // dP(t) by then); the dS tile is free for dS(t+1) once dP(t+1) has
+            // completed, since dK(t) was issued before it.  Tiles of one key
+            // tile only: the next key tile's K / V wait for this one's MMAs.
             auto set_col = [](int t) { return (t & 1) ? kColSet1 : 0u; };
             auto issue_s = [&](int t) -> bool {
                 const int st = t & 1;
@@ -345,14 +346,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const bool more = i + 1 < kt.ntiles;
                     const uint32_t qs = sbase + L::OFF_Q + s * L::Q_STAGE;
                     const uint32_t ds_ = sbase + L::OFF_DO + d * L::DO_STAGE;
-                    const uint32_t pds = s ? dss : ps;
+                    const uint32_t pt = s ? dss : ps, dst_s = sbase + L::OFF_STG;
                     if (!wait(B_P_FULL, tc_i & 1)) { ok = false; break; }
                     tc::tc_fence_after();
                     // dV^T += dY^T P (A: dY tile MN-major, B: P MN-major)
                     for (int kk = 0; kk < kRows / 16; ++kk)
                         mma(tmem + kColDV, tc::sw128_desc(ds_ + kk * 2048, 16384, 1024),
-                            tc::sw128_desc(pds + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
-                    commit(&bars[B_P_FREE]);
+                            tc::sw128_desc(pt + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
                     commit(&bars[B_DO_EMPTY0 + d]);
                     if (more && !issue_s(tc_i + 1)) { ok = false; break; }
                     if (!wait(B_DS_FULL, tc_i & 1)) { ok = false; break; }
@@ -360,11 +360,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     // dK^T += Q^T dS, dims [0,128) and (192 wide) dims [64,192)
                     for (int kk = 0; kk < kRows / 16; ++kk)
                         mma(tmem + kColDKlo, tc::sw128_desc(qs + kk * 2048, 16384, 1024),
-                            tc::sw128_desc(pds + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
+                            tc::sw128_desc(dst_s + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
                     if (DQK == 192)
                         for (int kk = 0; kk < kRows / 16; ++kk)
                             mma(tmem + kColDKhi, tc::sw128_desc(qs + 16384 + kk * 2048, 16384, 1024),
-                                tc::sw128_desc(pds + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
+                                tc::sw128_desc(dst_s + kk * 2048, 16384, 1024), id_t, (i > 0) || (kk > 0));
                     commit(&bars[B_Q_EMPTY0 + s]);
                     commit(&bars[B_MMA_DONE + s]);
                     if (more && !issue_dp(tc_i + 1)) { ok = false; break; }
@@ -470,11 +470,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint8_t *prow = smem + L::OFF_P;
                 uint8_t *drow = smem + L::OFF_DS;
                 if constexpr (kPipelined) {
-                    // this tile's S / dP set and shared tile (P, then dS)
+                    // this tile's S / dP set and P tile; the one dS tile
                     uint8_t *buf = s ? drow : prow;
+                    uint8_t *dsb = smem + L::OFF_STG;
                     const uint32_t tset = trow + (s ? kColSet1 : 0u);
-                    // dK two tiles back must be done with the shared tile (it
-                    // is: S of this tile was issued after it)
+                    // the MMAs two tiles back must be done with the P tile (they
+                    // are: S of this tile was issued after them)
                     if (tc_i >= 2) {
                         ok = tc::mbar_wait(&bars[B_MMA_DONE + s], ((tc_i >> 1) - 1) & 1, abort_flag, kWaitNs);
                         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -521,14 +522,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tc::fence_proxy_async_smem();
                     tc::tc_fence_before();
                     tc::mbar_arrive(&bars[B_P_FULL]);
-                    // dS = P (dP - Delta) once dP has landed and dV has read P
-                    // (dS takes P's place in the shared tile), and to the workspace
+                    // dS = P (dP - Delta) once dP has landed (dK of the previous
+                    // tile, issued before dP, is then done with the dS tile),
+                    // also to the workspace
                     ok = tc::mbar_wait(&bars[B_DP_FULL + s], (tc_i >> 1) & 1, abort_flag, kWaitNs);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     tc::tc_fence_after();
-                    // dV must be done reading P before dS overwrites it
-                    ok = tc::mbar_wait(&bars[B_P_FREE], tc_i & 1, abort_flag, kWaitNs);
-                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         if (32 * h >= nk) break;
@@ -552,7 +551,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 w4[e / 2] = pack2<kFp16>(d0, d1);
                             }
                             const uint4 v4 = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                            *reinterpret_cast<uint4 *>(buf + sw_off(r, 4 * h + j)) = v4;
+                            *reinterpret_cast<uint4 *>(dsb + sw_off(r, 4 * h + j)) = v4;
                             if (valid) dst[4 * h + j] = v4;
                         }
                     }
