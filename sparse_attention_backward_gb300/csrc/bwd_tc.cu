@@ -17,8 +17,10 @@
 // (dV = P^T dY, dK = dS^T Q / sqrt(d), dQ = dS K / sqrt(d): README function
 // description; dS = P * (dP - Delta): softmax adjoint of the dense formulas of
 // "aclnnFlashAttentionUnpaddingScoreGradV3").  When dQ is formed by the
-// fixed-order pass (always in deterministic mode) it is not formed here: dS
-// is stored, and two query tiles are in flight (see the MMA role).
+// fixed-order pass from the stored dS it is not formed here: dS is stored,
+// and two query tiles are in flight (see the MMA role).  With per-slot
+// partials each key tile's dQ tile is stored for the summing pass instead of
+// being reduced.
 //
 // Warp roles (320 threads): 0 TMA producer, 1 MMA issuer and TMEM owner,
 // 2-5 softmax / dS (thread = query row = TMEM lane), 6-9 epilogue (dQ reds per
@@ -54,9 +56,12 @@ struct Smem {
     static constexpr int OFF_V = OFF_K + K_TILE;
     static constexpr int OFF_Q = OFF_V + V_TILE;
     static constexpr int OFF_DO = OFF_Q + 2 * Q_STAGE;
+    // the P and dS tiles, or, when dS is stored, the P tiles of the two query
+    // tiles in flight
     static constexpr int OFF_P = OFF_DO + DOS * DO_STAGE;
     static constexpr int OFF_DS = OFF_P + 16384;
-    static constexpr int OFF_STG = OFF_DS + 16384;       // 4 epilogue warps x 4 KB
+    // 4 epilogue warps x 4 KB of dQ staging, or the dS tile when dS is stored
+    static constexpr int OFF_STG = OFF_DS + 16384;
     static constexpr int OFF_META = OFF_STG + 16384;     // kMeta x 128 ints
     static constexpr int OFF_BAR = OFF_META + kMeta * kRows * 4;
     static constexpr int TOTAL = OFF_BAR + 256 + 1024;   // + slack for 1024-B alignment
@@ -73,7 +78,7 @@ struct TcArgs {
     Workspace ws;
     uint16_t *dk, *dv, *dk_rope;
     int nk, halves, tpt, deterministic;
-    int early_s;            // issue S = Q K^T before dY has landed
+    int early_s;            // issue S = Q K^T before dY has landed (one tile in flight)
     int64_t n_titems;
 };
 
