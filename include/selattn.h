@@ -256,8 +256,10 @@ sag_status sel_attn_grad_plan_info(const sag_desc *desc, sag_plan_info *info);
  * sel_attn_grad with two optional cudaEvent_t handles (NULL = not recorded):
  * main_start is recorded on `stream` just before the first launch of the main
  * backward kernel and main_stop just after its last one, so a caller can time
- * the dominant kernel alone with cudaEventElapsedTime.  Arguments, ownership
- * and errors are those of sel_attn_grad.
+ * the dominant kernel alone with cudaEventElapsedTime.  When dQ is formed by
+ * the fixed-order pass (sag_plan_info.dq_path 1 or 2), the main kernel and the
+ * pass alternate per token chunk and main_stop follows the last pass.
+ * Arguments, ownership and errors are those of sel_attn_grad.
  */
 sag_status sel_attn_grad_timed(const sag_desc *desc, const void *query, const void *key,
                                const void *value, const void *attention_out,
