@@ -459,7 +459,8 @@ def time_workloads(dev, stream, peak):
     """ms per call (CUDA events, after warm-up; inputs beyond L2) of the
     long-context, max-selection and small-group workloads in both modes, with
     TFLOP/s and the fraction of the bf16 burst peak; the main kernel alone in
-    parentheses (`main_ms`).  Attention outputs and stats from the library's
+    parentheses (`main_ms`, which spans the dQ pass too when the plan's
+    `dq_path` is 1 or 2).  Attention outputs and stats from the library's
     forward."""
     import sparse_attention_backward_gb300 as sab
     out = {}
@@ -501,7 +502,8 @@ def time_workloads(dev, stream, peak):
             tf = w.flops() / (ms * 1e-3) / 1e12
             out[f"{w.name}:{'deterministic' if det else 'default'}"] = {
                 "ms": ms, "main_ms": main_ms, "tflops": tf, "frac": tf / peak,
-                "main_frac": w.flops() / (main_ms * 1e-3) / 1e12 / peak, "calls": reps}
+                "main_frac": w.flops() / (main_ms * 1e-3) / 1e12 / peak, "calls": reps,
+                "dq_path": int(sab.plan_info(desc).dq_path)}
             del ws
         del x, o, m, l, ins, outs
         torch.cuda.empty_cache()
