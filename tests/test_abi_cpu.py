@@ -287,3 +287,26 @@ def test_indexer_descriptor_validation(lib):
     assert _li_status(layout=sab.SAG_LAYOUT_BSND, s1_max=700, s2_max=700)[0] == sab.SAG_OK
     assert _li_status(layout=sab.SAG_LAYOUT_BSND, s1_max=699, s2_max=700)[0] == G
     assert _li_status(s1_max=700)[0] == G
+
+
+def test_default_dq_path_rule_by_kernel(lib):
+    """The default mode's dQ path by bytes per query row.  For the main
+    tensor-core kernel (G >= 8) the pass is taken under 3x the reductions'
+    bytes counted once per selected block; the split schedule (G <= 4) and the
+    CUDA-core kernel keep the stricter rule (under half the reductions' bytes,
+    counted per 64-key tile)."""
+    kv = dict(cu_seqlens_q=[0, 512], cu_seqlens_kv=[0, 2048])
+
+    def path(**kw):
+        return sab.plan_info(_desc(**dict(kv, **kw))).dq_path
+
+    # pass / reductions per row: 16 blocks of 64, Dqk 192
+    assert path(n1=16, n2=1, block_size=64, block_count=16) == 1     # G = 16: 28672 / 12288 = 2.33
+    assert path(n1=32, n2=1, block_size=64, block_count=16) == 1     # G = 32: 16384 / 12288 = 1.33
+    assert path(n1=8, n2=1, block_size=64, block_count=16) == 0      # G = 8: 53248 / 12288 = 4.33
+    assert path(n1=16, n2=1, block_size=128, block_count=8) == 0     # 128-key blocks, G = 16: 28672 / 6144 = 4.67
+    assert path(n1=32, n2=1, block_size=128, block_count=8) == 1     # G = 32: 16384 / 6144 = 2.67
+    # the split schedule: G = 4, 16-key blocks (ratio 2.08, which the main kernel's rule would take)
+    assert path(n1=4, n2=1, block_size=16, block_count=4) == 0
+    # the CUDA-core kernel (Dv = 192), G = 16, 64-key blocks
+    assert path(n1=16, n2=1, d_qk=128, d_v=192, block_size=64, block_count=16) == 0
