@@ -310,3 +310,15 @@ def test_default_dq_path_rule_by_kernel(lib):
     assert path(n1=4, n2=1, block_size=16, block_count=4) == 0
     # the CUDA-core kernel (Dv = 192), G = 16, 64-key blocks
     assert path(n1=16, n2=1, d_qk=128, d_v=192, block_size=64, block_count=16) == 0
+
+
+def test_default_and_deterministic_share_the_pass_workspace(lib):
+    """On a problem whose default mode takes the fixed-order pass in one token
+    chunk, both modes carve the same workspace (dS buffer, no fp32 dQ
+    accumulator); the default mode launches one kernel fewer (no bucket sort)."""
+    kw = dict(cu_seqlens_q=[0, 512], cu_seqlens_kv=[0, 2048], n1=16, n2=1, block_size=64, block_count=16)
+    d = sab.plan_info(_desc(**kw))
+    t = sab.plan_info(_desc(deterministic=True, **kw))
+    assert d.dq_path == t.dq_path == 1 and d.token_chunks == t.token_chunks == 1
+    assert d.workspace_bytes == t.workspace_bytes
+    assert d.launches + 1 == t.launches
