@@ -45,7 +45,8 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 //   reductions: count * halves * d_qk * 4 (one fp32 partial per 64-key tile)
 //   dS pass:    count * bs * 2 * 2 (dS out and back) + count * bs * d_qk * 2 / G
 //               (every selected key block re-read per (token, KV head))
-// For the tensor-core kernel of the larger query groups (G >= 8) the pass is
+// For the tensor-core kernel of the larger query groups (G >= 8), with
+// blocks of 64 or 128 keys (the tensor-core dQ pass), the pass is
 // taken when it moves less than 3x the reductions' bytes counted once per
 // selected block: the 64-key tiles of a larger block reduce into the same
 // rows back to back and measure like one, and the pass's key re-reads are
@@ -53,8 +54,9 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 // query tiles in flight): 64-key blocks with G = 16 (ratio 2.33) 9.93 ms with
 // the reductions, 9.15 ms with the pass; 128-key blocks with G = 32 (ratio
 // 2.67) 954 ms against 919 ms.  Elsewhere (the split schedule of the small
-// groups, the CUDA-core kernel) it is taken only when it moves less than half
-// the reductions' bytes.  SELATTN_DQ_PASS=0 / 1 forces either.
+// groups, the CUDA-core kernel, the CUDA-core dQ pass of other block sizes)
+// it is taken only when it moves less than half the reductions' bytes.
+// SELATTN_DQ_PASS=0 / 1 forces either.
 bool prefer_dq_pass(const Geometry &g, bool main_tc_kernel) {
     const char *env = getenv("SELATTN_DQ_PASS");
     if (env && env[0] == '0') return false;
@@ -207,7 +209,8 @@ sag_status make_plan(const sag_desc *d, Plan *p, bool forward = false) {
     // forces windows on smaller problems too).
     const char *wenv = getenv(forward ? "SELATTN_FWD_WINDOW_TOKENS" : "SELATTN_WINDOW_TOKENS");
     const int acc_cols = forward ? g.d_v : g.d_qk;
-    if (!forward && !p->det) p->ds_path = prefer_dq_pass(g, p->use_tc && !bwd_split_preferred(g));
+    if (!forward && !p->det)
+        p->ds_path = prefer_dq_pass(g, p->use_tc && !bwd_split_preferred(g) && dq_tc_supported(g));
     p->slot_path = !forward && p->ds_path && p->use_tc && prefer_dq_slots(g);
     g.dq_slots = p->slot_path ? 1 : 0;
     g.windowed = p->use_tc && !p->ds_path &&

@@ -322,3 +322,10 @@ def test_default_and_deterministic_share_the_pass_workspace(lib):
     assert d.dq_path == t.dq_path == 1 and d.token_chunks == t.token_chunks == 1
     assert d.workspace_bytes == t.workspace_bytes
     assert d.launches + 1 == t.launches
+
+
+def test_default_dq_path_rule_off_the_tensor_core_pass(lib):
+    """Block sizes the tensor-core dQ pass does not take (here 48 keys, G = 16:
+    the main kernel's rule would pick the pass) keep the stricter rule."""
+    kw = dict(cu_seqlens_q=[0, 512], cu_seqlens_kv=[0, 1536], n1=16, n2=1, block_size=48, block_count=16)
+    assert sab.plan_info(_desc(**kw)).dq_path == 0

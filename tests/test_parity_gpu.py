@@ -296,8 +296,9 @@ def test_default_mode_with_the_dq_pass(small_data, name, slots, monkeypatch):
 
 @pytest.mark.parametrize("name", ["varlen", "bs48", "cnt1", "g32_bs16", "g32_bs128", "g6"])
 def test_default_mode_with_the_reductions(small_data, name, monkeypatch):
-    """The default mode with dQ reduced in the main kernel, forced on shapes
-    whose plan takes the fixed-order pass."""
+    """The default mode with dQ reduced in the main kernel, forced; varlen,
+    cnt1 and G = 32 with 16- and 128-key blocks are shapes whose plan takes
+    the fixed-order pass."""
     monkeypatch.setenv("SELATTN_DQ_PASS", "0")
     w, x, (rdq, rdk, rdv) = small_data(name)
     desc = sab.make_desc(w.cu_q, w.cu_kv, w.n1, w.n2, w.d_qk, w.d_v, w.block_size, w.block_count, w.scale,
